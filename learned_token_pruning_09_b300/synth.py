@@ -1,0 +1,275 @@
+"""Seeded synthetic inputs for the TokenGate pruned-prefill path.
+
+This module draws random numbers and lays them out; it holds none of the
+method's arithmetic (no gate, no score transform, no selection, no RoPE, no
+attention).  Both the CUDA path and the CPU oracle take their inputs from
+here, so a workload is identical on both sides.
+
+The shapes follow the workloads the TokenGate write-ups measure on: Qwen3-1.7B
+(hidden 2048, 16 query heads, 8 KV heads, head_dim 128) at batch 1 with a long
+document followed by a short question, 16k to 128k tokens ("How does TokenGate
+perform on the benchmarks?" and the TL;DR of the MarkTechPost article).  The
+task datasets themselves (RepoBench-P, 2WikiMultihopQA, MultiNews, BioDEX,
+NIAH) are not used; these draws stand in for their shapes only.
+
+All floating-point tensors are drawn in float32 by numpy's PCG64 and encoded
+to bfloat16 by round-to-nearest-even where the path stores bf16.  bf16 arrays
+are returned as ``uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional
+
+import numpy as np
+
+BASE_SEED = 20261202
+
+# ---------------------------------------------------------------------------
+# encoding helpers (storage formats, not method arithmetic)
+# ---------------------------------------------------------------------------
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (round-to-nearest-even); return bits."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    rounding = np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))
+    return ((u + rounding) >> np.uint64(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Decode bfloat16 bit patterns to float32 (exact)."""
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _rng(seed_seq: np.random.SeedSequence) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed_seq))
+
+
+def _normal_bf16(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return f32_to_bf16_bits(x)
+
+
+# ---------------------------------------------------------------------------
+# workload description
+# ---------------------------------------------------------------------------
+
+
+@dataclass
+class Shape:
+    """Sizes of one workload (no tensors)."""
+
+    name: str
+    n_doc: List[int]          # document tokens per sequence
+    n_q: List[int]            # question tokens per sequence
+    k: List[int]              # document keep budget per sequence
+    d: int                    # hidden size of the gate-layer residual
+    h: int                    # gate MLP hidden width
+    hq: int                   # query heads
+    hkv: int                  # key/value heads
+    head_dim: int
+    n_layers: int = 1         # token-gated attention layers above the gate
+    with_proj: bool = False   # layers carry Q/K/V/O projections
+    planted: bool = False     # gate logits carry a planted needle set
+    planted_frac: float = 0.02
+    tau_fixed: Optional[float] = None
+    seed: int = BASE_SEED
+
+    @property
+    def batch(self) -> int:
+        return len(self.n_doc)
+
+    @property
+    def seqlens(self) -> List[int]:
+        return [a + b for a, b in zip(self.n_doc, self.n_q)]
+
+    @property
+    def cu_seqlens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.seqlens)]).astype(np.int32)
+
+    @property
+    def n_rows(self) -> int:
+        return int(sum(self.seqlens))
+
+    @property
+    def k_eff(self) -> List[int]:
+        return [min(k, n) for k, n in zip(self.k, self.n_doc)]
+
+    @property
+    def kept_lens(self) -> List[int]:
+        return [ke + q for ke, q in zip(self.k_eff, self.n_q)]
+
+    @property
+    def cu_kept(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.kept_lens)]).astype(np.int32)
+
+    @property
+    def n_kept(self) -> int:
+        return int(sum(self.kept_lens))
+
+
+def tiny(seed_offset: int = 0) -> Shape:
+    """Tiny case: 512 document + 32 question tokens, d=256, 4/2 heads, D=64."""
+    return Shape("tiny", [512], [32], [128], d=256, h=64, hq=4, hkv=2,
+                 head_dim=64, tau_fixed=1.1, seed=BASE_SEED + 0 + seed_offset)
+
+
+def qwen3_16k() -> Shape:
+    """Qwen3-1.7B-shaped single layer: 16,320 document + 64 question tokens."""
+    return Shape("qwen3-1.7b-16k", [16320], [64], [2048], d=2048, h=256,
+                 hq=16, hkv=8, head_dim=128, seed=BASE_SEED + 1)
+
+
+def budget_32k(k: int) -> Shape:
+    """Budget sweep at 32k: 32,704 document + 64 question tokens, planted logits."""
+    assert k in (1024, 4096, 8192)
+    return Shape(f"budget-32k-k{k}", [32704], [64], [k], d=2048, h=256,
+                 hq=16, hkv=8, head_dim=128, planted=True, seed=BASE_SEED + 2)
+
+
+def long_128k(n_layers: int = 27) -> Shape:
+    """Long context: 131,008 document + 64 question tokens, K=8192, a stack
+    of token-gated attention layers with their own projections."""
+    return Shape("long-128k", [131008], [64], [8192], d=2048, h=256, hq=16,
+                 hkv=8, head_dim=128, n_layers=n_layers, with_proj=True,
+                 seed=BASE_SEED + 3)
+
+
+def ragged_batch() -> Shape:
+    """Ragged batch of 8: document lengths U{8192..65536}, 32-128 question
+    tokens, keep fraction U[5%, 25%] per sequence (k = floor(frac * n_doc))."""
+    ss = np.random.SeedSequence(BASE_SEED + 4)
+    rng = _rng(ss.spawn(1)[0])
+    n_doc = rng.integers(8192, 65536, size=8, endpoint=True).tolist()
+    n_q = rng.integers(32, 128, size=8, endpoint=True).tolist()
+    frac = rng.uniform(0.05, 0.25, size=8)
+    k = [int(np.floor(f * n)) for f, n in zip(frac, n_doc)]
+    return Shape("ragged-8", n_doc, n_q, k, d=2048, h=256, hq=16, hkv=8,
+                 head_dim=128, seed=BASE_SEED + 4)
+
+
+def custom(name: str, n_doc, n_q, k, d=256, h=64, hq=4, hkv=2, head_dim=64,
+           seed: int = BASE_SEED + 100, **kw) -> Shape:
+    """Any other shape, for edge cases."""
+    return Shape(name, list(n_doc), list(n_q), list(k), d=d, h=h, hq=hq,
+                 hkv=hkv, head_dim=head_dim, seed=seed, **kw)
+
+
+# ---------------------------------------------------------------------------
+# draws
+# ---------------------------------------------------------------------------
+
+# sub-stream ids (stable: adding a stream never changes another's draws)
+_S_X, _S_W1, _S_W2, _S_QKV, _S_GAIN, _S_TAU, _S_PLANT, _S_SCORES, _S_LAYERS = range(9)
+
+
+def _stream(shape: Shape, sid: int) -> np.random.Generator:
+    ss = np.random.SeedSequence(entropy=shape.seed, spawn_key=(sid,))
+    return _rng(ss)
+
+
+def residuals(shape: Shape) -> np.ndarray:
+    """Gate-layer residual stream X [n_rows, d], bf16 ~ N(0, 1)."""
+    return _normal_bf16(_stream(shape, _S_X), (shape.n_rows, shape.d))
+
+
+def gate_weights(shape: Shape) -> Dict[str, object]:
+    """Gate MLP parameters d -> h -> 1.  W1 [h, d] ~ N(0, 1/d) (nn.Linear
+    layout), w2 [h] ~ N(0, 1/h); both biases zero, as the workloads state."""
+    w1 = _normal_bf16(_stream(shape, _S_W1), (shape.h, shape.d), std=1.0 / np.sqrt(shape.d))
+    w2 = _normal_bf16(_stream(shape, _S_W2), (shape.h,), std=1.0 / np.sqrt(shape.h))
+    return {"w1": w1, "w2": w2, "b1": np.zeros(shape.h, np.float32), "b2": 0.0}
+
+
+def attention_inputs(shape: Shape, n_kept: Optional[int] = None) -> Dict[str, object]:
+    """Per-layer attention inputs for the single-layer workloads:
+    q [T, hq, D], k and v [T, hkv, D], bf16 ~ N(0, 1); gain [hq] ~ U(0.5, 2);
+    tau = the workload's fixed value, else ~ U(0.9, 1.3)."""
+    t = shape.n_kept if n_kept is None else n_kept
+    r = _stream(shape, _S_QKV)
+    q = _normal_bf16(r, (t, shape.hq, shape.head_dim))
+    k = _normal_bf16(r, (t, shape.hkv, shape.head_dim))
+    v = _normal_bf16(r, (t, shape.hkv, shape.head_dim))
+    gain = _stream(shape, _S_GAIN).uniform(0.5, 2.0, size=shape.hq).astype(np.float32)
+    if shape.tau_fixed is not None:
+        tau = float(np.float32(shape.tau_fixed))
+    else:
+        tau = float(np.float32(_stream(shape, _S_TAU).uniform(0.9, 1.3)))
+    return {"q": q, "k": k, "v": v, "gain": gain, "tau": tau}
+
+
+def layer_params(shape: Shape, layer: int) -> Dict[str, object]:
+    """Projections and gate parameters of one stacked layer: W_qkv
+    [(hq+2 hkv) D, d] and W_o [d, hq D], bf16 ~ N(0, 1/fan_in); gain [hq] ~
+    U(0.5, 2); tau ~ U(0.9, 1.3)."""
+    ss = np.random.SeedSequence(entropy=shape.seed, spawn_key=(_S_LAYERS, layer))
+    r = _rng(ss)
+    n_qkv = (shape.hq + 2 * shape.hkv) * shape.head_dim
+    n_o_in = shape.hq * shape.head_dim
+    w_qkv = _normal_bf16(r, (n_qkv, shape.d), std=1.0 / np.sqrt(shape.d))
+    w_o = _normal_bf16(r, (shape.d, n_o_in), std=1.0 / np.sqrt(n_o_in))
+    gain = r.uniform(0.5, 2.0, size=shape.hq).astype(np.float32)
+    tau = float(np.float32(r.uniform(0.9, 1.3)))
+    return {"w_qkv": w_qkv, "w_o": w_o, "gain": gain, "tau": tau}
+
+
+def planted_logits(shape: Shape) -> np.ndarray:
+    """Gate logits with a needle-like structure, per sequence: z ~ N(0, 1)
+    except round(frac * n_doc) positions chosen uniformly without replacement
+    with z ~ N(3, 1).  Returned as float64 over document rows only, packed in
+    sequence order (length sum(n_doc))."""
+    r = _stream(shape, _S_PLANT)
+    out = []
+    for n in shape.n_doc:
+        z = r.standard_normal(n)
+        m = int(round(shape.planted_frac * n))
+        idx = r.choice(n, size=m, replace=False)
+        z[idx] = r.normal(3.0, 1.0, size=m)
+        out.append(z)
+    return np.concatenate(out) if out else np.zeros(0)
+
+
+def score_draws(shape: Shape, tie_frac: float = 0.05) -> np.ndarray:
+    """Non-positive float32 values shaped like gate scores, for testing the
+    selector on its own: -|N(0, 4)| per row, with ``tie_frac`` of the document
+    rows copied from another row (exact ties) and a few exact -0.0 and +0.0
+    values; question rows are +0.0.  Returned over all n_rows."""
+    r = _stream(shape, _S_SCORES)
+    s = -np.abs(r.normal(0.0, 4.0, size=shape.n_rows)).astype(np.float32)
+    cu = shape.cu_seqlens
+    for b in range(shape.batch):
+        lo, nd = int(cu[b]), shape.n_doc[b]
+        if nd > 1:
+            m = max(1, int(tie_frac * nd))
+            src = r.integers(0, nd, size=m)
+            dst = r.integers(0, nd, size=m)
+            s[lo + dst] = s[lo + src]
+            z = r.integers(0, nd, size=min(4, nd))
+            s[lo + z[: len(z) // 2]] = np.float32(-0.0)
+            s[lo + z[len(z) // 2:]] = np.float32(0.0)
+        s[lo + nd: lo + nd + shape.n_q[b]] = 0.0
+    return s
+
+
+def budgets(shape: Shape) -> np.ndarray:
+    return np.asarray(shape.k, dtype=np.int32)
+
+
+def n_doc_array(shape: Shape) -> np.ndarray:
+    return np.asarray(shape.n_doc, dtype=np.int32)
+
+
+ALL_SHAPES = {
+    "tiny": tiny,
+    "qwen3-1.7b-16k": qwen3_16k,
+    "budget-32k-k1024": lambda: budget_32k(1024),
+    "budget-32k-k4096": lambda: budget_32k(4096),
+    "budget-32k-k8192": lambda: budget_32k(8192),
+    "long-128k": long_128k,
+    "ragged-8": ragged_batch,
+}

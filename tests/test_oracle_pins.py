@@ -1,0 +1,458 @@
+"""Pins for the CPU oracle: each test checks the oracle against something
+other than itself -- closed forms, brute force written a different way on
+tiny inputs, library routines (torch SDPA in float64) and invariants -- so
+that a dropped term, a flipped sign, a wrong index or a transposed operand in
+``oracle/tokengate_oracle.py`` fails at least one of them."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from learned_token_pruning_09_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# gate
+# ---------------------------------------------------------------------------
+
+
+def test_logsigmoid_closed_forms():
+    ls = oracle.logsigmoid
+    assert ls(np.array([0.0]))[0] == pytest.approx(-math.log(2.0), abs=1e-15)
+    z = np.linspace(-30, 30, 121)
+    # logsigmoid(z) - logsigmoid(-z) = z
+    np.testing.assert_allclose(ls(z) - ls(-z), z, atol=1e-12)
+    # sigmoid(ln 3) = 3/4
+    assert ls(np.array([math.log(3.0)]))[0] == pytest.approx(math.log(0.75), abs=1e-15)
+    # tails: no overflow, asymptotes
+    assert ls(np.array([800.0]))[0] == 0.0 or abs(ls(np.array([800.0]))[0]) < 1e-300
+    assert ls(np.array([-800.0]))[0] == pytest.approx(-800.0, rel=1e-15)
+    assert ls(np.array([40.0]))[0] == pytest.approx(-math.exp(-40.0), rel=1e-12)
+    assert np.all(ls(z) <= 0.0)
+
+
+def test_gelu_closed_forms():
+    g = oracle.gelu
+    assert g(np.array([0.0]))[0] == 0.0
+    u = np.linspace(-6, 6, 97)
+    # GELU(u) - GELU(-u) = u (since Phi(u) + Phi(-u) = 1)
+    np.testing.assert_allclose(g(u) - g(-u), u, atol=1e-14)
+    # GELU(1) = Phi(1), the standard normal CDF at 1 (textbook value)
+    assert g(np.array([1.0]))[0] == pytest.approx(0.8413447460685429, abs=1e-15)
+    # GELU(-1) = -(1 - Phi(1))
+    assert g(np.array([-1.0]))[0] == pytest.approx(-0.15865525393145707, abs=1e-15)
+
+
+def _gate_bruteforce(x, w1, b1, w2, b2):
+    """Pure-Python loops with the math module only."""
+    out = []
+    for row in x:
+        z = b2
+        for j in range(len(w1)):
+            u = b1[j] + sum(w1[j][c] * row[c] for c in range(len(row)))
+            z += w2[j] * 0.5 * u * (1.0 + math.erf(u / math.sqrt(2.0)))
+        # logsigmoid via log of 1/(1+e^-z)
+        out.append(math.log(1.0 / (1.0 + math.exp(-z))))
+    return out
+
+
+def test_gate_matches_bruteforce_tiny():
+    rng = np.random.default_rng(7)
+    n, d, h = 9, 8, 4
+    shape = synth.custom("t", [6], [3], [2], d=d, h=h)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((n, d)).astype(np.float32))
+    w1 = synth.f32_to_bf16_bits(rng.standard_normal((h, d)).astype(np.float32) * 0.5)
+    w2 = synth.f32_to_bf16_bits(rng.standard_normal(h).astype(np.float32))
+    b1 = rng.standard_normal(h).astype(np.float32)
+    b2 = 0.3
+    s = oracle.gate_score(x, shape.cu_seqlens, shape.n_doc, w1, b1, w2, b2)
+    xf = synth.bf16_bits_to_f32(x).astype(float).tolist()
+    ref = _gate_bruteforce(xf[:6], synth.bf16_bits_to_f32(w1).astype(float).tolist(),
+                           b1.astype(float).tolist(),
+                           synth.bf16_bits_to_f32(w2).astype(float).tolist(), b2)
+    np.testing.assert_allclose(s[:6].astype(float), ref, rtol=1e-6, atol=1e-7)
+    assert np.all(s[6:] == 0.0) and not np.any(np.signbit(s[6:]))
+
+
+def test_gate_zero_w2_gives_logsigmoid_b2():
+    shape = synth.custom("t", [40, 7], [5, 2], [4, 4], d=64, h=16)
+    x = synth.residuals(shape)
+    p = synth.gate_weights(shape)
+    w2 = np.zeros(16, dtype=np.uint16)            # bf16 +0.0
+    b2 = math.log(3.0)
+    s = oracle.gate_score(x, shape.cu_seqlens, shape.n_doc, p["w1"], None, w2, b2)
+    cu = shape.cu_seqlens
+    for b in range(2):
+        doc = s[cu[b]: cu[b] + shape.n_doc[b]]
+        np.testing.assert_array_equal(doc, np.float32(math.log(0.75)))
+        assert np.all(s[cu[b] + shape.n_doc[b]: cu[b + 1]] == 0.0)
+
+
+def test_gate_single_hidden_unit_closed_form():
+    """h = 1, W1 = e_0, w2 = 1: z = GELU(x_0) exactly."""
+    d = 16
+    x = synth.f32_to_bf16_bits(np.array([[1.0] + [5.0] * (d - 1),
+                                         [-1.0] + [2.0] * (d - 1),
+                                         [0.0] * d], dtype=np.float32))
+    w1 = synth.f32_to_bf16_bits(np.eye(1, d, dtype=np.float32))
+    w2 = synth.f32_to_bf16_bits(np.ones(1, np.float32))
+    s = oracle.gate_score(x, [0, 3], [3], w1, None, w2, 0.0)
+    phi1 = 0.8413447460685429
+    expect = [-math.log1p(math.exp(-phi1)),
+              -math.log1p(math.exp(-(-(1 - phi1)))),
+              -math.log(2.0)]
+    np.testing.assert_allclose(s.astype(float), expect, rtol=1e-7)
+
+
+def test_gate_rows_subset_consistent():
+    shape = synth.custom("t", [50], [6], [8], d=64, h=16)
+    x = synth.residuals(shape)
+    p = synth.gate_weights(shape)
+    full = oracle.gate_score(x, shape.cu_seqlens, shape.n_doc, p["w1"], p["b1"], p["w2"], 0.1)
+    rows = np.array([0, 3, 49, 50, 55])
+    sub = oracle.gate_score(x, shape.cu_seqlens, shape.n_doc, p["w1"], p["b1"], p["w2"], 0.1, rows=rows)
+    np.testing.assert_array_equal(sub[rows], full[rows])
+
+
+# ---------------------------------------------------------------------------
+# top-K
+# ---------------------------------------------------------------------------
+
+
+def _topk_by_rank_counting(s, lo, nd, k):
+    """O(n^2) brute force: row j is kept iff fewer than k rows beat it, where
+    i beats j when s_i > s_j, or s_i == s_j and i < j."""
+    kept = []
+    for j in range(nd):
+        beaten = 0
+        for i in range(nd):
+            if s[lo + i] > s[lo + j] or (s[lo + i] == s[lo + j] and i < j):
+                beaten += 1
+        if beaten < k:
+            kept.append(lo + j)
+    return kept
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_matches_rank_counting(seed):
+    rng = np.random.default_rng(seed)
+    n_doc = rng.integers(0, 60, size=3).tolist()
+    n_q = rng.integers(0, 5, size=3).tolist()
+    k = rng.integers(0, 70, size=3).tolist()
+    shape = synth.custom("t", n_doc, n_q, k)
+    cu = shape.cu_seqlens
+    # values from a small set -> many exact ties, including -0.0 and +0.0
+    pool = np.array([-3.5, -1.0, -0.25, -0.0, 0.0, -7.0], dtype=np.float32)
+    s = pool[rng.integers(0, len(pool), size=shape.n_rows)]
+    kept, cu_kept = oracle.topk_select(s, cu, n_doc, k)
+    expect, ecu = [], [0]
+    for b in range(3):
+        expect += _topk_by_rank_counting(s, int(cu[b]), n_doc[b], k[b])
+        expect += list(range(int(cu[b]) + n_doc[b], int(cu[b + 1])))
+        ecu.append(len(expect))
+    np.testing.assert_array_equal(kept, expect)
+    np.testing.assert_array_equal(cu_kept, ecu)
+
+
+def test_topk_special_cases():
+    # all equal -> the first K document rows
+    s = np.full(20, -1.0, np.float32)
+    kept, _ = oracle.topk_select(s, [0, 20], [16], [5])
+    np.testing.assert_array_equal(kept, [0, 1, 2, 3, 4, 16, 17, 18, 19])
+    # a planted set of K distinct maxima -> exactly that set
+    rng = np.random.default_rng(3)
+    s = -rng.uniform(1, 2, 100).astype(np.float32)
+    plant = np.array([97, 5, 44, 60, 12])
+    s[plant] = -np.array([0.1, 0.2, 0.3, 0.4, 0.5], np.float32)
+    kept, cu = oracle.topk_select(s, [0, 100], [100], [5])
+    np.testing.assert_array_equal(kept, np.sort(plant))
+    # K >= n_doc keeps the whole document; K = 0 keeps the question only
+    kept, cu = oracle.topk_select(s, [0, 100], [90], [1000])
+    np.testing.assert_array_equal(kept, np.arange(100))
+    kept, cu = oracle.topk_select(s, [0, 100], [90], [0])
+    np.testing.assert_array_equal(kept, np.arange(90, 100))
+    # +0.0 and -0.0 tie: the lower index wins
+    s = np.array([-1.0, 0.0, -0.0, -2.0], np.float32)
+    s2 = np.array([-1.0, -0.0, 0.0, -2.0], np.float32)
+    assert oracle.topk_select(s, [0, 4], [4], [1])[0].tolist() == [1]
+    assert oracle.topk_select(s2, [0, 4], [4], [1])[0].tolist() == [1]
+    # NaN ranks after every number
+    s = np.array([np.nan, -5.0, np.nan, -9.0], np.float32)
+    assert oracle.topk_select(s, [0, 4], [4], [2])[0].tolist() == [1, 3]
+    assert oracle.topk_select(s, [0, 4], [4], [3])[0].tolist() == [0, 1, 3]
+    # empty document
+    assert oracle.topk_select(np.zeros(3, np.float32), [0, 3], [0], [4])[0].tolist() == [0, 1, 2]
+
+
+def test_topk_invariants_on_workload_draws():
+    shape = synth.ragged_batch()
+    shape = synth.custom("r", [n // 64 for n in shape.n_doc], shape.n_q,
+                         [k // 64 for k in shape.k])
+    s = synth.score_draws(shape)
+    kept, cu_kept = oracle.topk_select(s, shape.cu_seqlens, shape.n_doc, shape.k)
+    np.testing.assert_array_equal(cu_kept, shape.cu_kept)
+    cu = shape.cu_seqlens
+    for b in range(shape.batch):
+        ks = kept[cu_kept[b]: cu_kept[b + 1]]
+        assert np.all(np.diff(ks) > 0)
+        qrows = np.arange(cu[b] + shape.n_doc[b], cu[b + 1])
+        assert set(qrows) <= set(ks.tolist())
+        doc_kept = ks[ks < cu[b] + shape.n_doc[b]]
+        doc_all = np.arange(cu[b], cu[b] + shape.n_doc[b])
+        dropped = np.setdiff1d(doc_all, doc_kept)
+        if len(doc_kept) and len(dropped):
+            assert s[doc_kept].min() >= s[dropped].max()
+            # equality only where the index rule applies
+            t = s[doc_kept].min()
+            eq_kept = doc_kept[s[doc_kept] == t]
+            eq_drop = dropped[s[dropped] == t]
+            if len(eq_drop):
+                assert eq_kept.max() < eq_drop.min()
+
+
+# ---------------------------------------------------------------------------
+# gather
+# ---------------------------------------------------------------------------
+
+
+def test_gather_definition():
+    shape = synth.custom("g", [10, 6], [2, 3], [4, 9])
+    x = synth.residuals(shape)
+    s = synth.score_draws(shape)
+    kept, cu_kept = oracle.topk_select(s, shape.cu_seqlens, shape.n_doc, shape.k)
+    xk, pos, sk = oracle.gather_kept(x, s, shape.cu_seqlens, kept, cu_kept)
+    for i, r in enumerate(kept):
+        assert np.array_equal(xk[i], x[r])
+        b = 0 if r < shape.cu_seqlens[1] else 1
+        assert pos[i] == r - shape.cu_seqlens[b]
+        assert sk[i].tobytes() == s[r].tobytes()
+
+
+# ---------------------------------------------------------------------------
+# RoPE
+# ---------------------------------------------------------------------------
+
+
+def _rope_complex(x, pos, theta):
+    """Independent form: pair (x_i, x_{i+D/2}) as a complex number times
+    exp(j * pos * theta^(-2i/D))."""
+    d = x.shape[-1]
+    half = d // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    freq = np.array([theta ** (-(2.0 * i) / d) for i in range(half)])
+    rot = np.exp(1j * np.outer(pos, freq))[:, None, :]
+    w = z * rot
+    return np.concatenate([w.real, w.imag], axis=-1)
+
+
+def test_rope_pins():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((7, 3, 16))
+    pos = np.array([0, 1, 2, 100, 4097, 131071, 65536])
+    r = oracle.rope(x, pos, 1.0e6)
+    np.testing.assert_allclose(r, _rope_complex(x, pos, 1.0e6), atol=1e-12)
+    # position 0 is the identity
+    np.testing.assert_array_equal(oracle.rope(x[:1], np.array([0]), 1e6), x[:1])
+    # dimension 0 rotates by exactly pos radians
+    e = np.zeros((1, 1, 16)); e[0, 0, 0] = 1.0
+    r1 = oracle.rope(e, np.array([1]), 1e6)
+    assert r1[0, 0, 0] == pytest.approx(math.cos(1.0), abs=1e-15)
+    assert r1[0, 0, 8] == pytest.approx(math.sin(1.0), abs=1e-15)
+    # relative: <R_p q, R_p' k> depends only on p' - p
+    q = rng.standard_normal((1, 1, 16)); k = rng.standard_normal((1, 1, 16))
+    a = np.sum(oracle.rope(q, np.array([5]), 1e6) * oracle.rope(k, np.array([12]), 1e6))
+    b = np.sum(oracle.rope(q, np.array([1005]), 1e6) * oracle.rope(k, np.array([1012]), 1e6))
+    assert a == pytest.approx(b, abs=1e-10)
+
+
+# ---------------------------------------------------------------------------
+# token-gated attention
+# ---------------------------------------------------------------------------
+
+
+def _attn_bruteforce(q, k, v, pos, s, gain, tau, theta):
+    """Explicit full masked-softmax matrix with Python loops on tiny
+    inputs (single sequence); RoPE through the complex form."""
+    t, hq, d = q.shape
+    hkv = k.shape[1]
+    qr = _rope_complex(q, pos, theta)
+    kr = _rope_complex(k, pos, theta)
+    o = np.zeros((t, hq, d))
+    for h in range(hq):
+        g = h * hkv // hq
+        for i in range(t):
+            logits = []
+            for j in range(t):
+                if pos[j] <= pos[i]:
+                    dot = sum(qr[i, h, c] * kr[j, g, c] for c in range(d))
+                    logits.append((j, dot / (math.sqrt(d) * tau) + gain[h] * s[j]))
+            mx = max(val for _, val in logits)
+            w = [(j, math.exp(val - mx)) for j, val in logits]
+            tot = sum(val for _, val in w)
+            for j, val in w:
+                o[i, h] += val / tot * v[j, g]
+    return o
+
+
+def _rand_qkv(rng, t, hq, hkv, d):
+    bf = lambda a: synth.f32_to_bf16_bits(a.astype(np.float32))
+    return (bf(rng.standard_normal((t, hq, d))), bf(rng.standard_normal((t, hkv, d))),
+            bf(rng.standard_normal((t, hkv, d))))
+
+
+def test_attention_matches_bruteforce_shuffled_positions():
+    rng = np.random.default_rng(5)
+    t, hq, hkv, d = 7, 4, 2, 8
+    q, k, v = _rand_qkv(rng, t, hq, hkv, d)
+    pos = np.array([30, 2, 17, 5, 100, 3, 64])
+    s = -rng.uniform(0, 3, t)
+    gain = np.array([0.5, 1.0, 1.5, 2.0])
+    o, lse = oracle.gated_attention(q, k, v, pos, s, gain, 1.2, [0, t], 1e6)
+    ref = _attn_bruteforce(oracle.bf16_decode(q), oracle.bf16_decode(k), oracle.bf16_decode(v),
+                           pos, s, gain, 1.2, 1e6)
+    np.testing.assert_allclose(o, ref, atol=1e-12)
+
+
+def _dense_causal_sdpa(q, k, v, pos, theta, tau=1.0):
+    """Dense causal attention by torch's scaled_dot_product_attention in
+    float64, GQA by repeating KV heads (head h reads KV head h // G)."""
+    qr = torch.from_numpy(_rope_complex(q, pos, theta)).permute(1, 0, 2)
+    kr = torch.from_numpy(_rope_complex(k, pos, theta)).permute(1, 0, 2)
+    vv = torch.from_numpy(v).permute(1, 0, 2)
+    g = q.shape[1] // k.shape[1]
+    kr = kr.repeat_interleave(g, dim=0)
+    vv = vv.repeat_interleave(g, dim=0)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qr, kr, vv, is_causal=True, scale=1.0 / (math.sqrt(q.shape[-1]) * tau))
+    return o.permute(1, 0, 2).numpy()
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 2), (4, 4), (8, 2)])
+def test_attention_reduces_to_dense_causal(hq, hkv):
+    """K = N, gain 0 (or s = 0) and tau = 1: plain causal attention."""
+    rng = np.random.default_rng(hq * 10 + hkv)
+    t, d = 40, 16
+    q, k, v = _rand_qkv(rng, t, hq, hkv, d)
+    pos = np.arange(t)
+    s = -rng.uniform(0, 4, t)
+    qf, kf, vf = (oracle.bf16_decode(a) for a in (q, k, v))
+    o0, _ = oracle.gated_attention(q, k, v, pos, s, np.zeros(hq), 1.0, [0, t], 1e6)
+    o1, _ = oracle.gated_attention(q, k, v, pos, np.zeros(t), rng.uniform(0.5, 2, hq), 1.0, [0, t], 1e6)
+    ref = _dense_causal_sdpa(qf, kf, vf, pos, 1e6)
+    np.testing.assert_allclose(o0, ref, atol=1e-12)
+    np.testing.assert_allclose(o1, ref, atol=1e-12)
+    # tau: same as zero-bias attention with the softmax scale divided by tau
+    o2, _ = oracle.gated_attention(q, k, v, pos, s, np.zeros(hq), 1.7, [0, t], 1e6)
+    np.testing.assert_allclose(o2, _dense_causal_sdpa(qf, kf, vf, pos, 1e6, tau=1.7), atol=1e-12)
+
+
+def test_attention_bias_invariants():
+    rng = np.random.default_rng(21)
+    t, hq, hkv, d = 24, 2, 1, 16
+    q, k, v = _rand_qkv(rng, t, hq, hkv, d)
+    pos = np.sort(rng.choice(1000, t, replace=False))
+    gain = np.array([0.7, 1.9])
+    # a constant score shifts every logit of a row equally: no effect
+    c1, _ = oracle.gated_attention(q, k, v, pos, np.full(t, -0.3), gain, 1.1, [0, t])
+    c2, _ = oracle.gated_attention(q, k, v, pos, np.full(t, -5.0), gain, 1.1, [0, t])
+    np.testing.assert_allclose(c1, c2, atol=1e-12)
+    # a key with a huge negative bias drops out: same as removing it
+    s = -rng.uniform(0, 1, t)
+    s_big = s.copy(); s_big[3] = -1e6
+    ob, _ = oracle.gated_attention(q, k, v, pos, s_big, gain, 1.1, [0, t])
+    keep = np.array([i for i in range(t) if i != 3])
+    orm, _ = oracle.gated_attention(q[keep], k[keep], v[keep], pos[keep], s[keep], gain, 1.1, [0, t - 1])
+    np.testing.assert_allclose(ob[keep], orm, atol=1e-12)
+    # a larger score means more weight: with q = 0 the output is the
+    # score-weighted mean: weights exp(g_h s_j) / sum
+    zero = np.zeros_like(q)
+    oz, lse = oracle.gated_attention(zero, k, v, pos, s, gain, 1.1, [0, t])
+    vf = oracle.bf16_decode(v)
+    for h in range(hq):
+        w = np.exp(gain[h] * s)
+        i = t - 1
+        np.testing.assert_allclose(oz[i, h], (w[:, None] * vf[:, 0]).sum(0) / w.sum(), atol=1e-12)
+        assert lse[h, i] == pytest.approx(math.log(w.sum()), abs=1e-12)
+
+
+def test_attention_permutation_and_shift_consistency():
+    rng = np.random.default_rng(8)
+    t, hq, hkv, d = 20, 4, 2, 16
+    q, k, v = _rand_qkv(rng, t, hq, hkv, d)
+    pos = np.sort(rng.choice(500, t, replace=False))
+    s = -rng.uniform(0, 2, t)
+    gain = rng.uniform(0.5, 2, hq)
+    o, lse = oracle.gated_attention(q, k, v, pos, s, gain, 0.95, [0, t])
+    perm = rng.permutation(t)
+    op, lsep = oracle.gated_attention(q[perm], k[perm], v[perm], pos[perm], s[perm], gain, 0.95, [0, t])
+    np.testing.assert_allclose(op, o[perm], atol=1e-12)
+    np.testing.assert_allclose(lsep, lse[:, perm], atol=1e-12)
+    # RoPE is relative: shifting every position leaves the output unchanged
+    os_, _ = oracle.gated_attention(q, k, v, pos + 777, s, gain, 0.95, [0, t])
+    np.testing.assert_allclose(os_, o, atol=1e-9)
+
+
+def test_attention_varlen_equals_separate_calls():
+    rng = np.random.default_rng(9)
+    lens = [5, 11, 1]
+    t = sum(lens)
+    q, k, v = _rand_qkv(rng, t, 2, 1, 8)
+    pos = np.concatenate([np.arange(n) * 3 for n in lens])
+    s = -rng.uniform(0, 2, t)
+    gain = np.array([1.0, 1.5])
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o, _ = oracle.gated_attention(q, k, v, pos, s, gain, 1.0, cu)
+    for b in range(3):
+        a, e = cu[b], cu[b + 1]
+        ob, _ = oracle.gated_attention(q[a:e], k[a:e], v[a:e], pos[a:e], s[a:e], gain, 1.0, [0, e - a])
+        np.testing.assert_allclose(o[a:e], ob, atol=1e-13)
+
+
+def test_attention_golden_orthogonal_example():
+    """Hand-derived example (tests/golden/attention_orthogonal.json)."""
+    with open(os.path.join(GOLDEN, "attention_orthogonal.json")) as f:
+        case = json.load(f)
+    q = np.array(case["q"], float)[:, None, :]
+    k = np.array(case["k"], float)[:, None, :]
+    v = np.array(case["v"], float)[:, None, :]
+    o, lse = oracle.gated_attention(q, k, v, np.array(case["pos"]), np.array(case["s"]),
+                                    np.array([case["gain"]]), case["tau"], [0, len(case["pos"])],
+                                    q_is_f64=True)
+    np.testing.assert_allclose(o[:, 0, :], np.array(case["o"]), atol=1e-14)
+    np.testing.assert_allclose(lse[0], np.array(case["lse"]), atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# stacked layer
+# ---------------------------------------------------------------------------
+
+
+def test_stacked_layer_loops():
+    rng = np.random.default_rng(2)
+    t, dm, hq, hkv, dh = 6, 8, 2, 1, 4
+    x = rng.standard_normal((t, dm))
+    wqkv = synth.f32_to_bf16_bits(rng.standard_normal(((hq + 2 * hkv) * dh, dm)).astype(np.float32) * 0.3)
+    wo = synth.f32_to_bf16_bits(rng.standard_normal((dm, hq * dh)).astype(np.float32) * 0.3)
+    pos = np.array([0, 3, 4, 9, 10, 12])
+    s = -rng.uniform(0, 1, t)
+    gain = np.array([1.0, 0.6])
+    out, o = oracle.stacked_layer(x, wqkv, wo, pos, s, gain, 1.05, [0, t], hq, hkv, dh)
+    W = oracle.bf16_decode(wqkv)
+    Wo = oracle.bf16_decode(wo)
+    qkv = [[sum(x[i][c] * W[r][c] for c in range(dm)) for r in range(W.shape[0])] for i in range(t)]
+    qkv = np.array(qkv)
+    q = qkv[:, :hq * dh].reshape(t, hq, dh)
+    k = qkv[:, hq * dh:(hq + hkv) * dh].reshape(t, hkv, dh)
+    v = qkv[:, (hq + hkv) * dh:].reshape(t, hkv, dh)
+    oref = _attn_bruteforce(q, k, v, pos, s, gain, 1.05, 1e6)
+    np.testing.assert_allclose(o, oref, atol=1e-12)
+    flat = oref.reshape(t, hq * dh)
+    xref = np.array([[x[i][r] + sum(flat[i][c] * Wo[r][c] for c in range(hq * dh))
+                      for r in range(dm)] for i in range(t)])
+    np.testing.assert_allclose(out, xref, atol=1e-12)
