@@ -1,0 +1,207 @@
+/*
+ * tokengate.h -- C ABI of libtokengate.so, the TokenGate pruned-prefill hot
+ * path on NVIDIA B300 (sm_103a).
+ *
+ * TokenGate (MarkTechPost article "Researchers from Stanford and UC Berkeley
+ * introduce TokenGate", section "How does TokenGate's learned token pruning
+ * work?") splits the prefill forward pass in three phases: the layers below
+ * the gate layer L run on all N tokens; at layer L a small MLP scores every
+ * token from its post-attention residual and a top-K selector keeps the
+ * highest-scoring ones (only the document is prunable, the question is never
+ * pruned); the layers above L run on the kept tokens only and create no KV
+ * entries for the pruned ones.  Section "What is token-gated attention?": the
+ * kept token's score becomes a bias on the attention logits above the gate,
+ * refined by a learnable per-head gain and a learnable temperature.
+ *
+ * The calls below are the steps of that path, in order:
+ *   tg_gate_score -> tg_topk_select -> tg_gather_kept -> (per layer)
+ *   [tg_linear_bf16 for Q/K/V] -> tg_gated_attention_fwd -> [tg_linear_bf16
+ *   for the output projection with the residual add].
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is DEVICE memory, allocated and owned by the
+ *   caller, unless stated otherwise.  The library allocates no device memory
+ *   on any compute call; scratch space is passed in as `workspace`.
+ * - bf16 tensors are dense row-major arrays of 16-bit bfloat16 values; base
+ *   pointers of bf16 matrices must be 16-byte aligned.
+ * - Packed (varlen) layout: the rows of the `batch` sequences are
+ *   concatenated; sequence b owns rows [cu_seqlens[b], cu_seqlens[b+1]).  Each
+ *   sequence is its document (the first n_doc[b] rows) followed by its
+ *   question (the remaining rows).
+ * - Calls are asynchronous on `stream` and never synchronise.  Arguments are
+ *   validated on the host before anything is launched: an invalid argument
+ *   returns an error status and launches nothing.  Conditions that only the
+ *   device can see (an index out of range, a device-side wait that timed out)
+ *   are recorded in a device status word, read by tg_check_device_status().
+ * - Thread safety: calls may be issued from several host threads; the last
+ *   error string is per thread.
+ */
+#ifndef TOKENGATE_H_
+#define TOKENGATE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define TG_API __attribute__((visibility("default")))
+#else
+#define TG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TG_OK = 0,
+  TG_ERR_INVALID_ARG = 1,   /* bad pointer, size, shape or alignment        */
+  TG_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim 96) */
+  TG_ERR_WORKSPACE = 3,     /* workspace missing or too small               */
+  TG_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed            */
+  TG_ERR_TIMEOUT = 5,       /* a device-side wait exceeded its cycle limit  */
+  TG_ERR_DEVICE_INDEX = 6   /* a device-side index/size check failed        */
+} tg_status;
+
+/*
+ * Gate MLP scores (gate module, "How does TokenGate's learned token pruning
+ * work?", second phase; the spec fixes the algebra).  For every DOCUMENT row j:
+ *     z_j = w2 . GELU(W1 x_j + b1) + b2,   s_j = logsigmoid(z_j)
+ * with the exact-erf GELU; for every QUESTION row s_j = +0.0.
+ *
+ *   x_bf16     [n_rows, d] bf16, the gate-layer residuals (packed layout)
+ *   n_rows     total rows; must equal cu_seqlens[batch]
+ *   d          hidden size, multiple of 64, 64 <= d <= 65536
+ *   cu_seqlens [batch+1] int32, device
+ *   n_doc      [batch] int32, device; 0 <= n_doc[b] <= seqlen_b
+ *   w1_bf16    [h, d] bf16 (nn.Linear layout)
+ *   b1         [h] fp32 or NULL (zero)
+ *   w2_bf16    [h] bf16
+ *   b2         scalar
+ *   h          hidden width, multiple of 16, 16 <= h <= 256
+ *   s_out      [n_rows] fp32 output
+ * Bf16 inputs, fp32 accumulation on the tensor cores, fp32 epilogue.
+ * Device-side errors: n_doc out of range -> TG_ERR_DEVICE_INDEX (those rows
+ * are then left unwritten).
+ */
+TG_API tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d,
+                        const int32_t* cu_seqlens, const int32_t* n_doc, int32_t batch,
+                        const void* w1_bf16, const float* b1, const void* w2_bf16, float b2,
+                        int32_t h, float* s_out, cudaStream_t stream);
+
+/*
+ * Top-K selection (same section: "a top-K selector keeps the tokens with the
+ * highest score"; "only the document part of the prompt is prunable, the
+ * question is never pruned").  For each sequence b with K_b = min(k[b],
+ * n_doc[b]): the K_b document rows with the largest s (ties broken towards the
+ * lower row index; -0.0 equals +0.0; NaN ranks below every number), written
+ * in ascending row order, followed by every question row of b in order.
+ * Row ids are global (packed) row numbers.  k[b] > n_doc[b] keeps the whole
+ * document; k[b] = 0 keeps the question only.
+ *
+ *   s           [n_rows] fp32 scores
+ *   cu_seqlens  [batch+1] int32, n_doc [batch] int32, k [batch] int32 (device)
+ *   max_n_doc   host-side upper bound on every n_doc[b] (sizes the launch);
+ *               a larger n_doc[b] on the device -> TG_ERR_DEVICE_INDEX
+ *   kept_idx    [sum_b T_b] int32 output, T_b = min(k[b], n_doc[b]) + n_q[b]
+ *   cu_kept     [batch+1] int32 output, prefix sums of T_b
+ * Exact integer result: bit-identical to the definition for any input.
+ * Uses no workspace.
+ */
+TG_API tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* cu_seqlens,
+                         const int32_t* n_doc, const int32_t* k, int32_t batch,
+                         int32_t max_n_doc, int32_t* kept_idx, int32_t* cu_kept,
+                         cudaStream_t stream);
+
+/*
+ * Gather of the kept rows (third phase: the layers above L run on the kept
+ * tokens only).  For kept slot i of sequence b:
+ *     x_kept[i] = X[kept_idx[i]],  pos_kept[i] = kept_idx[i] - cu_seqlens[b],
+ *     s_kept[i] = s[kept_idx[i]]
+ *
+ *   x_bf16 [n_rows, d] bf16; s [n_rows] fp32; cu_seqlens [batch+1];
+ *   kept_idx [n_kept], cu_kept [batch+1] as written by tg_topk_select
+ *   n_kept  host-side total kept rows (= cu_kept[batch])
+ *   x_kept_bf16 [n_kept, d] bf16, pos_kept [n_kept] int32, s_kept [n_kept]
+ *   fp32 outputs; any of the three may be NULL to skip it.
+ * A kept index outside its sequence -> TG_ERR_DEVICE_INDEX, row skipped.
+ */
+TG_API tg_status tg_gather_kept(const void* x_bf16, int64_t n_rows, int32_t d, const float* s,
+                         const int32_t* cu_seqlens, const int32_t* kept_idx,
+                         const int32_t* cu_kept, int32_t batch, int64_t n_kept,
+                         void* x_kept_bf16, int32_t* pos_kept, float* s_kept,
+                         cudaStream_t stream);
+
+/*
+ * Token-gated causal attention over the kept tokens ("What is token-gated
+ * attention?"; the spec fixes the algebra).  For kept row i of sequence b and
+ * query head h, with G = hq / hkv and g = floor(h / G):
+ *   logit_ij = (q'_i,h . k'_j,g) / (sqrt(head_dim) * tau) + gain[h] * s_kept[j]
+ * over the kept rows j of b with pos_kept[j] <= pos_kept[i];
+ *   o_i,h = sum_j softmax_j(logit_ij) v_j,g,   lse[h, i] = ln sum_j exp(logit_ij)
+ * where q' and k' are q and k rotated by rotate-half RoPE at the ORIGINAL
+ * positions pos_kept with base rope_theta (1e6 for Qwen3).
+ *
+ *   q  [n_kept, hq, head_dim] bf16;  k, v [n_kept, hkv, head_dim] bf16
+ *   pos_kept [n_kept] int32, STRICTLY increasing within each sequence (as
+ *            tg_gather_kept writes it); otherwise TG_ERR_DEVICE_INDEX
+ *   s_kept [n_kept] fp32;  gain [hq] fp32;  tau > 0;  rope_theta > 0
+ *   cu_kept [batch+1] int32 (device);  max_kept: host upper bound on every
+ *            sequence's kept length (sizes the launch)
+ *   hq % hkv == 0, hq / hkv even or 1; head_dim in {64, 128}
+ *   o      [n_kept, hq, head_dim] bf16 output
+ *   lse    [hq, n_kept] fp32 output (natural log), or NULL
+ *   k_cache [n_kept, hkv, head_dim] bf16 output: the rotated keys k' (the
+ *            kept-only KV cache), or NULL (then kept in the workspace)
+ *   workspace of at least tg_attention_workspace_size(...) bytes, 256-byte
+ *            aligned; holds q' (and k' when k_cache is NULL)
+ * Rounding: q', k' and the softmax probabilities are rounded to bf16 before
+ * the tensor-core products; accumulation and softmax are fp32.
+ */
+TG_API tg_status tg_gated_attention_fwd(const void* q, const void* k, const void* v,
+                                 const int32_t* pos_kept, const float* s_kept,
+                                 const float* gain, float tau, float rope_theta,
+                                 const int32_t* cu_kept, int32_t batch, int64_t n_kept,
+                                 int32_t max_kept, int32_t hq, int32_t hkv, int32_t head_dim,
+                                 void* o, float* lse, void* k_cache,
+                                 void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/* Bytes of workspace tg_gated_attention_fwd needs (q' and, if no k_cache is
+ * given, k').  Host-only, no CUDA call. */
+TG_API size_t tg_attention_workspace_size(int64_t n_kept, int32_t hq, int32_t hkv,
+                                   int32_t head_dim, int32_t has_k_cache);
+
+/*
+ * Dense projection for the layers above the gate (long-context workload: a
+ * stack of token-gated attention layers, each with its own Q/K/V/O
+ * projections):  out[m, n] = sum_k a[m, k] * w[n, k]  (+ residual[m, n])
+ *
+ *   a [m, kdim] bf16, w [n, kdim] bf16 (nn.Linear layout), residual [m, n]
+ *   bf16 or NULL, out [m, n] bf16 (may alias residual).
+ *   kdim multiple of 64; n multiple of 16.  fp32 accumulation, one rounding.
+ */
+TG_API tg_status tg_linear_bf16(const void* a, const void* w, const void* residual, void* out,
+                         int64_t m, int32_t n, int32_t kdim, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device: TG_OK, TG_ERR_TIMEOUT or TG_ERR_DEVICE_INDEX. */
+TG_API tg_status tg_check_device_status(cudaStream_t stream);
+
+/* Cycle limit of every device-side wait (default 2^31 SM cycles, about one
+ * second).  A wait that runs out records TG_ERR_TIMEOUT and its kernel
+ * returns.  0 restores the default. */
+TG_API void tg_set_watchdog_cycles(long long cycles);
+
+/* Message of the last error returned on this host thread ("" if none). */
+TG_API const char* tg_last_error_string(void);
+
+/* Library version string. */
+TG_API const char* tg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOKENGATE_H_ */

@@ -1,0 +1,361 @@
+// C ABI of libtokengate.so (declared in include/tokengate.h): argument
+// validation, TMA descriptor encoding, the device status word and kernel
+// launches.  Every compute entry point validates on the host and launches
+// nothing when an argument is invalid.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "tg_internal.h"
+#include "../../include/tokengate.h"
+
+namespace tg {
+
+// The status word lives in this module's static device memory (one copy per
+// device that loads the library); kernels receive its device address.
+__device__ unsigned int g_device_status;
+
+namespace {
+
+thread_local std::string g_last_error;
+long long g_watchdog_cycles = 1LL << 31;
+
+tg_status fail(tg_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+tg_status ok() {
+  g_last_error.clear();
+  return TG_OK;
+}
+
+tg_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(TG_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  unsigned int* status = nullptr;
+  int num_sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+tg_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(TG_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.status = static_cast<unsigned int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return TG_OK;
+}
+
+// ---- TMA descriptors -------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor of `rank` dims (innermost first), 128-byte swizzle.
+tg_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                   const uint32_t* box, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(TG_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5];
+  cuuint32_t es[5];
+  for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; es[i] = 1; }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs,
+                  bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(TG_ERR_INVALID_ARG, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+  return TG_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace tg
+
+using namespace tg;
+
+extern "C" {
+
+const char* tg_version(void) { return "tokengate-b300 0.1 (sm_103a)"; }
+
+const char* tg_last_error_string(void) { return g_last_error.c_str(); }
+
+void tg_set_watchdog_cycles(long long cycles) { g_watchdog_cycles = cycles > 0 ? cycles : (1LL << 31); }
+
+tg_status tg_check_device_status(cudaStream_t stream) {
+  DeviceInfo* di = nullptr;
+  tg_status s = device_info(&di);
+  if (s != TG_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "read status");
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "clear status");
+  if (v == kStatusTimeout) return fail(TG_ERR_TIMEOUT, "a device-side wait exceeded its cycle limit");
+  if (v == kStatusIndex) return fail(TG_ERR_DEVICE_INDEX, "a device-side index or size check failed");
+  if (v != 0) return fail(TG_ERR_CUDA, "unknown device status %u", v);
+  return ok();
+}
+
+tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d, const int32_t* cu_seqlens,
+                        const int32_t* n_doc, int32_t batch, const void* w1_bf16, const float* b1,
+                        const void* w2_bf16, float b2, int32_t h, float* s_out, cudaStream_t stream) {
+  if (n_rows < 0 || n_rows > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_rows out of range");
+  if (batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
+  if (d < 64 || d % 64 != 0 || d > (1 << 20)) return fail(TG_ERR_INVALID_ARG, "d must be a positive multiple of 64");
+  if (h < 16 || h > 256 || h % 16 != 0) return fail(TG_ERR_INVALID_ARG, "h must be a multiple of 16 in [16, 256]");
+  if (!cu_seqlens || !n_doc || !w1_bf16 || !w2_bf16) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (n_rows == 0) return ok();
+  if (!x_bf16 || !s_out) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(x_bf16) || !aligned16(w1_bf16)) return fail(TG_ERR_INVALID_ARG, "x and w1 must be 16-byte aligned");
+  if (!std::isfinite(b2)) return fail(TG_ERR_INVALID_ARG, "b2 must be finite");
+  DeviceInfo* di = nullptr;
+  tg_status s = device_info(&di);
+  if (s != TG_OK) return s;
+  CUtensorMap mx, mw;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(n_rows)};
+    const uint64_t str[1] = {static_cast<uint64_t>(d) * 2};
+    const uint32_t box[2] = {64, 128};
+    if ((s = make_map(&mx, x_bf16, 2, dims, str, box, "x")) != TG_OK) return s;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(h)};
+    const uint64_t str[1] = {static_cast<uint64_t>(d) * 2};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(h)};
+    if ((s = make_map(&mw, w1_bf16, 2, dims, str, box, "w1")) != TG_OK) return s;
+  }
+  GateArgs a{};
+  a.b1 = b1;
+  a.w2 = static_cast<const __nv_bfloat16*>(w2_bf16);
+  a.b2 = b2;
+  a.cu_seqlens = cu_seqlens;
+  a.n_doc = n_doc;
+  a.batch = batch;
+  a.n_rows = n_rows;
+  a.d = d;
+  a.h = h;
+  a.s_out = s_out;
+  a.status = di->status;
+  a.watchdog = g_watchdog_cycles;
+  cudaError_t e = launch_gate(mx, mw, a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gate kernel launch");
+  return ok();
+}
+
+tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* cu_seqlens, const int32_t* n_doc,
+                         const int32_t* k, int32_t batch, int32_t max_n_doc, int32_t* kept_idx,
+                         int32_t* cu_kept, cudaStream_t stream) {
+  if (batch < 0 || batch > (1 << 24)) return fail(TG_ERR_INVALID_ARG, "batch out of range");
+  if (n_rows < 0 || n_rows > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_rows out of range");
+  if (max_n_doc < 0) return fail(TG_ERR_INVALID_ARG, "max_n_doc must be >= 0");
+  if (batch == 0) return ok();
+  if (!cu_seqlens || !n_doc || !k || !cu_kept) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (n_rows > 0 && (!s || !kept_idx)) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+  TopkArgs a{};
+  a.s = s;
+  a.cu_seqlens = cu_seqlens;
+  a.n_doc = n_doc;
+  a.k = k;
+  a.batch = batch;
+  a.max_n_doc = max_n_doc;
+  a.kept_idx = kept_idx;
+  a.cu_kept = cu_kept;
+  a.status = di->status;
+  cudaError_t e = launch_topk(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "top-K kernel launch");
+  return ok();
+}
+
+tg_status tg_gather_kept(const void* x_bf16, int64_t n_rows, int32_t d, const float* s,
+                         const int32_t* cu_seqlens, const int32_t* kept_idx, const int32_t* cu_kept,
+                         int32_t batch, int64_t n_kept, void* x_kept_bf16, int32_t* pos_kept, float* s_kept,
+                         cudaStream_t stream) {
+  if (batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
+  if (n_kept < 0 || n_kept > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_kept out of range");
+  if (n_rows < 0 || n_rows > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_rows out of range");
+  if (d < 8 || d % 8 != 0) return fail(TG_ERR_INVALID_ARG, "d must be a positive multiple of 8");
+  if (!cu_seqlens || !cu_kept) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (n_kept == 0) return ok();
+  if (!kept_idx) return fail(TG_ERR_INVALID_ARG, "null kept_idx");
+  if (x_kept_bf16 && (!x_bf16 || !aligned16(x_bf16) || !aligned16(x_kept_bf16)))
+    return fail(TG_ERR_INVALID_ARG, "x and x_kept must be non-null and 16-byte aligned");
+  if (s_kept && !s) return fail(TG_ERR_INVALID_ARG, "s_kept requested without s");
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+  GatherArgs a{};
+  a.x = x_bf16;
+  a.d = d;
+  a.s = s;
+  a.cu_seqlens = cu_seqlens;
+  a.kept_idx = kept_idx;
+  a.cu_kept = cu_kept;
+  a.batch = batch;
+  a.n_kept = n_kept;
+  a.x_kept = x_kept_bf16;
+  a.pos_kept = pos_kept;
+  a.s_kept = s_kept;
+  a.status = di->status;
+  a.num_sms = di->num_sms;
+  cudaError_t e = launch_gather(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+  return ok();
+}
+
+size_t tg_attention_workspace_size(int64_t n_kept, int32_t hq, int32_t hkv, int32_t head_dim,
+                                   int32_t has_k_cache) {
+  if (n_kept <= 0 || hq <= 0 || hkv <= 0 || head_dim <= 0) return 0;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  size_t b = up(static_cast<size_t>(n_kept) * hq * head_dim * 2);
+  if (!has_k_cache) b += up(static_cast<size_t>(n_kept) * hkv * head_dim * 2);
+  return b;
+}
+
+tg_status tg_gated_attention_fwd(const void* q, const void* k, const void* v, const int32_t* pos_kept,
+                                 const float* s_kept, const float* gain, float tau, float rope_theta,
+                                 const int32_t* cu_kept, int32_t batch, int64_t n_kept, int32_t max_kept,
+                                 int32_t hq, int32_t hkv, int32_t head_dim, void* o, float* lse,
+                                 void* k_cache, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+  if (batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
+  if (n_kept < 0 || n_kept > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_kept out of range");
+  if (max_kept < 0) return fail(TG_ERR_INVALID_ARG, "max_kept must be >= 0");
+  if (hq < 1 || hkv < 1 || hq % hkv != 0) return fail(TG_ERR_INVALID_ARG, "hq must be a positive multiple of hkv");
+  if (head_dim != 64 && head_dim != 128) return fail(TG_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (!(tau > 0.0f) || !std::isfinite(tau)) return fail(TG_ERR_INVALID_ARG, "tau must be positive and finite");
+  if (!(rope_theta > 0.0f) || !std::isfinite(rope_theta)) return fail(TG_ERR_INVALID_ARG, "rope_theta must be positive");
+  if (!cu_kept) return fail(TG_ERR_INVALID_ARG, "null cu_kept");
+  if (n_kept == 0) return ok();
+  if (!q || !k || !v || !pos_kept || !s_kept || !gain || !o) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (k_cache && !aligned16(k_cache)))
+    return fail(TG_ERR_INVALID_ARG, "q, k, v, o and k_cache must be 16-byte aligned");
+  const size_t need = tg_attention_workspace_size(n_kept, hq, hkv, head_dim, k_cache ? 1 : 0);
+  if (!workspace || workspace_bytes < need)
+    return fail(TG_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(TG_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (max_kept == 0) return ok();
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* q_rot = ws;
+  void* k_rot = k_cache;
+  if (!k_rot) k_rot = ws + ((static_cast<size_t>(n_kept) * hq * head_dim * 2 + 255) & ~static_cast<size_t>(255));
+
+  RopeFreqs f{};
+  for (int i = 0; i < head_dim / 2; ++i)
+    f.inv_freq[i] = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim);
+  RopeArgs ra{};
+  ra.q = q; ra.k = k; ra.pos = pos_kept; ra.cu_kept = cu_kept; ra.batch = batch; ra.n_kept = n_kept;
+  ra.hq = hq; ra.hkv = hkv; ra.head_dim = head_dim; ra.q_out = q_rot; ra.k_out = k_rot;
+  ra.status = di->status; ra.num_sms = di->num_sms;
+  cudaError_t e = launch_rope(ra, f, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "RoPE kernel launch");
+
+  CUtensorMap mq, mk, mv;
+  const uint32_t box[3] = {64, 1, 128};
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(head_dim), static_cast<uint64_t>(hq), static_cast<uint64_t>(n_kept)};
+    const uint64_t str[2] = {static_cast<uint64_t>(head_dim) * 2, static_cast<uint64_t>(hq) * head_dim * 2};
+    if ((st = make_map(&mq, q_rot, 3, dims, str, box, "q'")) != TG_OK) return st;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(head_dim), static_cast<uint64_t>(hkv), static_cast<uint64_t>(n_kept)};
+    const uint64_t str[2] = {static_cast<uint64_t>(head_dim) * 2, static_cast<uint64_t>(hkv) * head_dim * 2};
+    if ((st = make_map(&mk, k_rot, 3, dims, str, box, "k'")) != TG_OK) return st;
+    if ((st = make_map(&mv, v, 3, dims, str, box, "v")) != TG_OK) return st;
+  }
+  AttnArgs a{};
+  a.pos = pos_kept; a.s_kept = s_kept; a.gain = gain; a.cu_kept = cu_kept; a.batch = batch;
+  a.n_kept = n_kept; a.max_kept = max_kept; a.hq = hq; a.hkv = hkv; a.head_dim = head_dim;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / (std::sqrt(static_cast<double>(head_dim)) * tau));
+  a.o = o; a.lse = lse; a.status = di->status; a.watchdog = g_watchdog_cycles;
+  e = launch_attention(mq, mk, mv, a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+  return ok();
+}
+
+tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual, void* out, int64_t m, int32_t n,
+                         int32_t kdim, cudaStream_t stream) {
+  if (m < 0 || m > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "m out of range");
+  if (n < 16 || n % 16 != 0) return fail(TG_ERR_INVALID_ARG, "n must be a positive multiple of 16");
+  if (kdim < 64 || kdim % 64 != 0) return fail(TG_ERR_INVALID_ARG, "kdim must be a positive multiple of 64");
+  if (m == 0) return ok();
+  if (!a_ptr || !w || !out) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(a_ptr) || !aligned16(w) || !aligned16(out) || (residual && !aligned16(residual)))
+    return fail(TG_ERR_INVALID_ARG, "a, w, residual and out must be 16-byte aligned");
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+  const int bn = n >= 256 ? 256 : n;
+  CUtensorMap ma, mw;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(kdim), static_cast<uint64_t>(m)};
+    const uint64_t str[1] = {static_cast<uint64_t>(kdim) * 2};
+    const uint32_t box[2] = {64, 128};
+    if ((st = make_map(&ma, a_ptr, 2, dims, str, box, "a")) != TG_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(kdim), static_cast<uint64_t>(n)};
+    const uint64_t str[1] = {static_cast<uint64_t>(kdim) * 2};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(bn)};
+    if ((st = make_map(&mw, w, 2, dims, str, box, "w")) != TG_OK) return st;
+  }
+  LinearArgs la{};
+  la.residual = residual; la.out = out; la.m = m; la.n = n; la.kdim = kdim;
+  la.status = di->status; la.watchdog = g_watchdog_cycles;
+  cudaError_t e = launch_linear(ma, mw, la, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "linear kernel launch");
+  return ok();
+}
+
+}  // extern "C"

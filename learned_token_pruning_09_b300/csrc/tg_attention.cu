@@ -1,0 +1,406 @@
+// Token-gated causal attention over the kept tokens (TokenGate, "What is
+// token-gated attention?": each kept token's score is a bias on the attention
+// logits above the gate, scaled by a learnable per-head gain, with a learnable
+// temperature).  Per kept query row i and head h:
+//   logit_ij = (q'_i . k'_j) / (sqrt(D) tau) + gain_h s_j,  pos_j <= pos_i,
+//   o_i = softmax_j(logit_ij) v_j.
+//
+// Flash-attention forward on tcgen05:
+//   * a CTA owns two 128-row query tiles that share one KV head: the two
+//     query heads of a GQA pair on the same rows (hq/hkv even), or two
+//     consecutive row blocks of one head (hq/hkv odd);
+//   * warp 8 streams K and V tiles (128 keys x D) with TMA into a 2-stage
+//     ring, plus each key's score and original position;
+//   * warp 9 issues the MMAs: S_t = Q_t K^T into TMEM (fp32, 128 columns per
+//     tile), then O_t += P_t V with P_t read straight from TMEM;
+//   * warps 0-3 / 4-7 are the softmax warpgroups of tile 0 / tile 1, one
+//     thread per query row: they read S from TMEM, fold scale, log2(e), the
+//     gain-scaled score bias and the causal mask on ORIGINAL positions into
+//     the logits, keep the running max/sum (the max only moves when it grows
+//     by more than 2^8, so O is rarely rescaled), write P as bf16 back into
+//     TMEM over S, and finally normalise O and store it.
+//   TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [384,384+D).
+//
+// Keys are visited only up to the query tile's diagonal: positions strictly
+// increase inside a sequence (checked by the RoPE prologue), so a key after
+// the last query row of the tile has a larger position and is masked anyway.
+#include "tg_common.cuh"
+
+namespace tg {
+
+constexpr int kAttnThreads = 320;   // 8 softmax warps + producer + MMA
+constexpr int kTileRows = 128;
+constexpr int kKvStages = 2;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int kD>
+struct AttnSmem {
+  static constexpr int kTileBytes = kTileRows * kD * 2;   // one 128 x D bf16 tile
+  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t k[kKvStages][kTileBytes];
+  alignas(1024) uint8_t v[kKvStages][kTileBytes];
+  float bias[kKvStages][kTileRows];
+  int32_t kpos[kKvStages][kTileRows];
+  int32_t kmax[kKvStages];
+  uint64_t q_full;
+  uint64_t k_full[kKvStages];
+  uint64_t v_full[kKvStages];
+  uint64_t kv_empty[kKvStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t mma_final;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+template <int kD>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+            const __grid_constant__ CUtensorMap map_v, AttnArgs a, int n_units_per_rb, int pair_heads) {
+  extern __shared__ uint8_t smem_raw[];
+  using Smem = AttnSmem<kD>;
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kBoxes = kD / 64;                 // 64-column TMA boxes per tile
+  constexpr uint32_t kBoxBytes = kTileRows * 64 * 2;
+  constexpr uint32_t kTileBytes = Smem::kTileBytes;
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int group = a.hq / a.hkv;
+
+  // ---- work unit: longest row blocks first -------------------------------
+  const int rb_rev = blockIdx.x / n_units_per_rb;
+  const int rest = blockIdx.x - rb_rev * n_units_per_rb;
+  const int b = rest % a.batch;
+  const int hu = rest / a.batch;
+  const int seq_start = __ldg(a.cu_kept + b);
+  const int seq_len = __ldg(a.cu_kept + b + 1) - seq_start;
+  int head[2], row0[2];
+  int n_rb;
+  if (pair_heads) {
+    n_rb = (a.max_kept + kTileRows - 1) / kTileRows;
+    const int rb = n_rb - 1 - rb_rev;
+    head[0] = 2 * hu; head[1] = 2 * hu + 1;
+    row0[0] = row0[1] = rb * kTileRows;
+  } else {
+    n_rb = (a.max_kept + 2 * kTileRows - 1) / (2 * kTileRows);
+    const int rb = n_rb - 1 - rb_rev;
+    head[0] = head[1] = hu;
+    row0[0] = rb * 2 * kTileRows;
+    row0[1] = row0[0] + kTileRows;
+  }
+  if (seq_len < 0 || seq_start < 0 || static_cast<long long>(seq_start) + seq_len > a.n_kept) {
+    if (threadIdx.x == 0) record_error(a.status, kStatusIndex);
+    return;
+  }
+  if (row0[0] >= seq_len) return;                 // nothing in this sequence
+  const int kvh = head[0] / group;
+  const int row_end = min(seq_len, row0[1] + kTileRows);
+  const int n_kv = (row_end + kTileRows - 1) / kTileRows;
+
+  // ---- setup ---------------------------------------------------------------
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], 128);
+      mbar_init(&sm.o_done[t], 1);
+    }
+    mbar_init(&sm.mma_final, 1);
+    sm.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) { tmem_alloc(&sm.tmem_base, 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const long long wd = a.watchdog;
+
+  if (warp == 8) {
+    // ======================= producer =======================
+    if (lane == 0) {
+      prefetch_tmap(&map_q); prefetch_tmap(&map_k); prefetch_tmap(&map_v);
+      mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_load_3d(sm.q[t] + bx * kBoxBytes, &map_q, &sm.q_full, bx * 64, head[t], seq_start + row0[t]);
+    }
+    int issued = 0;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      const uint32_t use = j >> 1;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&sm.kv_empty[st], (use & 1u) ^ 1u, wd, a.status, kStatusTimeout);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || sm.abort) { sm.abort = 1; break; }
+      int kmax = INT_MIN;
+      for (int c = lane; c < kTileRows; c += 32) {
+        const int kr = j * kTileRows + c;
+        float sv = 0.0f;
+        int pv = INT_MAX;
+        if (kr < seq_len) {
+          sv = __ldg(a.s_kept + seq_start + kr);
+          pv = __ldg(a.pos + seq_start + kr);
+        }
+        sm.bias[st][c] = sv;
+        sm.kpos[st][c] = pv;
+        kmax = max(kmax, pv);
+      }
+      for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+      if (lane == 0) sm.kmax[st] = kmax;
+      __syncwarp();
+      if (lane == 0) {
+        const int krow = seq_start + j * kTileRows;
+        mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_load_3d(sm.k[st] + bx * kBoxBytes, &map_k, &sm.k_full[st], bx * 64, kvh, krow);
+        mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_load_3d(sm.v[st] + bx * kBoxBytes, &map_v, &sm.v_full[st], bx * 64, kvh, krow);
+      }
+      issued = j + 1;
+    }
+    if (lane == 0) {
+      // every issued copy must land before the CTA may leave
+      mbar_wait(&sm.q_full, 0, wd, a.status, kStatusTimeout);
+      for (int st = 0; st < kKvStages && st < issued; ++st) {
+        const int last = ((issued - 1 - st) / kKvStages) * kKvStages + st;
+        const uint32_t par = static_cast<uint32_t>(last >> 1) & 1u;
+        mbar_wait(&sm.k_full[st], par, wd, a.status, kStatusTimeout);
+        mbar_wait(&sm.v_full[st], par, wd, a.status, kStatusTimeout);
+      }
+    }
+  } else if (warp == 9) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, kD, 0, 1);
+      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
+      auto issue_s = [&](int t, int st) {
+        const uint32_t qa = smem_u32(sm.q[t]);
+        const uint32_t ka = smem_u32(sm.k[st]);
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kBoxBytes + (ks & 3) * 32;
+          mma_ss(tS[t], smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                 idesc_qk, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&sm.s_full[t]);
+      };
+      auto issue_pv = [&](int t, int st, int j) {
+        const uint32_t va = smem_u32(sm.v[st]);
+#pragma unroll
+        for (int ks = 0; ks < kTileRows / 16; ++ks) {
+          mma_ts(tO[t], tS[t] + ks * 8, smem_desc_sw128(va + ks * 2048, kBoxBytes, 1024), idesc_pv,
+                 (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(&sm.o_done[t]);
+      };
+      bool ok = mbar_wait(&sm.q_full, 0, wd, a.status, kStatusTimeout);
+      ok = ok && mbar_wait(&sm.k_full[0], 0, wd, a.status, kStatusTimeout);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int st = j & 1;
+        const uint32_t use = j >> 1;
+        const uint32_t pj = j & 1;
+        ok = mbar_wait(&sm.v_full[st], use & 1u, wd, a.status, kStatusTimeout) && !sm.abort;
+        ok = ok && mbar_wait(&sm.p_full[0], pj, wd, a.status, kStatusTimeout) && !sm.abort;
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(0, st, j);
+        const bool more = j + 1 < n_kv;
+        const int st2 = (j + 1) & 1;
+        const uint32_t use2 = (j + 1) >> 1;
+        if (more) {
+          ok = mbar_wait(&sm.k_full[st2], use2 & 1u, wd, a.status, kStatusTimeout);
+          // S_0(j+1) overwrites P_0(j): wait until O_0 += P_0 V_j has finished
+          ok = ok && mbar_wait(&sm.o_done[0], pj, wd, a.status, kStatusTimeout);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(0, st2);
+        }
+        ok = mbar_wait(&sm.p_full[1], pj, wd, a.status, kStatusTimeout) && !sm.abort;
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(1, st, j);
+        mma_commit(&sm.kv_empty[st]);
+        if (more) {
+          ok = mbar_wait(&sm.o_done[1], pj, wd, a.status, kStatusTimeout);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(1, st2);
+        }
+      }
+      if (!ok) sm.abort = 1;
+      mma_commit(&sm.mma_final);
+      mbar_wait(&sm.mma_final, 0, wd, a.status, kStatusTimeout);
+    }
+  } else {
+    // ======================= softmax warpgroups =======================
+    const int t = warp >> 2;                      // tile
+    const int sub = warp & 3;                     // TMEM lane quarter
+    const int r = sub * 32 + lane;                // row inside the tile
+    const int qrow = row0[t] + r;
+    const bool valid = qrow < seq_len;
+    const int qpos = valid ? __ldg(a.pos + seq_start + qrow) : -1;
+    const float gh = __ldg(a.gain + head[t]) * 1.4426950408889634f;
+    const float sl2 = a.scale_log2;
+    const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
+    const uint32_t tS = tmem + static_cast<uint32_t>(t * 128) + lane_off;
+    const uint32_t tO = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_off;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      const uint32_t use = j >> 1;
+      bool w = mbar_wait(&sm.k_full[st], use & 1u, wd, a.status, kStatusTimeout);
+      w = w && mbar_wait(&sm.s_full[t], j & 1u, wd, a.status, kStatusTimeout);
+      ok = __all_sync(0xffffffffu, w) && !sm.abort;
+      if (!ok) break;
+      tc_fence_after();
+      float s[kTileRows];
+      {
+        uint32_t rr[32];
+#pragma unroll
+        for (int c = 0; c < kTileRows / 32; ++c) {
+          tmem_ld32(tS + c * 32, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[i]);
+        }
+      }
+      const bool need_mask = sm.kmax[st] > qpos;
+      float mt = -INFINITY;
+      const float* bias = sm.bias[st];
+      const int* kp = sm.kpos[st];
+#pragma unroll
+      for (int c = 0; c < kTileRows; ++c) {
+        float x = fmaf(s[c], sl2, gh * bias[c]);
+        if (need_mask && kp[c] > qpos) x = -INFINITY;
+        s[c] = x;
+        mt = fmaxf(mt, x);
+      }
+      const float m_new = (mt > m + kRescaleThreshold) ? mt : m;
+      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+      const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_use);
+      float rs = 0.0f;
+#pragma unroll
+      for (int c = 0; c < kTileRows; ++c) {
+        const float p = ex2_approx(s[c] - m_use);
+        s[c] = p;
+        rs += p;
+      }
+      l = l * alpha + rs;
+      m = m_new;
+      // rescale O when this row's max moved (warp-uniform TMEM access)
+      if (__any_sync(0xffffffffu, j > 0 && alpha != 1.0f)) {
+        const bool w2 = __all_sync(0xffffffffu,
+                                   mbar_wait(&sm.o_done[t], (j - 1) & 1u, wd, a.status, kStatusTimeout));
+        if (!w2) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kD / 16; ++c) {
+          uint32_t o16[16];
+          tmem_ld16(tO + c * 16, o16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o16[i] = __float_as_uint(__uint_as_float(o16[i]) * alpha);
+          tmem_st16(tO + c * 16, o16);
+        }
+      }
+      // P (bf16 pairs) over the first 64 columns of S
+#pragma unroll
+      for (int c = 0; c < kTileRows / 32; ++c) {
+        uint32_t p16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) p16[i] = pack_bf16x2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]);
+        tmem_st16(tS + c * 16, p16);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[t]);
+    }
+    if (!ok) sm.abort = 1;
+    // ---- epilogue: O / l -> bf16 ----
+    const bool w3 = ok && __all_sync(0xffffffffu,
+                                     mbar_wait(&sm.o_done[t], (n_kv - 1) & 1u, wd, a.status, kStatusTimeout));
+    if (w3) {
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
+                            (static_cast<size_t>(seq_start + qrow) * a.hq + head[t]) * kD;
+#pragma unroll
+      for (int c = 0; c < kD / 16; ++c) {
+        uint32_t o16[16];
+        tmem_ld16(tO + c * 16, o16);
+        tmem_ld_wait();
+        if (valid) {
+          uint4 v0, v1;
+          uint32_t* p0 = reinterpret_cast<uint32_t*>(&v0);
+          uint32_t* p1 = reinterpret_cast<uint32_t*>(&v1);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            p0[i] = pack_bf16x2(__uint_as_float(o16[2 * i]) * inv, __uint_as_float(o16[2 * i + 1]) * inv);
+            p1[i] = pack_bf16x2(__uint_as_float(o16[8 + 2 * i]) * inv, __uint_as_float(o16[8 + 2 * i + 1]) * inv);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+          dst[0] = v0;
+          dst[1] = v1;
+        }
+      }
+      if (valid && a.lse)
+        a.lse[static_cast<size_t>(head[t]) * a.n_kept + seq_start + qrow] =
+            (((m == -INFINITY) ? 0.0f : m) + __log2f(l)) * 0.6931471805599453f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) { tc_fence_after(); tmem_dealloc(tmem, 512); }
+}
+
+template <int kD>
+static cudaError_t launch_attn_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                 const AttnArgs& a, cudaStream_t st) {
+  const int group = a.hq / a.hkv;
+  const int pair_heads = (group % 2 == 0) ? 1 : 0;
+  int n_rb, units_per_rb;
+  if (pair_heads) {
+    n_rb = (a.max_kept + kTileRows - 1) / kTileRows;
+    units_per_rb = a.batch * (a.hq / 2);
+  } else {
+    n_rb = (a.max_kept + 2 * kTileRows - 1) / (2 * kTileRows);
+    units_per_rb = a.batch * a.hq;
+  }
+  // at least 116 KB so that one CTA (holding all 512 TMEM columns) runs per SM
+  size_t smem = sizeof(AttnSmem<kD>) + 1024;
+  if (smem < 116 * 1024) smem = 116 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<kD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(n_rb) * units_per_rb;
+  if (grid == 0) return cudaSuccess;
+  attn_kernel<kD><<<static_cast<unsigned>(grid), kAttnThreads, smem, st>>>(mq, mk, mv, a, units_per_rb,
+                                                                          pair_heads);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                             const AttnArgs& a, cudaStream_t st) {
+  if (a.n_kept == 0 || a.batch == 0) return cudaSuccess;
+  if (a.head_dim == 128) return launch_attn_d<128>(mq, mk, mv, a, st);
+  return launch_attn_d<64>(mq, mk, mv, a, st);
+}
+
+}  // namespace tg

@@ -1,0 +1,121 @@
+// Internal declarations shared by the C-ABI layer (tg_api.cu) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace tg {
+
+// device status codes (same values as tg_status)
+constexpr unsigned int kStatusTimeout = 5;
+constexpr unsigned int kStatusIndex = 6;
+
+constexpr int kMaxHeadDimHalf = 64;
+
+struct RopeFreqs {
+  double inv_freq[kMaxHeadDimHalf];   // theta^(-2i/D), i < D/2
+};
+
+// ---- gate ------------------------------------------------------------------
+struct GateArgs {
+  const float* b1;          // [h] or null
+  const __nv_bfloat16* w2;  // [h]
+  float b2;
+  const int32_t* cu_seqlens;
+  const int32_t* n_doc;
+  int32_t batch;
+  int64_t n_rows;
+  int32_t d;
+  int32_t h;
+  float* s_out;
+  unsigned int* status;
+  long long watchdog;
+};
+cudaError_t launch_gate(const CUtensorMap& map_x, const CUtensorMap& map_w1, const GateArgs& a,
+                        cudaStream_t st);
+
+// ---- top-K -----------------------------------------------------------------
+struct TopkArgs {
+  const float* s;
+  const int32_t* cu_seqlens;
+  const int32_t* n_doc;
+  const int32_t* k;
+  int32_t batch;
+  int32_t max_n_doc;
+  int32_t* kept_idx;
+  int32_t* cu_kept;
+  unsigned int* status;
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
+
+// ---- gather ----------------------------------------------------------------
+struct GatherArgs {
+  const void* x;
+  int32_t d;
+  const float* s;
+  const int32_t* cu_seqlens;
+  const int32_t* kept_idx;
+  const int32_t* cu_kept;
+  int32_t batch;
+  int64_t n_kept;
+  void* x_kept;
+  int32_t* pos_kept;
+  float* s_kept;
+  unsigned int* status;
+  int num_sms;
+};
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t st);
+
+// ---- RoPE prologue ---------------------------------------------------------
+struct RopeArgs {
+  const void* q;        // [T, hq, D]
+  const void* k;        // [T, hkv, D]
+  const int32_t* pos;   // [T]
+  const int32_t* cu_kept;
+  int32_t batch;
+  int64_t n_kept;
+  int32_t hq, hkv, head_dim;
+  void* q_out;
+  void* k_out;
+  unsigned int* status;
+  int num_sms;
+};
+cudaError_t launch_rope(const RopeArgs& a, const RopeFreqs& f, cudaStream_t st);
+
+// ---- attention -------------------------------------------------------------
+struct AttnArgs {
+  const int32_t* pos;
+  const float* s_kept;
+  const float* gain;
+  const int32_t* cu_kept;
+  int32_t batch;
+  int64_t n_kept;
+  int32_t max_kept;
+  int32_t hq, hkv, head_dim;
+  float scale_log2;     // log2(e) / (sqrt(D) * tau)
+  void* o;
+  float* lse;
+  unsigned int* status;
+  long long watchdog;
+};
+cudaError_t launch_attention(const CUtensorMap& map_q, const CUtensorMap& map_k,
+                             const CUtensorMap& map_v, const AttnArgs& a, cudaStream_t st);
+
+// ---- linear ----------------------------------------------------------------
+struct LinearArgs {
+  const void* residual;
+  void* out;
+  int64_t m;
+  int32_t n;
+  int32_t kdim;
+  unsigned int* status;
+  long long watchdog;
+};
+cudaError_t launch_linear(const CUtensorMap& map_a, const CUtensorMap& map_w, const LinearArgs& a,
+                          cudaStream_t st);
+
+}  // namespace tg

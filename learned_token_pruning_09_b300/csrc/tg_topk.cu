@@ -1,0 +1,238 @@
+// Top-K selection of document tokens per sequence, question tokens always
+// kept (TokenGate gate module: "a top-K selector keeps the tokens with the
+// highest score"; "only the document part of the prompt is prunable").
+//
+// One thread-block cluster of kCluster CTAs per sequence.  Each CTA owns a
+// contiguous slice of the sequence's document rows, converts its scores to
+// 32-bit order keys once (kept in shared memory when they fit) and the
+// cluster runs an MSB-first radix select (4 passes x 8 bits): every CTA
+// builds a 256-bin histogram of its slice, the histograms are summed across
+// the cluster through distributed shared memory, and every CTA derives the
+// same next digit.  The result is the exact K-th key and the number of keys
+// equal to it that are taken (lowest row index first).  A final ordered
+// compaction (warp ballots + prefix sums, slice offsets exchanged across the
+// cluster) writes the kept rows in ascending order, then the question rows.
+#include <cooperative_groups.h>
+
+#include "tg_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace tg {
+
+constexpr int kTopkCluster = 8;
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkMaxSmemKeys = (200 * 1024) / 4;
+
+// Monotone map float -> uint32: a larger key means a larger score.  -0.0 is
+// folded onto +0.0 (so the two tie and the lower index wins), every NaN maps
+// to 0, below -inf (0x007FFFFF).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0u;
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+struct TopkShared {
+  uint32_t hist[2][256];
+  uint32_t warp_tot[8];
+  uint32_t warp_gt[kTopkWarps];
+  uint32_t warp_eq[kTopkWarps];
+  uint32_t cta_gt;          // read by the other CTAs of the cluster
+  uint32_t cta_eq;
+  uint32_t digit;
+  int32_t remaining;
+  int32_t found;
+  long long base;           // first output slot of this sequence
+};
+
+template <bool kSmemKeys>
+__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 1)
+topk_kernel(TopkArgs a) {
+  extern __shared__ __align__(16) uint32_t keys_smem[];
+  __shared__ TopkShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int b = blockIdx.x / kTopkCluster;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+
+  const int lo = a.cu_seqlens[b];
+  const int hi = a.cu_seqlens[b + 1];
+  const int nd = a.n_doc[b];
+  const int kb = a.k[b];
+  // every CTA of the cluster sees the same values, so all leave together
+  if (hi < lo || nd < 0 || nd > hi - lo || nd > a.max_n_doc || kb < 0) {
+    if (rank == 0 && tid == 0) record_error(a.status, kStatusIndex);
+    return;
+  }
+  const int ke = min(kb, nd);
+  const int nq = hi - lo - nd;
+
+  // output offset of this sequence: sum of the kept lengths of earlier ones
+  if (tid == 0) sh.base = 0;
+  __syncthreads();
+  {
+    long long part = 0;
+    for (int bb = tid; bb < b; bb += kTopkThreads) {
+      const int l2 = a.cu_seqlens[bb], h2 = a.cu_seqlens[bb + 1], n2 = a.n_doc[bb], k2 = a.k[bb];
+      part += static_cast<long long>(min(max(k2, 0), n2)) + (h2 - l2 - n2);
+    }
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(0xffffffffu, part, o);
+    if (lane == 0 && part) atomicAdd(reinterpret_cast<unsigned long long*>(&sh.base),
+                                     static_cast<unsigned long long>(part));
+  }
+  __syncthreads();
+  const long long base = sh.base;
+  if (rank == 0 && tid == 0) {
+    a.cu_kept[b + 1] = static_cast<int32_t>(base + ke + nq);
+    if (b == 0) a.cu_kept[0] = 0;
+  }
+  // question rows, spread over the cluster
+  for (int t = rank * kTopkThreads + tid; t < nq; t += kTopkCluster * kTopkThreads)
+    a.kept_idx[base + ke + t] = lo + nd + t;
+
+  // this CTA's slice of the document
+  const int chunk = (nd + kTopkCluster - 1) / kTopkCluster;
+  const int s0 = min(nd, rank * chunk);
+  const int n_loc = min(nd, s0 + chunk) - s0;
+  const float* src = a.s + lo + s0;
+  int32_t* out = a.kept_idx + base;
+
+  if (ke == nd) {             // whole document kept (also nd == 0)
+    for (int i = tid; i < n_loc; i += kTopkThreads) out[s0 + i] = lo + s0 + i;
+    return;
+  }
+  if (ke == 0) return;        // question only
+
+  if (kSmemKeys) {
+    for (int i = tid; i < n_loc; i += kTopkThreads) keys_smem[i] = order_key(src[i]);
+  }
+  auto key_at = [&](int i) -> uint32_t {
+    if (kSmemKeys) return keys_smem[i];
+    return order_key(__ldg(src + i));
+  };
+
+  // ---- radix select, 4 passes of 8 bits --------------------------------
+  uint32_t prefix = 0, mask = 0;
+  int remaining = ke;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    uint32_t* h = sh.hist[pass & 1];
+    if (tid < 256) h[tid] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_loc; i += kTopkThreads) {
+      const uint32_t key = key_at(i);
+      if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
+    }
+    cluster.sync();
+    // bin tid summed over the cluster; inclusive suffix sums over bins
+    uint32_t tot = 0;
+    if (tid < 256) {
+      for (int r = 0; r < kTopkCluster; ++r) tot += cluster.map_shared_rank(h, r)[tid];
+    }
+    uint32_t suf = tot;
+    if (warp < 8) {
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += v;
+      }
+      if (lane == 0) sh.warp_tot[warp] = suf;
+    }
+    if (tid == 0) sh.found = 0;
+    __syncthreads();
+    if (warp < 8) {
+      for (int w2 = warp + 1; w2 < 8; ++w2) suf += sh.warp_tot[w2];
+      // digit d is the one with suffix(d+1) < remaining <= suffix(d)
+      const uint32_t above = suf - tot;
+      if (static_cast<uint32_t>(remaining) <= suf && above < static_cast<uint32_t>(remaining)) {
+        sh.digit = static_cast<uint32_t>(tid);
+        sh.remaining = remaining - static_cast<int>(above);
+        sh.found = 1;
+      }
+    }
+    __syncthreads();
+    if (!sh.found) {          // counts inconsistent: cannot happen for valid input
+      if (tid == 0) record_error(a.status, kStatusIndex);
+      cluster.sync();
+      return;
+    }
+    prefix |= sh.digit << shift;
+    mask |= 255u << shift;
+    remaining = sh.remaining;
+  }
+  const uint32_t kth = prefix;     // exact K-th largest key
+  const int take_eq = remaining;   // keys equal to kth that are kept
+
+  // ---- ordered compaction ---------------------------------------------
+  const int seg = ((n_loc + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
+  const int w0 = min(n_loc, warp * seg);
+  const int w1 = min(n_loc, w0 + seg);
+  uint32_t gt = 0, eq = 0;
+  for (int i = w0 + lane; i < w1; i += 32) {
+    const uint32_t key = key_at(i);
+    gt += key > kth;
+    eq += key == kth;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    gt += __shfl_down_sync(0xffffffffu, gt, o);
+    eq += __shfl_down_sync(0xffffffffu, eq, o);
+  }
+  if (lane == 0) { sh.warp_gt[warp] = gt; sh.warp_eq[warp] = eq; }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t g = 0, e = 0;
+    for (int w2 = 0; w2 < kTopkWarps; ++w2) { g += sh.warp_gt[w2]; e += sh.warp_eq[w2]; }
+    sh.cta_gt = g;
+    sh.cta_eq = e;
+  }
+  cluster.sync();
+  // offsets of this CTA's slice (CTAs of lower rank come first)
+  uint32_t gt_before = 0, eq_before = 0;
+  for (int r = 0; r < rank; ++r) {
+    const TopkShared* o = cluster.map_shared_rank(&sh, r);
+    gt_before += o->cta_gt;
+    eq_before += o->cta_eq;
+  }
+  const int eq_take_cta = max(0, min(static_cast<int>(sh.cta_eq), take_eq - static_cast<int>(eq_before)));
+  const long long cta_out = static_cast<long long>(gt_before) + min(static_cast<int>(eq_before), take_eq);
+  uint32_t gt_w = 0, eq_w = 0;
+  for (int w2 = 0; w2 < warp; ++w2) { gt_w += sh.warp_gt[w2]; eq_w += sh.warp_eq[w2]; }
+  long long pos = cta_out + gt_w + min(static_cast<int>(eq_w), eq_take_cta);
+  int eq_seen = static_cast<int>(eq_w);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = (i < w1) ? key_at(i) : 0u;
+    const bool is_eq = (i < w1) && key == kth;
+    const uint32_t eq_bal = __ballot_sync(0xffffffffu, is_eq);
+    const int my_eq_rank = eq_seen + __popc(eq_bal & lt_mask);
+    const bool keep = (i < w1) && (key > kth || (is_eq && my_eq_rank < eq_take_cta));
+    const uint32_t keep_bal = __ballot_sync(0xffffffffu, keep);
+    if (keep) out[pos + __popc(keep_bal & lt_mask)] = lo + s0 + i;
+    pos += __popc(keep_bal);
+    eq_seen += __popc(eq_bal);
+  }
+  cluster.sync();   // no CTA leaves while another may still read its counts
+}
+
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
+  if (a.batch == 0) return cudaSuccess;
+  const int chunk = (a.max_n_doc + kTopkCluster - 1) / kTopkCluster;
+  const dim3 grid(static_cast<unsigned>(a.batch) * kTopkCluster);
+  if (chunk <= kTopkMaxSmemKeys) {
+    const size_t smem = static_cast<size_t>(max(chunk, 4)) * sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    topk_kernel<true><<<grid, kTopkThreads, smem, st>>>(a);
+  } else {
+    topk_kernel<false><<<grid, kTopkThreads, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace tg

@@ -1,0 +1,239 @@
+"""Python binding of libtokengate.so (C ABI in include/tokengate.h).
+
+Argument marshalling only: each ``tg_*`` function here takes torch CUDA
+tensors, checks dtypes/shapes/contiguity, allocates outputs with torch when
+the caller passes none, and calls the C entry point of the same name on the
+current CUDA stream.  Every step of the path runs in the library's kernels;
+there is no fallback: if the library is missing or fails to load, importing
+this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtokengate.so")
+
+TG_OK = 0
+TG_ERR_INVALID_ARG = 1
+TG_ERR_UNSUPPORTED = 2
+TG_ERR_WORKSPACE = 3
+TG_ERR_CUDA = 4
+TG_ERR_TIMEOUT = 5
+TG_ERR_DEVICE_INDEX = 6
+
+_STATUS_NAMES = {0: "TG_OK", 1: "TG_ERR_INVALID_ARG", 2: "TG_ERR_UNSUPPORTED", 3: "TG_ERR_WORKSPACE",
+                 4: "TG_ERR_CUDA", 5: "TG_ERR_TIMEOUT", 6: "TG_ERR_DEVICE_INDEX"}
+
+
+class TokenGateError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        super().__init__(f"{where}: {_STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libtokengate.so is not built ({LIB_PATH}); run "
+                          "`python -m learned_token_pruning_09_b300.build`")
+    return ctypes.CDLL(LIB_PATH)
+
+
+lib = _load()
+
+_vp, _i64, _i32, _f32, _sz, _ll = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                   ctypes.c_size_t, ctypes.c_longlong)
+_SIGS = {
+    "tg_gate_score": [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _f32, _i32, _vp, _vp],
+    "tg_topk_select": [_vp, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp],
+    "tg_gather_kept": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp],
+    "tg_gated_attention_fwd": [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _i32, _i64, _i32, _i32, _i32,
+                               _i32, _vp, _vp, _vp, _vp, _sz, _vp],
+    "tg_attention_workspace_size": [_i64, _i32, _i32, _i32, _i32],
+    "tg_linear_bf16": [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp],
+    "tg_check_device_status": [_vp],
+    "tg_set_watchdog_cycles": [_ll],
+    "tg_last_error_string": [],
+    "tg_version": [],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+lib.tg_attention_workspace_size.restype = ctypes.c_size_t
+lib.tg_last_error_string.restype = ctypes.c_char_p
+lib.tg_version.restype = ctypes.c_char_p
+lib.tg_set_watchdog_cycles.restype = None
+
+
+def _check(code: int, where: str) -> None:
+    if code != TG_OK:
+        raise TokenGateError(code, where, lib.tg_last_error_string().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, name: str, ndim: Optional[int] = None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def version() -> str:
+    return lib.tg_version().decode()
+
+
+def tg_set_watchdog_cycles(cycles: int) -> None:
+    lib.tg_set_watchdog_cycles(int(cycles))
+
+
+def tg_check_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return lib.tg_check_device_status(_stream(stream))
+
+
+def tg_gate_score(x: torch.Tensor, cu_seqlens: torch.Tensor, n_doc: torch.Tensor, w1: torch.Tensor,
+                  b1: Optional[torch.Tensor], w2: torch.Tensor, b2: float,
+                  s_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Gate scores s [n_rows] fp32 (logsigmoid of the gate MLP logit for
+    document rows, 0 for question rows)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(w1, torch.bfloat16, "w1", 2)
+    _need(w2, torch.bfloat16, "w2", 1)
+    _need(cu_seqlens, torch.int32, "cu_seqlens", 1)
+    _need(n_doc, torch.int32, "n_doc", 1)
+    if b1 is not None:
+        _need(b1, torch.float32, "b1", 1)
+    n_rows, d = x.shape
+    h = w1.shape[0]
+    if w1.shape[1] != d or w2.shape[0] != h:
+        raise ValueError("w1 must be [h, d] and w2 [h]")
+    if s_out is None:
+        s_out = torch.empty(n_rows, dtype=torch.float32, device=x.device)
+    _need(s_out, torch.float32, "s_out", 1)
+    _check(lib.tg_gate_score(_ptr(x), n_rows, d, _ptr(cu_seqlens), _ptr(n_doc), n_doc.shape[0], _ptr(w1),
+                             _ptr(b1), _ptr(w2), float(b2), h, _ptr(s_out), _stream(stream)), "tg_gate_score")
+    return s_out
+
+
+def kept_lengths(seqlens: Sequence[int], n_doc: Sequence[int], k: Sequence[int]):
+    """Host-side kept length per sequence: min(k, n_doc) + question length."""
+    return [min(int(kb), int(nd)) + int(sl) - int(nd) for sl, nd, kb in zip(seqlens, n_doc, k)]
+
+
+def tg_topk_select(s: torch.Tensor, cu_seqlens: torch.Tensor, n_doc: torch.Tensor, k: torch.Tensor,
+                   max_n_doc: int, n_kept: int, kept_idx: Optional[torch.Tensor] = None,
+                   cu_kept: Optional[torch.Tensor] = None, stream=None):
+    """Kept row ids [n_kept] int32 and cu_kept [batch+1] int32.  ``n_kept``
+    (host) sizes the output: sum over sequences of min(k, n_doc) + n_q."""
+    _need(s, torch.float32, "s", 1)
+    for t, nme in ((cu_seqlens, "cu_seqlens"), (n_doc, "n_doc"), (k, "k")):
+        _need(t, torch.int32, nme, 1)
+    batch = n_doc.shape[0]
+    if kept_idx is None:
+        kept_idx = torch.empty(max(n_kept, 1), dtype=torch.int32, device=s.device)[:n_kept]
+    if cu_kept is None:
+        cu_kept = torch.empty(batch + 1, dtype=torch.int32, device=s.device)
+    _check(lib.tg_topk_select(_ptr(s), s.shape[0], _ptr(cu_seqlens), _ptr(n_doc), _ptr(k), batch,
+                              int(max_n_doc), _ptr(kept_idx), _ptr(cu_kept), _stream(stream)), "tg_topk_select")
+    return kept_idx, cu_kept
+
+
+def tg_gather_kept(x: Optional[torch.Tensor], s: Optional[torch.Tensor], cu_seqlens: torch.Tensor,
+                   kept_idx: torch.Tensor, cu_kept: torch.Tensor, n_kept: int, d: Optional[int] = None,
+                   x_kept: Optional[torch.Tensor] = None, pos_kept: Optional[torch.Tensor] = None,
+                   s_kept: Optional[torch.Tensor] = None, want=("x", "pos", "s"), stream=None):
+    """x_kept [n_kept, d] bf16, pos_kept [n_kept] int32, s_kept [n_kept] fp32."""
+    _need(cu_seqlens, torch.int32, "cu_seqlens", 1)
+    _need(cu_kept, torch.int32, "cu_kept", 1)
+    _need(kept_idx, torch.int32, "kept_idx", 1)
+    dev = kept_idx.device
+    if x is not None:
+        _need(x, torch.bfloat16, "x", 2)
+        d = x.shape[1]
+    n_rows = x.shape[0] if x is not None else (s.shape[0] if s is not None else 0)
+    if "x" in want and x_kept is None and x is not None:
+        x_kept = torch.empty((n_kept, d), dtype=torch.bfloat16, device=dev)
+    if "pos" in want and pos_kept is None:
+        pos_kept = torch.empty(n_kept, dtype=torch.int32, device=dev)
+    if "s" in want and s_kept is None and s is not None:
+        s_kept = torch.empty(n_kept, dtype=torch.float32, device=dev)
+    _check(lib.tg_gather_kept(_ptr(x), n_rows, int(d or 8), _ptr(s), _ptr(cu_seqlens), _ptr(kept_idx),
+                              _ptr(cu_kept), cu_kept.shape[0] - 1, int(n_kept), _ptr(x_kept), _ptr(pos_kept),
+                              _ptr(s_kept), _stream(stream)), "tg_gather_kept")
+    return x_kept, pos_kept, s_kept
+
+
+def tg_attention_workspace_size(n_kept: int, hq: int, hkv: int, head_dim: int, has_k_cache: bool) -> int:
+    return int(lib.tg_attention_workspace_size(int(n_kept), hq, hkv, head_dim, 1 if has_k_cache else 0))
+
+
+def tg_gated_attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pos_kept: torch.Tensor,
+                           s_kept: torch.Tensor, gain: torch.Tensor, tau: float, rope_theta: float,
+                           cu_kept: torch.Tensor, max_kept: int, o: Optional[torch.Tensor] = None,
+                           lse: Optional[torch.Tensor] = None, want_lse: bool = False,
+                           k_cache: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                           stream=None):
+    """o [T, hq, D] bf16 (and lse [hq, T] fp32 when requested or given)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k, torch.bfloat16, "k", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    _need(pos_kept, torch.int32, "pos_kept", 1)
+    _need(s_kept, torch.float32, "s_kept", 1)
+    _need(gain, torch.float32, "gain", 1)
+    _need(cu_kept, torch.int32, "cu_kept", 1)
+    t, hq, dh = q.shape
+    hkv = k.shape[1]
+    if k.shape != (t, hkv, dh) or v.shape != (t, hkv, dh):
+        raise ValueError("k and v must be [T, hkv, D] matching q")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((hq, t), dtype=torch.float32, device=q.device)
+    if k_cache is not None:
+        _need(k_cache, torch.bfloat16, "k_cache", 3)
+    need = tg_attention_workspace_size(t, hq, hkv, dh, k_cache is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(lib.tg_gated_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(pos_kept), _ptr(s_kept), _ptr(gain),
+                                      float(tau), float(rope_theta), _ptr(cu_kept), cu_kept.shape[0] - 1, t,
+                                      int(max_kept), hq, hkv, dh, _ptr(o), _ptr(lse), _ptr(k_cache),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)),
+           "tg_gated_attention_fwd")
+    return (o, lse) if lse is not None else o
+
+
+def tg_linear_bf16(a: torch.Tensor, w: torch.Tensor, residual: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out = a w^T (+ residual), bf16 [m, n]."""
+    _need(a, torch.bfloat16, "a", 2)
+    _need(w, torch.bfloat16, "w", 2)
+    m, kd = a.shape
+    n = w.shape[0]
+    if w.shape[1] != kd:
+        raise ValueError("w must be [n, k]")
+    if residual is not None:
+        _need(residual, torch.bfloat16, "residual", 2)
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    _check(lib.tg_linear_bf16(_ptr(a), _ptr(w), _ptr(residual), _ptr(out), m, n, kd, _stream(stream)),
+           "tg_linear_bf16")
+    return out

@@ -130,10 +130,11 @@ def gate_score(x_bits: np.ndarray, cu_seqlens: Sequence[int], n_doc: Sequence[in
 
 def _rank_key(value: float, index: int):
     """Sort key for 'larger score first, then lower index'.  -0.0 and +0.0
-    compare equal (float comparison); NaN ranks after every number."""
+    compare equal (float comparison); NaN ranks after every number,
+    including -inf."""
     if math.isnan(value):
-        return (math.inf, index)
-    return (-value, index)
+        return (1, 0.0, index)
+    return (0, -value, index)
 
 
 def topk_select(s: np.ndarray, cu_seqlens: Sequence[int], n_doc: Sequence[int],
@@ -230,14 +231,13 @@ def gated_attention(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
     Returns (o float64 [T, hq, D], lse float64 [hq, T]); rows not requested
     are NaN."""
     dec = (lambda a: np.asarray(a, np.float64)) if q_is_f64 else bf16_decode
-    q, k, v = dec(q_bits), dec(k_bits), dec(v_bits)
-    t, hq, d = q.shape
+    k, v = dec(k_bits), dec(v_bits)
+    t, hq, d = np.asarray(q_bits).shape
     hkv = k.shape[1]
     group = hq // hkv
     pos = np.asarray(pos, dtype=np.int64)
     s_kept = np.asarray(s_kept, dtype=np.float64)
     gain = np.asarray(gain, dtype=np.float64)
-    qr = rope(q, pos, theta)
     kr = rope(k, pos, theta)
     scale = 1.0 / (math.sqrt(d) * float(tau))
     seq_of = np.empty(t, dtype=np.int64)
@@ -247,13 +247,14 @@ def gated_attention(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
     o = np.full((t, hq, d), np.nan)
     lse = np.full((hq, t), np.nan)
     for i in want:
+        qr_i = rope(dec(np.asarray(q_bits)[i:i + 1]), pos[i:i + 1], theta)[0]   # [hq, D]
         b = seq_of[i]
         lo, hi = int(cu_kept[b]), int(cu_kept[b + 1])
         js = np.arange(lo, hi)
         js = js[pos[lo:hi] <= pos[i]]              # causal on original positions
         for h in range(hq):
             g = h // group
-            logit = (kr[js, g, :] @ qr[i, h, :]) * scale + gain[h] * s_kept[js]
+            logit = (kr[js, g, :] @ qr_i[h, :]) * scale + gain[h] * s_kept[js]
             m = logit.max()
             e = np.exp(logit - m)
             den = e.sum()

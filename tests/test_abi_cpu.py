@@ -1,0 +1,114 @@
+"""The C-ABI library loads without a GPU, exports every symbol declared in
+include/tokengate.h, and rejects invalid arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tokengate.h")
+
+
+@pytest.fixture(scope="module")
+def tg():
+    from learned_token_pruning_09_b300 import build
+    build.build()
+    from learned_token_pruning_09_b300 import tokengate
+    return tokengate
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    syms = declared_symbols()
+    for s in ("tg_gate_score", "tg_topk_select", "tg_gather_kept", "tg_gated_attention_fwd"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(tg):
+    out = subprocess.run(["nm", "-D", "--defined-only", tg.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (tg_[a-z0-9_]+)\b", out))
+    missing = [s for s in declared_symbols() if s not in exported]
+    assert not missing, missing
+    for s in declared_symbols():
+        assert hasattr(tg.lib, s)
+
+
+def test_version_and_error_string(tg):
+    assert "sm_103a" in tg.version()
+    assert isinstance(tg.lib.tg_last_error_string(), bytes)
+
+
+def test_workspace_size(tg):
+    ws = tg.tg_attention_workspace_size(8256, 16, 8, 128, True)
+    assert ws == ((8256 * 16 * 128 * 2 + 255) // 256) * 256
+    ws2 = tg.tg_attention_workspace_size(8256, 16, 8, 128, False)
+    assert ws2 == ws + ((8256 * 8 * 128 * 2 + 255) // 256) * 256
+    assert tg.tg_attention_workspace_size(0, 16, 8, 128, True) == 0
+
+
+def _c(v):
+    return ctypes.c_void_p(v)
+
+
+def test_host_validation_rejects_before_launch(tg):
+    L = tg.lib
+    p = _c(256)      # a fake 16-byte-aligned address: never dereferenced
+    # gate: d not a multiple of 64, h out of range, null weights, misalignment
+    assert L.tg_gate_score(p, 10, 63, p, p, 1, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 1, p, None, p, 0.0, 8, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 1, p, None, p, 0.0, 272, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 1, None, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(_c(258), 10, 64, p, p, 1, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 0, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 1, p, None, p, float("nan"), 64, p, None) == tg.TG_ERR_INVALID_ARG
+    assert b"multiple of 16" in L.tg_last_error_string() or L.tg_last_error_string()
+    # top-K
+    assert L.tg_topk_select(p, 10, p, p, p, -1, 5, p, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select(p, 10, p, p, p, 1, -1, p, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select(p, 10, None, p, p, 1, 5, p, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select(p, 10, p, p, p, 0, 5, p, p, None) == tg.TG_OK       # empty batch: no-op
+    # gather
+    assert L.tg_gather_kept(p, 10, 12, p, p, p, p, 1, 4, p, p, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gather_kept(p, 10, 64, p, p, None, p, 1, 4, p, p, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gather_kept(p, 10, 64, p, p, p, p, 0, 4, p, p, p, None) == tg.TG_ERR_INVALID_ARG
+    # attention
+    args = dict(q=p, k=p, v=p, pos=p, s=p, g=p, tau=1.0, th=1e6, cu=p, b=1, t=100, mk=100, hq=16, hkv=8, d=128,
+                o=p, lse=None, kc=None, ws=p, wsb=1 << 30)
+
+    def attn(**kw):
+        a = dict(args, **kw)
+        return L.tg_gated_attention_fwd(a["q"], a["k"], a["v"], a["pos"], a["s"], a["g"], a["tau"], a["th"],
+                                        a["cu"], a["b"], a["t"], a["mk"], a["hq"], a["hkv"], a["d"], a["o"],
+                                        a["lse"], a["kc"], a["ws"], a["wsb"], None)
+    assert attn(hq=12, hkv=8) == tg.TG_ERR_INVALID_ARG
+    assert attn(d=96) == tg.TG_ERR_UNSUPPORTED
+    assert attn(tau=0.0) == tg.TG_ERR_INVALID_ARG
+    assert attn(tau=float("inf")) == tg.TG_ERR_INVALID_ARG
+    assert attn(wsb=10) == tg.TG_ERR_WORKSPACE
+    assert attn(ws=None) == tg.TG_ERR_WORKSPACE
+    assert attn(ws=_c(272)) == tg.TG_ERR_INVALID_ARG        # not 256-byte aligned
+    assert attn(o=None) == tg.TG_ERR_INVALID_ARG
+    assert attn(q=_c(264)) == tg.TG_ERR_INVALID_ARG         # not 16-byte aligned
+    assert attn(b=0) == tg.TG_ERR_INVALID_ARG
+    assert attn(t=0) == tg.TG_OK                            # nothing to do
+    # linear
+    assert L.tg_linear_bf16(p, p, None, p, 10, 24, 64, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_linear_bf16(p, p, None, p, 10, 32, 96, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_linear_bf16(p, None, None, p, 10, 32, 64, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_linear_bf16(p, p, None, p, 0, 32, 64, None) == tg.TG_OK
+
+
+def test_binding_refuses_cpu_tensors(tg):
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises((ValueError, TypeError)):
+        tg.tg_linear_bf16(x, x)

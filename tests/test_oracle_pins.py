@@ -186,6 +186,9 @@ def test_topk_special_cases():
     s = np.array([np.nan, -5.0, np.nan, -9.0], np.float32)
     assert oracle.topk_select(s, [0, 4], [4], [2])[0].tolist() == [1, 3]
     assert oracle.topk_select(s, [0, 4], [4], [3])[0].tolist() == [0, 1, 3]
+    s = np.array([np.nan, -np.inf, -1.0, np.nan], np.float32)
+    assert oracle.topk_select(s, [0, 4], [4], [2])[0].tolist() == [1, 2]
+    assert oracle.topk_select(s, [0, 4], [4], [3])[0].tolist() == [0, 1, 2]
     # empty document
     assert oracle.topk_select(np.zeros(3, np.float32), [0, 3], [0], [4])[0].tolist() == [0, 1, 2]
 
