@@ -1,0 +1,535 @@
+#!/usr/bin/env python3
+"""Benchmark of the TokenGate pruned-prefill hot path on B300.
+
+One step = one pass of the whole path over one synthetic batch, inputs
+resident in HBM: gate MLP scores -> top-K (question kept) -> gather of kept
+rows/positions/scores -> the token-gated attention layers above the gate.
+For the long-context workload (default) that is 27 layers, each
+q/k/v projections -> RoPE + token-gated attention -> output projection with
+the residual add; single-layer workloads run one attention layer on seeded
+q/k/v.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   (the CPU oracle, bounded sample)
+
+Prints ONE JSON line (rank 0).  ``value`` is gated-attention TFLOP/s:
+causal-triangle flops 2*hq*D*T(T+1) per layer over the measured attention
+time (RoPE prologue + attention kernel), summed over ranks.
+``gate_topk_gather`` gives the GB/s of the first three steps on algorithmic
+bytes.  Every call is captured once in a CUDA graph and replayed, so the
+device time excludes host launch cost; ``e2e`` instead runs the public
+Python API with host buffers (copies in the timed region).  L2 is flushed
+(256 MB written) before every timed step.  N > 1 runs independent replicas:
+the workload is one sequence and the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "gated-attention TFLOP/s and ms/layer at 16k–128k; gate+top-K+gather GB/s"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "long-128k"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def attention_flops(kept_lens, hq, d):
+    """Causal-triangle flops of one layer: QK^T and PV, 2 flops per MAC,
+    over the (i, j <= i) pairs: 2 * hq * D * T (T + 1) per sequence."""
+    return float(sum(2.0 * hq * d * t * (t + 1) for t in kept_lens))
+
+
+def path_bytes(shape):
+    """Algorithmic HBM bytes of gate + top-K + gather: residuals read once
+    (2 d per row), scores written and read (4 + 4 per row), kept ids
+    written and read (4 + 4 per kept row), kept rows read and written
+    (2 * 2 d per kept row), kept positions and scores written (8 per kept
+    row)."""
+    n, t, d = shape.n_rows, shape.n_kept, shape.d
+    return float(n * 2 * d + n * 8 + t * 8 + t * 4 * d + t * 8)
+
+
+def proj_flops(shape):
+    t, d = shape.n_kept, shape.d
+    return 2.0 * t * d * (shape.hq + 2 * shape.hkv) * shape.head_dim + 2.0 * t * shape.hq * shape.head_dim * d
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons, pw = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+                pw.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------
+# inputs
+# ---------------------------------------------------------------------------
+
+
+def make_inputs(shape):
+    from learned_token_pruning_09_b300 import synth
+    inp = {"x": synth.residuals(shape), "p": synth.gate_weights(shape), "s_draw": synth.score_draws(shape)}
+    if shape.with_proj:
+        inp["layers"] = [synth.layer_params(shape, i) for i in range(shape.n_layers)]
+    else:
+        inp["ai"] = synth.attention_inputs(shape)
+    return inp
+
+
+def workload_config(shape):
+    return {"workload": shape.name, "batch": shape.batch, "n_doc": shape.n_doc, "n_q": shape.n_q,
+            "k": shape.k, "kept_tokens": shape.n_kept, "d": shape.d, "gate_h": shape.h, "hq": shape.hq,
+            "hkv": shape.hkv, "head_dim": shape.head_dim, "layers_above_gate": shape.n_layers,
+            "projections": shape.with_proj, "rope_theta": 1e6,
+            "l2": "flushed (256 MB write) before every timed step", "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm / CPU baseline: the oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+
+def oracle_step_sample(shape, inputs, rng, n_gate_rows=256, n_attn_rows=16):
+    """One bounded sample of the workload through the oracle: gate scores of
+    ``n_gate_rows`` document rows, top-K over the full score vector, the
+    gather, and attention outputs of ``n_attn_rows`` query rows (all heads)
+    of one layer (for the stacked workload: layer 0, keys and values
+    projected for every kept row).  Returns (seconds, attention flops of the
+    sampled rows)."""
+    import oracle
+    x, p, s_full = inputs["x"], inputs["p"], inputs["s_draw"]
+    t0 = time.perf_counter()
+    rows = rng.choice(shape.n_doc[0], n_gate_rows, replace=False)
+    oracle.gate_score(x, shape.cu_seqlens, shape.n_doc, p["w1"], p["b1"], p["w2"], p["b2"], rows=rows)
+    kept, cu_kept = oracle.topk_select(s_full, shape.cu_seqlens, shape.n_doc, shape.k)
+    xk, pos, sk = oracle.gather_kept(x, s_full, shape.cu_seqlens, kept, cu_kept)
+    t_rows = rng.choice(len(kept), n_attn_rows, replace=False)
+    if shape.with_proj:
+        lp = inputs["layers"][0]
+        oracle.stacked_layer(oracle.bf16_decode(xk), lp["w_qkv"], lp["w_o"], pos, sk, lp["gain"], lp["tau"],
+                             cu_kept, shape.hq, shape.hkv, shape.head_dim, rows=t_rows)
+    else:
+        ai = inputs["ai"]
+        oracle.gated_attention(ai["q"], ai["k"], ai["v"], pos, sk, ai["gain"], ai["tau"], cu_kept, rows=t_rows)
+    dt = time.perf_counter() - t0
+    seq = np.searchsorted(cu_kept, t_rows, side="right") - 1
+    visible = t_rows - cu_kept[seq] + 1          # kept rows are in position order
+    flops = float(np.sum(4.0 * shape.hq * shape.head_dim * visible))
+    return dt, flops
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+SAMPLE_TEXT = ("gate on 256 document rows, full top-K and gather, then attention outputs of 16 random kept "
+               "query rows x all heads of one layer{proj}; value = causal flops of the sampled rows / time")
+
+
+def run_reference(args, shape):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inputs = make_inputs(shape)
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle_step_sample(shape, inputs, rng, 16, 1)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_step_sample(shape, inputs, rng)
+        tot_t += dt
+        tot_f += fl
+    val = tot_f / tot_t / 1e12
+    sample = "per step: " + SAMPLE_TEXT.format(proj=" (with its K/V projections of every kept row)"
+                                               if shape.with_proj else "")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(shape),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample, "cpu": cpu_model()},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+
+class Path:
+    """Device buffers and the calls of one step, through the public binding."""
+
+    def __init__(self, shape, inputs, dev):
+        import torch
+        from learned_token_pruning_09_b300 import tokengate as tg
+        self.tg, self.shape, self.dev = tg, shape, dev
+
+        def bf(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        def i32(a):
+            return torch.as_tensor(np.asarray(a, np.int32)).to(dev)
+
+        self.bf = bf
+        p = inputs["p"]
+        T, d = shape.n_kept, shape.d
+        self.X = bf(inputs["x"])
+        self.W1, self.W2, self.b2 = bf(p["w1"]), bf(p["w2"]), p["b2"]
+        self.cu, self.nd, self.kk = i32(shape.cu_seqlens), i32(shape.n_doc), i32(shape.k)
+        self.T, self.max_nd, self.max_kept = T, max(shape.n_doc), max(shape.kept_lens)
+        e = lambda *s, dt=torch.bfloat16: torch.empty(s, dtype=dt, device=dev)
+        self.s = e(shape.n_rows, dt=torch.float32)
+        self.kept = e(T, dt=torch.int32)
+        self.cu_kept = e(shape.batch + 1, dt=torch.int32)
+        self.xk = e(T, d)
+        self.pos = e(T, dt=torch.int32)
+        self.sk = e(T, dt=torch.float32)
+        hq, hkv, D = shape.hq, shape.hkv, shape.head_dim
+        self.ws = e(tg.tg_attention_workspace_size(T, hq, hkv, D, True), dt=torch.uint8)
+        self.layers = []
+        if shape.with_proj:
+            for lp in inputs["layers"]:
+                w = bf(lp["w_qkv"])
+                nq, nk = hq * D, hkv * D
+                self.layers.append({
+                    "wq": w[:nq].contiguous(), "wk": w[nq:nq + nk].contiguous(), "wv": w[nq + nk:].contiguous(),
+                    "wo": bf(lp["w_o"]), "gain": torch.as_tensor(lp["gain"]).to(dev), "tau": lp["tau"],
+                    "k_cache": e(T, hkv, D), "v": e(T, hkv, D)})
+            self.q, self.k = e(T, hq, D), e(T, hkv, D)
+            self.o = e(T, hq, D)
+        else:
+            ai = inputs["ai"]
+            self.q, self.k = bf(ai["q"]), bf(ai["k"])
+            self.layers.append({"v": bf(ai["v"]), "gain": torch.as_tensor(ai["gain"]).to(dev), "tau": ai["tau"],
+                                "k_cache": e(T, hkv, D)})
+            self.o = e(T, hq, D)
+
+    # the calls
+    def gate(self):
+        self.tg.tg_gate_score(self.X, self.cu, self.nd, self.W1, None, self.W2, self.b2, s_out=self.s)
+
+    def topk(self):
+        self.tg.tg_topk_select(self.s, self.cu, self.nd, self.kk, self.max_nd, self.T, kept_idx=self.kept,
+                               cu_kept=self.cu_kept)
+
+    def gather(self):
+        self.tg.tg_gather_kept(self.X, self.s, self.cu, self.kept, self.cu_kept, self.T, x_kept=self.xk,
+                               pos_kept=self.pos, s_kept=self.sk)
+
+    def proj_qkv(self, i):
+        L, tg, T = self.layers[i], self.tg, self.T
+        tg.tg_linear_bf16(self.xk, L["wq"], out=self.q.view(T, -1))
+        tg.tg_linear_bf16(self.xk, L["wk"], out=self.k.view(T, -1))
+        tg.tg_linear_bf16(self.xk, L["wv"], out=L["v"].view(T, -1))
+
+    def attn(self, i):
+        L = self.layers[i]
+        self.tg.tg_gated_attention_fwd(self.q, self.k, L["v"], self.pos, self.sk, L["gain"], L["tau"], 1e6,
+                                       self.cu_kept, self.max_kept, o=self.o, k_cache=L["k_cache"],
+                                       workspace=self.ws)
+
+    def proj_o(self, i):
+        L, T = self.layers[i], self.T
+        self.tg.tg_linear_bf16(self.o.view(T, -1), L["wo"], residual=self.xk, out=self.xk)
+
+    def segments(self):
+        """(name, callable) in step order."""
+        segs = [("gate", self.gate), ("topk", self.topk), ("gather", self.gather)]
+        for i in range(len(self.layers)):
+            if self.shape.with_proj:
+                segs.append((f"proj_qkv{i}", lambda i=i: self.proj_qkv(i)))
+            segs.append((f"attn{i}", lambda i=i: self.attn(i)))
+            if self.shape.with_proj:
+                segs.append((f"proj_o{i}", lambda i=i: self.proj_o(i)))
+        return segs
+
+    def launches_per_step(self):
+        n = 3
+        for _ in self.layers:
+            n += 2 + (4 if self.shape.with_proj else 0)
+        return n
+
+
+def run_gpu(args, shape):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inputs = make_inputs(shape)
+    P = Path(shape, inputs, dev)
+    tg = P.tg
+    segs = P.segments()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    # eager warm-up (initialises the library on this device), then capture
+    for _ in range(2):
+        for _, f in segs:
+            f()
+    torch.cuda.synchronize()
+    if tg.tg_check_device_status() != tg.TG_OK:
+        raise RuntimeError("device status after warm-up: " + tg.lib.tg_last_error_string().decode())
+    graphs = []
+    for name, f in segs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            f()
+        graphs.append((name, g))
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        for k, (_, g) in enumerate(graphs):
+            if ev is not None:
+                ev[k].record(stream)
+            g.replay()
+        if ev is not None:
+            ev[-1].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    nseg = len(graphs)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    if tg.tg_check_device_status() != tg.TG_OK:
+        raise RuntimeError("device status after timed steps: " + tg.lib.tg_last_error_string().decode())
+
+    per = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(nseg)] for i in range(args.steps)])
+    names = [n for n, _ in graphs]
+    seg_ms = dict(zip(names, per.mean(axis=0)))
+    step_ms = float(per.sum(axis=1).mean())
+    attn_ms = float(sum(v for n, v in seg_ms.items() if n.startswith("attn")))
+    proj_ms = float(sum(v for n, v in seg_ms.items() if n.startswith("proj")))
+    gtg_ms = seg_ms["gate"] + seg_ms["topk"] + seg_ms["gather"]
+    nl = len(P.layers)
+    if world > 1:
+        t = torch.tensor([step_ms, attn_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, attn_ms = float(t[0]), float(t[1])
+    flops_layer = attention_flops(shape.kept_lens, shape.hq, shape.head_dim)
+    tflops_rank = flops_layer * nl / (attn_ms * 1e-3) / 1e12
+    value = tflops_rank * world
+    byts = path_bytes(shape)
+    peaks = load_peaks()
+
+    # ---- end to end through the public API, host buffers ----
+    import torch as _t
+    x_h = _t.from_numpy(np.ascontiguousarray(inputs["x"]).view(np.int16)).view(_t.bfloat16).pin_memory()
+    h2d_list = [(P.X, x_h)]
+    if not shape.with_proj:
+        for dst, key in ((P.q, "q"), (P.k, "k"), (P.layers[0]["v"], "v")):
+            h2d_list.append((dst, _t.from_numpy(np.ascontiguousarray(inputs["ai"][key]).view(np.int16))
+                             .view(_t.bfloat16).pin_memory()))
+    out_dev = P.xk if shape.with_proj else P.o
+    out_h = _t.empty(out_dev.shape, dtype=_t.bfloat16).pin_memory()
+    kept_h = _t.empty(P.T, dtype=_t.int32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for _, h in h2d_list)
+    d2h = out_h.numel() * 2 + kept_h.numel() * 4
+
+    def e2e_step():
+        for dst, h in h2d_list:
+            dst.copy_(h, non_blocking=True)
+        for _, f in segs:
+            f()
+        out_h.copy_(out_dev, non_blocking=True)
+        kept_h.copy_(P.kept, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    e2e_val = flops_layer * nl / (e2e_ms * 1e-3) / 1e12 * world
+
+    # ---- oracle baseline on the host (rank 0, N = 1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rng = np.random.default_rng(0)
+        tt, ff, ns = 0.0, 0.0, 0
+        while tt < args.cpu_seconds:
+            dt, fl = oracle_step_sample(shape, inputs, rng)
+            tt, ff, ns = tt + dt, ff + fl, ns + 1
+        cpu = {"value": ff / tt / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{ns} samples, each: " + SAMPLE_TEXT.format(
+                   proj=" (with its K/V projections of every kept row)" if shape.with_proj else ""),
+               "seconds": tt, "cpu": cpu_model()}
+
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get(shape.name, {}).get("attn_kernel_dram_bytes_per_launch")
+
+    if rank == 0:
+        per_layer = attn_ms / nl
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(shape),
+            "ms_per_layer": per_layer,
+            "attention": {"ms_per_layer": per_layer, "tflops": tflops_rank, "layers": nl,
+                          "gflop_per_layer": flops_layer / 1e9},
+            "gate_topk_gather": {"us": gtg_ms * 1e3, "gbs": byts / (gtg_ms * 1e-3) / 1e9, "bytes": byts,
+                                 "frac_of_measured_hbm": byts / (gtg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                 "gate_us": seg_ms["gate"] * 1e3, "topk_us": seg_ms["topk"] * 1e3,
+                                 "gather_us": seg_ms["gather"] * 1e3},
+            "projections": ({"ms_per_step": proj_ms, "tflops": proj_flops(shape) * nl / (proj_ms * 1e-3) / 1e12}
+                            if shape.with_proj else None),
+            "roofline": {"bound": "tensor", "achieved": tflops_rank, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tflops_rank / peaks["bf16_tflops"], "traffic": traffic,
+                         "kernel": "token-gated attention layer (RoPE prologue + attn_kernel)",
+                         "peak_source": peaks["source"] + " burst bf16 (of measured)",
+                         "frac_of_sustained": tflops_rank / peaks["bf16_tflops_sustained"]
+                         if peaks.get("bf16_tflops_sustained") else None},
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": P.launches_per_step() * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--layers", type=int, default=None, help="override the stacked workload's layer count")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from learned_token_pruning_09_b300 import synth
+    if args.workload not in synth.ALL_SHAPES:
+        raise SystemExit(f"unknown workload {args.workload!r}; one of {sorted(synth.ALL_SHAPES)}")
+    shape = synth.ALL_SHAPES[args.workload]()
+    if args.layers is not None and shape.with_proj:
+        shape.n_layers = args.layers
+    if args.impl == "reference":
+        return run_reference(args, shape)
+    return run_gpu(args, shape)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -28,7 +28,14 @@
 
 namespace tg {
 
-constexpr int kAttnThreads = 320;   // 8 softmax warps + producer + MMA
+constexpr int kAttnThreads = 384;   // 2 softmax warpgroups + producer/MMA warpgroup
+// Register split by setmaxnreg: the kernel launches with kLaunchRegs per
+// thread (384 x 168 = 64512); the softmax warpgroups grow to kSoftmaxRegs and
+// the producer/MMA warpgroup shrinks to kCtrlRegs, 2*128*208 + 128*80 = 63488.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kCtrlRegs = 80;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kCtrlRegs <= kAttnThreads * kLaunchRegs, "register split");
 constexpr int kTileRows = 128;
 constexpr int kKvStages = 2;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -39,7 +46,7 @@ struct AttnSmem {
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t k[kKvStages][kTileBytes];
   alignas(1024) uint8_t v[kKvStages][kTileBytes];
-  float bias[kKvStages][kTileRows];
+  float bias[kKvStages][2][kTileRows];     // gain_h * log2(e) * s_j per tile
   int32_t kpos[kKvStages][kTileRows];
   int32_t kmax[kKvStages];
   uint64_t q_full;
@@ -122,15 +129,19 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const long long wd = a.watchdog;
-
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
   if (warp == 8) {
     // ======================= producer =======================
+    const float gh0 = __ldg(a.gain + head[0]) * 1.4426950408889634f;
+    const float gh1 = __ldg(a.gain + head[1]) * 1.4426950408889634f;
     if (lane == 0) {
       prefetch_tmap(&map_q); prefetch_tmap(&map_k); prefetch_tmap(&map_v);
       mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
       for (int t = 0; t < 2; ++t)
         for (int bx = 0; bx < kBoxes; ++bx)
-          tma_load_3d(sm.q[t] + bx * kBoxBytes, &map_q, &sm.q_full, bx * 64, head[t], seq_start + row0[t]);
+          tma_load_3d(sm.q[t] + bx * kBoxBytes, &map_q, &sm.q_full, bx * 64, t ? head[1] : head[0],
+                      seq_start + (t ? row0[1] : row0[0]));
     }
     int issued = 0;
     for (int j = 0; j < n_kv; ++j) {
@@ -149,7 +160,8 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           sv = __ldg(a.s_kept + seq_start + kr);
           pv = __ldg(a.pos + seq_start + kr);
         }
-        sm.bias[st][c] = sv;
+        sm.bias[st][0][c] = gh0 * sv;
+        sm.bias[st][1][c] = gh1 * sv;
         sm.kpos[st][c] = pv;
         kmax = max(kmax, pv);
       }
@@ -179,18 +191,19 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     }
   } else if (warp == 9) {
     // ======================= MMA issuer =======================
+    // tcgen05.mma operations of one thread execute in issue order, so
+    // S_t(j+1), issued after O_t += P_t(j) V_j, overwrites the TMEM columns
+    // of P_t(j) only after that product has read them.
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(128, kD, 0, 1);
-      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
-      const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
       auto issue_s = [&](int t, int st) {
         const uint32_t qa = smem_u32(sm.q[t]);
         const uint32_t ka = smem_u32(sm.k[st]);
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
           const uint32_t off = (ks >> 2) * kBoxBytes + (ks & 3) * 32;
-          mma_ss(tS[t], smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+          mma_ss(tmem + static_cast<uint32_t>(t) * 128u, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
                  idesc_qk, ks > 0 ? 1u : 0u);
         }
         mma_commit(&sm.s_full[t]);
@@ -199,7 +212,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const uint32_t va = smem_u32(sm.v[st]);
 #pragma unroll
         for (int ks = 0; ks < kTileRows / 16; ++ks) {
-          mma_ts(tO[t], tS[t] + ks * 8, smem_desc_sw128(va + ks * 2048, kBoxBytes, 1024), idesc_pv,
+          mma_ts(tmem + 256u + static_cast<uint32_t>(t) * 128u, tmem + static_cast<uint32_t>(t) * 128u + ks * 8, smem_desc_sw128(va + ks * 2048, kBoxBytes, 1024), idesc_pv,
                  (j > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(&sm.o_done[t]);
@@ -215,20 +228,17 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const int st = j & 1;
         const uint32_t use = j >> 1;
         const uint32_t pj = j & 1;
+        const bool more = j + 1 < n_kv;
+        const int st2 = (j + 1) & 1;
+        const uint32_t use2 = (j + 1) >> 1;
         ok = mbar_wait(&sm.v_full[st], use & 1u, wd, a.status, kStatusTimeout) && !sm.abort;
         ok = ok && mbar_wait(&sm.p_full[0], pj, wd, a.status, kStatusTimeout) && !sm.abort;
         if (!ok) break;
         tc_fence_after();
         issue_pv(0, st, j);
-        const bool more = j + 1 < n_kv;
-        const int st2 = (j + 1) & 1;
-        const uint32_t use2 = (j + 1) >> 1;
         if (more) {
           ok = mbar_wait(&sm.k_full[st2], use2 & 1u, wd, a.status, kStatusTimeout);
-          // S_0(j+1) overwrites P_0(j): wait until O_0 += P_0 V_j has finished
-          ok = ok && mbar_wait(&sm.o_done[0], pj, wd, a.status, kStatusTimeout);
           if (!ok) break;
-          tc_fence_after();
           issue_s(0, st2);
         }
         ok = mbar_wait(&sm.p_full[1], pj, wd, a.status, kStatusTimeout) && !sm.abort;
@@ -236,27 +246,24 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         tc_fence_after();
         issue_pv(1, st, j);
         mma_commit(&sm.kv_empty[st]);
-        if (more) {
-          ok = mbar_wait(&sm.o_done[1], pj, wd, a.status, kStatusTimeout);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(1, st2);
-        }
+        if (more) issue_s(1, st2);
       }
       if (!ok) sm.abort = 1;
       mma_commit(&sm.mma_final);
       mbar_wait(&sm.mma_final, 0, wd, a.status, kStatusTimeout);
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ======================= softmax warpgroups =======================
     const int t = warp >> 2;                      // tile
     const int sub = warp & 3;                     // TMEM lane quarter
     const int r = sub * 32 + lane;                // row inside the tile
-    const int qrow = row0[t] + r;
+    const int my_head = t ? head[1] : head[0];
+    const int qrow = (t ? row0[1] : row0[0]) + r;
     const bool valid = qrow < seq_len;
     const int qpos = valid ? __ldg(a.pos + seq_start + qrow) : -1;
-    const float gh = __ldg(a.gain + head[t]) * 1.4426950408889634f;
-    const float sl2 = a.scale_log2;
+    const float2 sl = make_float2(a.scale_log2, a.scale_log2);
     const uint32_t lane_off = static_cast<uint32_t>(sub * 32) << 16;
     const uint32_t tS = tmem + static_cast<uint32_t>(t * 128) + lane_off;
     const uint32_t tO = tmem + 256u + static_cast<uint32_t>(t * 128) + lane_off;
@@ -270,39 +277,44 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       ok = __all_sync(0xffffffffu, w) && !sm.abort;
       if (!ok) break;
       tc_fence_after();
-      float s[kTileRows];
-      {
-        uint32_t rr[32];
+      uint32_t rr[kTileRows];
 #pragma unroll
-        for (int c = 0; c < kTileRows / 32; ++c) {
-          tmem_ld32(tS + c * 32, rr);
-          tmem_ld_wait();
+      for (int c = 0; c < kTileRows / 32; ++c)
+        tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[c * 32]));
+      tmem_ld_wait();
+      // logits in log2 units: S * log2(e)/(sqrt(D) tau) + gain_h log2(e) s_j
+      const float2* bias2 = reinterpret_cast<const float2*>(sm.bias[st][t]);
+      float2 x[kTileRows / 2];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[i]);
+      for (int i = 0; i < kTileRows / 2; ++i)
+        x[i] = __ffma2_rn(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sl, bias2[i]);
+      if (__any_sync(0xffffffffu, sm.kmax[st] > qpos)) {
+        const int* kp = sm.kpos[st];
+#pragma unroll
+        for (int i = 0; i < kTileRows / 2; ++i) {
+          if (kp[2 * i] > qpos) x[i].x = -INFINITY;
+          if (kp[2 * i + 1] > qpos) x[i].y = -INFINITY;
         }
       }
-      const bool need_mask = sm.kmax[st] > qpos;
-      float mt = -INFINITY;
-      const float* bias = sm.bias[st];
-      const int* kp = sm.kpos[st];
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < kTileRows; ++c) {
-        float x = fmaf(s[c], sl2, gh * bias[c]);
-        if (need_mask && kp[c] > qpos) x = -INFINITY;
-        s[c] = x;
-        mt = fmaxf(mt, x);
-      }
+      for (int i = 0; i < kTileRows / 2; ++i) mx[i & 3] = fmax3(mx[i & 3], x[i].x, x[i].y);
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], -INFINITY);
       const float m_new = (mt > m + kRescaleThreshold) ? mt : m;
       const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
       const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_use);
-      float rs = 0.0f;
+      const float2 negm = make_float2(-m_use, -m_use);
+      float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int c = 0; c < kTileRows; ++c) {
-        const float p = ex2_approx(s[c] - m_use);
-        s[c] = p;
-        rs += p;
+      for (int i = 0; i < kTileRows / 2; ++i) {
+        const float2 y = __fadd2_rn(x[i], negm);
+        const float p0 = ex2_approx(y.x);
+        const float p1 = ex2_approx(y.y);
+        if (i & 1) acc1 = __fadd2_rn(acc1, make_float2(p0, p1));
+        else acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
+        rr[i] = pack_bf16x2(p0, p1);
       }
-      l = l * alpha + rs;
+      l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
       m = m_new;
       // rescale O when this row's max moved (warp-uniform TMEM access)
       if (__any_sync(0xffffffffu, j > 0 && alpha != 1.0f)) {
@@ -322,12 +334,8 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       }
       // P (bf16 pairs) over the first 64 columns of S
 #pragma unroll
-      for (int c = 0; c < kTileRows / 32; ++c) {
-        uint32_t p16[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) p16[i] = pack_bf16x2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]);
-        tmem_st16(tS + c * 16, p16);
-      }
+      for (int c = 0; c < kTileRows / 32; ++c)
+        tmem_st16(tS + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&rr[c * 16]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sm.p_full[t]);
@@ -340,28 +348,25 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       tc_fence_after();
       const float inv = 1.0f / l;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
-                            (static_cast<size_t>(seq_start + qrow) * a.hq + head[t]) * kD;
+                            (static_cast<size_t>(seq_start + qrow) * a.hq + my_head) * kD;
 #pragma unroll
-      for (int c = 0; c < kD / 16; ++c) {
-        uint32_t o16[16];
-        tmem_ld16(tO + c * 16, o16);
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t o32[32];
+        tmem_ld32(tO + c * 32, o32);
         tmem_ld_wait();
         if (valid) {
-          uint4 v0, v1;
-          uint32_t* p0 = reinterpret_cast<uint32_t*>(&v0);
-          uint32_t* p1 = reinterpret_cast<uint32_t*>(&v1);
+          uint4 v[4];
+          uint32_t* pw = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            p0[i] = pack_bf16x2(__uint_as_float(o16[2 * i]) * inv, __uint_as_float(o16[2 * i + 1]) * inv);
-            p1[i] = pack_bf16x2(__uint_as_float(o16[8 + 2 * i]) * inv, __uint_as_float(o16[8 + 2 * i + 1]) * inv);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
-          dst[0] = v0;
-          dst[1] = v1;
+          for (int i = 0; i < 16; ++i)
+            pw[i] = pack_bf16x2(__uint_as_float(o32[2 * i]) * inv, __uint_as_float(o32[2 * i + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = v[i];
         }
       }
       if (valid && a.lse)
-        a.lse[static_cast<size_t>(head[t]) * a.n_kept + seq_start + qrow] =
+        a.lse[static_cast<size_t>(my_head) * a.n_kept + seq_start + qrow] =
             (((m == -INFINITY) ? 0.0f : m) + __log2f(l)) * 0.6931471805599453f;
     }
   }
@@ -389,6 +394,12 @@ static cudaError_t launch_attn_d(const CUtensorMap& mq, const CUtensorMap& mk, c
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<kD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  // the setmaxnreg split is only valid for the launch register count it was
+  // sized for; refuse to launch otherwise (setmaxnreg.inc would never return)
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, attn_kernel<kD>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   const long long grid = static_cast<long long>(n_rb) * units_per_rb;
   if (grid == 0) return cudaSuccess;
   attn_kernel<kD><<<static_cast<unsigned>(grid), kAttnThreads, smem, st>>>(mq, mk, mv, a, units_per_rb,
