@@ -182,6 +182,7 @@ tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d, const int
   a.s_out = s_out;
   a.status = di->status;
   a.watchdog = g_watchdog_cycles;
+  a.num_sms = di->num_sms;
   cudaError_t e = launch_gate(mx, mw, a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gate kernel launch");
   return ok();

@@ -31,10 +31,10 @@ namespace tg {
 constexpr int kAttnThreads = 384;   // 2 softmax warpgroups + producer/MMA warpgroup
 // Register split by setmaxnreg: the kernel launches with kLaunchRegs per
 // thread (384 x 168 = 64512); the softmax warpgroups grow to kSoftmaxRegs and
-// the producer/MMA warpgroup shrinks to kCtrlRegs, 2*128*208 + 128*80 = 63488.
+// the producer/MMA warpgroup shrinks to kCtrlRegs, 2*128*200 + 128*96 = 63488.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 208;
-constexpr int kCtrlRegs = 80;
+constexpr int kSoftmaxRegs = 200;
+constexpr int kCtrlRegs = 96;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kCtrlRegs <= kAttnThreads * kLaunchRegs, "register split");
 constexpr int kTileRows = 128;
 constexpr int kKvStages = 2;
@@ -53,10 +53,11 @@ struct AttnSmem {
   uint64_t k_full[kKvStages];
   uint64_t v_full[kKvStages];
   uint64_t kv_empty[kKvStages];
+  uint64_t meta_full[kKvStages];   // per-key scores/positions of a stage written
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
-  uint64_t mma_final;
+  uint64_t mma_final[2];
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -113,13 +114,15 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.meta_full[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_done[t], 1);
     }
-    mbar_init(&sm.mma_final, 1);
+    mbar_init(&sm.mma_final[0], 1);
+    mbar_init(&sm.mma_final[1], 1);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -143,6 +146,24 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           tma_load_3d(sm.q[t] + bx * kBoxBytes, &map_q, &sm.q_full, bx * 64, t ? head[1] : head[0],
                       seq_start + (t ? row0[1] : row0[0]));
     }
+    // Each key's score and position (read by the softmax warps only) are
+    // fetched into registers one tile ahead, so that the K/V copies of a
+    // freed stage are issued without waiting for those loads.
+    float sv[kTileRows / 32];
+    int pv[kTileRows / 32];
+    auto load_meta = [&](int j) {
+#pragma unroll
+      for (int u = 0; u < kTileRows / 32; ++u) {
+        const int kr = j * kTileRows + u * 32 + lane;
+        sv[u] = 0.0f;
+        pv[u] = INT_MAX;                          // keys past the sequence end are masked
+        if (j < n_kv && kr < seq_len) {
+          sv[u] = __ldg(a.s_kept + seq_start + kr);
+          pv[u] = __ldg(a.pos + seq_start + kr);
+        }
+      }
+    };
+    load_meta(0);
     int issued = 0;
     for (int j = 0; j < n_kv; ++j) {
       const int st = j & 1;
@@ -151,23 +172,6 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       if (lane == 0) ok = mbar_wait(&sm.kv_empty[st], (use & 1u) ^ 1u, wd, a.status, kStatusTimeout);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || sm.abort) { sm.abort = 1; break; }
-      int kmax = INT_MIN;
-      for (int c = lane; c < kTileRows; c += 32) {
-        const int kr = j * kTileRows + c;
-        float sv = 0.0f;
-        int pv = INT_MAX;
-        if (kr < seq_len) {
-          sv = __ldg(a.s_kept + seq_start + kr);
-          pv = __ldg(a.pos + seq_start + kr);
-        }
-        sm.bias[st][0][c] = gh0 * sv;
-        sm.bias[st][1][c] = gh1 * sv;
-        sm.kpos[st][c] = pv;
-        kmax = max(kmax, pv);
-      }
-      for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-      if (lane == 0) sm.kmax[st] = kmax;
-      __syncwarp();
       if (lane == 0) {
         const int krow = seq_start + j * kTileRows;
         mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
@@ -178,6 +182,20 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           tma_load_3d(sm.v[st] + bx * kBoxBytes, &map_v, &sm.v_full[st], bx * 64, kvh, krow);
       }
       issued = j + 1;
+      int kmax = INT_MIN;
+#pragma unroll
+      for (int u = 0; u < kTileRows / 32; ++u) {
+        const int c = u * 32 + lane;
+        sm.bias[st][0][c] = gh0 * sv[u];
+        sm.bias[st][1][c] = gh1 * sv[u];
+        sm.kpos[st][c] = pv[u];
+        kmax = max(kmax, pv[u]);
+      }
+      for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+      if (lane == 0) sm.kmax[st] = kmax;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.meta_full[st]);
+      load_meta(j + 1);
     }
     if (lane == 0) {
       // every issued copy must land before the CTA may leave
@@ -193,28 +211,32 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     // ======================= MMA issuer =======================
     // tcgen05.mma operations of one thread execute in issue order, so
     // S_t(j+1), issued after O_t += P_t(j) V_j, overwrites the TMEM columns
-    // of P_t(j) only after that product has read them.
+    // of P_t(j) only after that product has read them.  The single issuing
+    // thread polls its barriers without suspending (test_wait), which keeps
+    // its reaction to a finished softmax short.
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(128, kD, 0, 1);
       auto issue_s = [&](int t, int st) {
         const uint32_t qa = smem_u32(sm.q[t]);
         const uint32_t ka = smem_u32(sm.k[st]);
+        const uint32_t tS = tmem + static_cast<uint32_t>(t) * 128u;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
           const uint32_t off = (ks >> 2) * kBoxBytes + (ks & 3) * 32;
-          mma_ss(tmem + static_cast<uint32_t>(t) * 128u, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                 idesc_qk, ks > 0 ? 1u : 0u);
+          mma_ss(tS, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_qk,
+                 ks > 0 ? 1u : 0u);
         }
         mma_commit(&sm.s_full[t]);
       };
       auto issue_pv = [&](int t, int st, int j) {
         const uint32_t va = smem_u32(sm.v[st]);
+        const uint32_t tS = tmem + static_cast<uint32_t>(t) * 128u;
+        const uint32_t tO = tmem + 256u + static_cast<uint32_t>(t) * 128u;
 #pragma unroll
-        for (int ks = 0; ks < kTileRows / 16; ++ks) {
-          mma_ts(tmem + 256u + static_cast<uint32_t>(t) * 128u, tmem + static_cast<uint32_t>(t) * 128u + ks * 8, smem_desc_sw128(va + ks * 2048, kBoxBytes, 1024), idesc_pv,
+        for (int ks = 0; ks < kTileRows / 16; ++ks)
+          mma_ts(tO, tS + ks * 8, smem_desc_sw128(va + ks * 2048, kBoxBytes, 1024), idesc_pv,
                  (j > 0 || ks > 0) ? 1u : 0u);
-        }
         mma_commit(&sm.o_done[t]);
       };
       bool ok = mbar_wait(&sm.q_full, 0, wd, a.status, kStatusTimeout);
@@ -231,17 +253,17 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const bool more = j + 1 < n_kv;
         const int st2 = (j + 1) & 1;
         const uint32_t use2 = (j + 1) >> 1;
-        ok = mbar_wait(&sm.v_full[st], use & 1u, wd, a.status, kStatusTimeout) && !sm.abort;
-        ok = ok && mbar_wait(&sm.p_full[0], pj, wd, a.status, kStatusTimeout) && !sm.abort;
+        ok = mbar_wait_spin(&sm.v_full[st], use & 1u, wd, a.status, kStatusTimeout) && !sm.abort;
+        ok = ok && mbar_wait_spin(&sm.p_full[0], pj, wd, a.status, kStatusTimeout) && !sm.abort;
         if (!ok) break;
         tc_fence_after();
         issue_pv(0, st, j);
         if (more) {
-          ok = mbar_wait(&sm.k_full[st2], use2 & 1u, wd, a.status, kStatusTimeout);
+          ok = mbar_wait_spin(&sm.k_full[st2], use2 & 1u, wd, a.status, kStatusTimeout);
           if (!ok) break;
           issue_s(0, st2);
         }
-        ok = mbar_wait(&sm.p_full[1], pj, wd, a.status, kStatusTimeout) && !sm.abort;
+        ok = mbar_wait_spin(&sm.p_full[1], pj, wd, a.status, kStatusTimeout) && !sm.abort;
         if (!ok) break;
         tc_fence_after();
         issue_pv(1, st, j);
@@ -249,8 +271,8 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         if (more) issue_s(1, st2);
       }
       if (!ok) sm.abort = 1;
-      mma_commit(&sm.mma_final);
-      mbar_wait(&sm.mma_final, 0, wd, a.status, kStatusTimeout);
+      mma_commit(&sm.mma_final[0]);
+      mbar_wait(&sm.mma_final[0], 0, wd, a.status, kStatusTimeout);
     }
   }
   } else {
@@ -272,24 +294,26 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     for (int j = 0; j < n_kv; ++j) {
       const int st = j & 1;
       const uint32_t use = j >> 1;
-      bool w = mbar_wait(&sm.k_full[st], use & 1u, wd, a.status, kStatusTimeout);
+      bool w = mbar_wait(&sm.meta_full[st], use & 1u, wd, a.status, kStatusTimeout);
       w = w && mbar_wait(&sm.s_full[t], j & 1u, wd, a.status, kStatusTimeout);
       ok = __all_sync(0xffffffffu, w) && !sm.abort;
       if (!ok) break;
       tc_fence_after();
+      // logits in log2 units: x = S * log2(e)/(sqrt(D) tau) + gain_h log2(e) s_j,
+      // one TMEM read of the whole 128-column row, then max, exp2 and P.
       uint32_t rr[kTileRows];
 #pragma unroll
       for (int c = 0; c < kTileRows / 32; ++c)
         tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[c * 32]));
-      tmem_ld_wait();
-      // logits in log2 units: S * log2(e)/(sqrt(D) tau) + gain_h log2(e) s_j
       const float2* bias2 = reinterpret_cast<const float2*>(sm.bias[st][t]);
+      const bool masked = __any_sync(0xffffffffu, sm.kmax[st] > qpos);
+      const int* kp = sm.kpos[st];
+      tmem_ld_wait();
       float2 x[kTileRows / 2];
 #pragma unroll
       for (int i = 0; i < kTileRows / 2; ++i)
         x[i] = __ffma2_rn(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sl, bias2[i]);
-      if (__any_sync(0xffffffffu, sm.kmax[st] > qpos)) {
-        const int* kp = sm.kpos[st];
+      if (masked) {
 #pragma unroll
         for (int i = 0; i < kTileRows / 2; ++i) {
           if (kp[2 * i] > qpos) x[i].x = -INFINITY;
@@ -306,13 +330,19 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const float2 negm = make_float2(-m_use, -m_use);
       float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int i = 0; i < kTileRows / 2; ++i) {
-        const float2 y = __fadd2_rn(x[i], negm);
-        const float p0 = ex2_approx(y.x);
-        const float p1 = ex2_approx(y.y);
-        if (i & 1) acc1 = __fadd2_rn(acc1, make_float2(p0, p1));
-        else acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
-        rr[i] = pack_bf16x2(p0, p1);
+      for (int c = 0; c < kTileRows / 32; ++c) {
+        uint32_t p16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 y = __fadd2_rn(x[c * 16 + i], negm);
+          const float p0 = ex2_approx(y.x);
+          const float p1 = ex2_approx(y.y);
+          if (i & 1) acc1 = __fadd2_rn(acc1, make_float2(p0, p1));
+          else acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
+          p16[i] = pack_bf16x2(p0, p1);
+        }
+        // P chunk c: bf16 pairs over S columns [16c, 16c + 16)
+        tmem_st16(tS + c * 16, p16);
       }
       l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
       m = m_new;
@@ -332,10 +362,6 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           tmem_st16(tO + c * 16, o16);
         }
       }
-      // P (bf16 pairs) over the first 64 columns of S
-#pragma unroll
-      for (int c = 0; c < kTileRows / 32; ++c)
-        tmem_st16(tS + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&rr[c * 16]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sm.p_full[t]);

@@ -78,6 +78,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   }
 }
 
+// Non-blocking probe of a phase (no suspension of the thread).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Like mbar_wait, but polls with test_wait so that a single latency-critical
+// thread (the MMA issuer) sees the phase change without a wake-up delay.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, long long limit,
+                                               unsigned int* status, unsigned int code) {
+  if (mbar_test(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test(bar, parity)) return true;
+    if (clock64() - t0 > limit) {
+      record_error(status, code);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) tile loads into shared memory, completion
 // signalled on an mbarrier by transaction bytes.
@@ -226,6 +252,58 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// GELU(u) = u * Phi(u) = 0.5 u (1 + erf(u / sqrt 2)), with erf from the
+// rational approximation of Abramowitz & Stegun, Handbook of Mathematical
+// Functions, formula 7.1.26: for x >= 0,
+//   erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
+//   t = 1 / (1 + p x),  |error| <= 1.5e-7,
+// and erf(-x) = -erf(x).  exp(-x^2) = 2^(-x^2 log2 e) on the ex2 unit.
+__device__ __forceinline__ float gelu_erf(float u) {
+  const float x = fabsf(u) * 0.70710678118654752f;
+  const float t = rcp_approx(fmaf(0.3275911f, x, 1.0f));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  poly *= t;
+  const float e = ex2_approx(-x * x * 1.4426950408889634f);
+  const float erf_abs = fmaf(-poly, e, 1.0f);
+  const float phi = 0.5f + 0.5f * copysignf(erf_abs, u);
+  return u * phi;
+}
+
+// GELU on two values with packed fp32 arithmetic and one reciprocal per
+// value: erf from Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.28: for x >= 0,
+//   erf(x) = 1 - (1 + a1 x + a2 x^2 + ... + a6 x^6)^(-16),  |error| <= 3e-7,
+// the 16th power taken by four squarings of the reciprocal.
+__device__ __forceinline__ float2 gelu_erf2(float2 u) {
+  const float2 x = __fmul2_rn(make_float2(fabsf(u.x), fabsf(u.y)),
+                              make_float2(0.70710678118654752f, 0.70710678118654752f));
+  float2 q = __ffma2_rn(make_float2(0.0000430638f, 0.0000430638f), x, make_float2(0.0002765672f, 0.0002765672f));
+  q = __ffma2_rn(q, x, make_float2(0.0001520143f, 0.0001520143f));
+  q = __ffma2_rn(q, x, make_float2(0.0092705272f, 0.0092705272f));
+  q = __ffma2_rn(q, x, make_float2(0.0422820123f, 0.0422820123f));
+  q = __ffma2_rn(q, x, make_float2(0.0705230784f, 0.0705230784f));
+  q = __ffma2_rn(q, x, make_float2(1.0f, 1.0f));
+  float2 r = make_float2(rcp_approx(q.x), rcp_approx(q.y));
+  r = __fmul2_rn(r, r);
+  r = __fmul2_rn(r, r);
+  r = __fmul2_rn(r, r);
+  r = __fmul2_rn(r, r);                                     // q^-16
+  // Phi(u) = 0.5 (1 + sign(u) (1 - q^-16))
+  const float2 erf_abs = __ffma2_rn(r, make_float2(-1.0f, -1.0f), make_float2(1.0f, 1.0f));
+  const float2 erf_s = make_float2(copysignf(erf_abs.x, u.x), copysignf(erf_abs.y, u.y));
+  const float2 phi = __ffma2_rn(erf_s, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));
+  return __fmul2_rn(u, phi);
 }
 
 // max of three floats in one instruction (sm_100+)

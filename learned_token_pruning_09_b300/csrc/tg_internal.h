@@ -34,6 +34,7 @@ struct GateArgs {
   float* s_out;
   unsigned int* status;
   long long watchdog;
+  int num_sms;
 };
 cudaError_t launch_gate(const CUtensorMap& map_x, const CUtensorMap& map_w1, const GateArgs& a,
                         cudaStream_t st);

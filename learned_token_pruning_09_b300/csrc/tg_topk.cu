@@ -20,7 +20,8 @@ namespace cg = cooperative_groups;
 
 namespace tg {
 
-constexpr int kTopkCluster = 8;
+constexpr int kTopkClusterMax = 16;   // non-portable cluster size, when the device allows it
+constexpr int kTopkClusterPortable = 8;
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkMaxSmemKeys = (200 * 1024) / 4;
@@ -49,12 +50,13 @@ struct TopkShared {
 };
 
 template <bool kSmemKeys>
-__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 1)
+__global__ void __launch_bounds__(kTopkThreads, 1)
 topk_kernel(TopkArgs a) {
   extern __shared__ __align__(16) uint32_t keys_smem[];
   __shared__ TopkShared sh;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
+  const int kTopkCluster = static_cast<int>(cluster.num_blocks());   // 8 or 16
   const int b = blockIdx.x / kTopkCluster;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -109,7 +111,21 @@ topk_kernel(TopkArgs a) {
   if (ke == 0) return;        // question only
 
   if (kSmemKeys) {
-    for (int i = tid; i < n_loc; i += kTopkThreads) keys_smem[i] = order_key(src[i]);
+    // eight loads in flight per thread before any is used (the scores were
+    // just written and sit in L2; one at a time would serialise its latency)
+    for (int i0 = tid; i0 < n_loc; i0 += 8 * kTopkThreads) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kTopkThreads;
+        v[u] = i < n_loc ? __ldg(src + i) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kTopkThreads;
+        if (i < n_loc) keys_smem[i] = order_key(v[u]);
+      }
+    }
   }
   auto key_at = [&](int i) -> uint32_t {
     if (kSmemKeys) return keys_smem[i];
@@ -219,20 +235,50 @@ topk_kernel(TopkArgs a) {
   cluster.sync();   // no CTA leaves while another may still read its counts
 }
 
+// Launch with `csize` CTAs per cluster; returns the launch error.
+template <bool kSmemKeys>
+static cudaError_t launch_topk_cluster(const TopkArgs& a, int csize, cudaStream_t st) {
+  const int chunk = (a.max_n_doc + csize - 1) / csize;
+  const size_t smem = kSmemKeys ? static_cast<size_t>(max(chunk, 4)) * sizeof(uint32_t) : 0;
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel<kSmemKeys>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (csize > kTopkClusterPortable) {
+    e = cudaFuncSetAttribute(topk_kernel<kSmemKeys>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.batch) * csize);
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // a cluster size the device cannot co-schedule is refused here, not at run time
+  int n_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&n_clusters, topk_kernel<kSmemKeys>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n_clusters < 1) return cudaErrorInvalidConfiguration;
+  return cudaLaunchKernelEx(&cfg, topk_kernel<kSmemKeys>, a);
+}
+
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   if (a.batch == 0) return cudaSuccess;
-  const int chunk = (a.max_n_doc + kTopkCluster - 1) / kTopkCluster;
-  const dim3 grid(static_cast<unsigned>(a.batch) * kTopkCluster);
-  if (chunk <= kTopkMaxSmemKeys) {
-    const size_t smem = static_cast<size_t>(max(chunk, 4)) * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    topk_kernel<true><<<grid, kTopkThreads, smem, st>>>(a);
-  } else {
-    topk_kernel<false><<<grid, kTopkThreads, 0, st>>>(a);
+  // 16-CTA clusters halve the per-CTA slice when the device allows them
+  for (int csize : {kTopkClusterMax, kTopkClusterPortable}) {
+    const int chunk = (a.max_n_doc + csize - 1) / csize;
+    const cudaError_t e = chunk <= kTopkMaxSmemKeys ? launch_topk_cluster<true>(a, csize, st)
+                                                    : launch_topk_cluster<false>(a, csize, st);
+    if (e == cudaSuccess) return cudaSuccess;
+    if (csize == kTopkClusterPortable) return e;
+    (void)cudaGetLastError();   // clear the refusal of the larger cluster, try the portable size
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace tg
