@@ -185,6 +185,42 @@ TG_API size_t tg_attention_workspace_size(int64_t n_kept, int32_t hq, int32_t hk
 TG_API tg_status tg_linear_bf16(const void* a, const void* w, const void* residual, void* out,
                          int64_t m, int32_t n, int32_t kdim, cudaStream_t stream);
 
+/*
+ * Token-gated attention with no workspace argument.  The TokenGate articles
+ * have no counterpart of this call: it computes exactly what
+ * tg_gated_attention_fwd computes, with the same arguments minus `workspace`
+ * and `workspace_bytes`, for callers that cannot allocate device memory when
+ * they call -- an engine that plans all of its device memory at start-up and
+ * forbids allocation afterwards, a plugin running under a host runtime that
+ * owns the allocator, or a plain C program that does not want to manage a
+ * scratch buffer.
+ *
+ * Scratch space (the rotated queries, and the rotated keys when k_cache is
+ * NULL) comes from a fixed array of tg_attention_static_scratch_bytes()
+ * bytes (64 MiB) inside the library, which every device that loads the
+ * library holds until the process exits.  A call needs
+ * tg_attention_workspace_size(n_kept, hq, hkv, head_dim, k_cache != NULL)
+ * bytes of it; a larger problem returns TG_ERR_WORKSPACE and launches
+ * nothing.  The library allocates no memory on this path.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current): make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents; nothing in it needs to start at zero, since each call overwrites
+ * what it reads.  Calls whose kernels overlap on the GPU (different streams
+ * or host threads) race on the array: serialise them.
+ */
+TG_API tg_status tg_gated_attention_fwd_noalloc(const void* q, const void* k, const void* v,
+                                                const int32_t* pos_kept, const float* s_kept,
+                                                const float* gain, float tau, float rope_theta,
+                                                const int32_t* cu_kept, int32_t batch, int64_t n_kept,
+                                                int32_t max_kept, int32_t hq, int32_t hkv, int32_t head_dim,
+                                                void* o, float* lse, void* k_cache, cudaStream_t stream);
+
+/* Size in bytes of the fixed scratch array used by
+ * tg_gated_attention_fwd_noalloc.  Host-only, no CUDA call. */
+TG_API size_t tg_attention_static_scratch_bytes(void);
+
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device: TG_OK, TG_ERR_TIMEOUT or TG_ERR_DEVICE_INDEX. */
 TG_API tg_status tg_check_device_status(cudaStream_t stream);

@@ -360,3 +360,71 @@ tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Token-gated attention without a caller-provided workspace.
+//
+// For callers that cannot allocate device memory at call time (an engine
+// that plans all of its device memory at start-up and forbids allocation
+// afterwards, a plugin running under a host runtime that owns the allocator,
+// a plain C program that does not want to manage a scratch buffer).  The
+// scratch space that tg_gated_attention_fwd takes as `workspace` (the
+// rotated queries, and the rotated keys when no K cache is given) lives in
+// a fixed array of this library's device memory instead.
+// ---------------------------------------------------------------------------
+namespace tg {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;   // 64 MiB
+// Every device that loads the library holds this array until the process exits.
+__device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_attn_scratch on the current device.  In host code
+// the symbol itself is only a host-side stand-in, so the address is asked
+// from the runtime once per device (with that device current) and cached.
+tg_status scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(TG_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return TG_OK;
+}
+
+}  // namespace
+}  // namespace tg
+
+extern "C" size_t tg_attention_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+extern "C" tg_status tg_gated_attention_fwd_noalloc(const void* q, const void* k, const void* v,
+                                                   const int32_t* pos_kept, const float* s_kept,
+                                                   const float* gain, float tau, float rope_theta,
+                                                   const int32_t* cu_kept, int32_t batch, int64_t n_kept,
+                                                   int32_t max_kept, int32_t hq, int32_t hkv,
+                                                   int32_t head_dim, void* o, float* lse, void* k_cache,
+                                                   cudaStream_t stream) {
+  if (n_kept < 0 || hq < 1 || hkv < 1 || head_dim < 1)
+    return fail(TG_ERR_INVALID_ARG, "n_kept, hq, hkv and head_dim must be positive");
+  const size_t need = tg_attention_workspace_size(n_kept, hq, hkv, head_dim, k_cache ? 1 : 0);
+  if (need > kStaticScratchBytes)
+    return fail(TG_ERR_WORKSPACE,
+                "this call needs %zu bytes of scratch; the library's fixed scratch holds %zu bytes "
+                "(use tg_gated_attention_fwd with a caller-provided workspace)",
+                need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  tg_status s = scratch_address(&scratch);
+  if (s != TG_OK) return s;
+  return tg_gated_attention_fwd(q, k, v, pos_kept, s_kept, gain, tau, rope_theta, cu_kept, batch, n_kept,
+                                max_kept, hq, hkv, head_dim, o, lse, k_cache, scratch, kStaticScratchBytes,
+                                stream);
+}
