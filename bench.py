@@ -69,6 +69,23 @@ def path_bytes(shape):
     return float(n * 2 * d + n * 8 + t * 8 + t * 4 * d + t * 8)
 
 
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the default process group (the
+    values unchanged when there is one rank): the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_tflops(flops_per_rank, world, max_ms):
+    """Whole-job throughput of N replicas: all ranks' flops over the slowest
+    rank's time."""
+    return flops_per_rank * world / (max_ms * 1e-3) / 1e12
+
+
 def proj_flops(shape):
     t, d = shape.n_kept, shape.d
     return 2.0 * t * d * (shape.hq + 2 * shape.hkv) * shape.head_dim + 2.0 * t * shape.hq * shape.head_dim * d
@@ -408,13 +425,10 @@ def run_gpu(args, shape):
     proj_ms = float(sum(v for n, v in seg_ms.items() if n.startswith("proj")))
     gtg_ms = seg_ms["gate"] + seg_ms["topk"] + seg_ms["gather"]
     nl = len(P.layers)
-    if world > 1:
-        t = torch.tensor([step_ms, attn_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, attn_ms = float(t[0]), float(t[1])
+    step_ms, attn_ms = max_over_ranks([step_ms, attn_ms], dev)
     flops_layer = attention_flops(shape.kept_lens, shape.hq, shape.head_dim)
-    tflops_rank = flops_layer * nl / (attn_ms * 1e-3) / 1e12
-    value = tflops_rank * world
+    tflops_rank = whole_job_tflops(flops_layer * nl, 1, attn_ms)
+    value = whole_job_tflops(flops_layer * nl, world, attn_ms)
     byts = path_bytes(shape)
     peaks = load_peaks()
 
@@ -450,11 +464,8 @@ def run_gpu(args, shape):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
-    e2e_val = flops_layer * nl / (e2e_ms * 1e-3) / 1e12 * world
+    e2e_ms, = max_over_ranks([e2e_ms], dev)
+    e2e_val = whole_job_tflops(flops_layer * nl, world, e2e_ms)
 
     # ---- oracle baseline on the host (rank 0, N = 1 only) ----
     cpu = None

@@ -199,12 +199,12 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     }
     if (lane == 0) {
       // every issued copy must land before the CTA may leave
-      mbar_wait(&sm.q_full, 0, wd, a.status, kStatusTimeout);
+      mbar_wait(&sm.q_full, 0, kDrainCycles, a.status, kStatusTimeout);
       for (int st = 0; st < kKvStages && st < issued; ++st) {
         const int last = ((issued - 1 - st) / kKvStages) * kKvStages + st;
         const uint32_t par = static_cast<uint32_t>(last >> 1) & 1u;
-        mbar_wait(&sm.k_full[st], par, wd, a.status, kStatusTimeout);
-        mbar_wait(&sm.v_full[st], par, wd, a.status, kStatusTimeout);
+        mbar_wait(&sm.k_full[st], par, kDrainCycles, a.status, kStatusTimeout);
+        mbar_wait(&sm.v_full[st], par, kDrainCycles, a.status, kStatusTimeout);
       }
     }
   } else if (warp == 9) {
@@ -272,7 +272,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       }
       if (!ok) sm.abort = 1;
       mma_commit(&sm.mma_final[0]);
-      mbar_wait(&sm.mma_final[0], 0, wd, a.status, kStatusTimeout);
+      mbar_wait(&sm.mma_final[0], 0, kDrainCycles, a.status, kStatusTimeout);
     }
   }
   } else {

@@ -62,6 +62,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Cycle limit of the final waits with which a CTA drains its own copies and
+// MMAs in flight before it frees TMEM and leaves.  It does not follow the
+// configurable watchdog, so that a kernel that gave up early (on a short
+// watchdog) still never leaves with asynchronous work outstanding.
+constexpr long long kDrainCycles = 1LL << 31;
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit` SM clock cycles, records `code` in the status word and returns
 // false; never spins without bound.

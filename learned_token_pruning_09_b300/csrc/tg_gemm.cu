@@ -63,7 +63,7 @@ __device__ __forceinline__ void gemm_mainloop(const CUtensorMap* map_a, const CU
     // wait for the last loads of every stage to land before anyone may leave
     for (int st = 0; st < kStages && st < issued; ++st) {
       const int last = ((issued - 1 - st) / kStages) * kStages + st;
-      mbar_wait(&head->full[st], (static_cast<uint32_t>(last / kStages)) & 1u, watchdog, status, kStatusTimeout);
+      mbar_wait(&head->full[st], (static_cast<uint32_t>(last / kStages)) & 1u, kDrainCycles, status, kStatusTimeout);
     }
   } else if (warp == 1 && lane == 0) {
     const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(bn), 0, 0);
@@ -89,6 +89,8 @@ __device__ __forceinline__ void gemm_mainloop(const CUtensorMap* map_a, const CU
       mma_commit(&head->empty[st]);
     }
     mma_commit(&head->acc_full);
+    // every MMA must have finished before TMEM may be freed
+    mbar_wait(&head->acc_full, 0, kDrainCycles, status, kStatusTimeout);
   }
 }
 
@@ -129,6 +131,7 @@ struct GateSmemHead {
   uint64_t b_empty[kGateMaxStages];
   uint64_t acc_full;
   uint64_t acc_empty;
+  uint64_t mma_done;
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -177,6 +180,7 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
     for (int i = 0; i < n_b; ++i) { mbar_init(&head.b_full[i], 1); mbar_init(&head.b_empty[i], 1); }
     mbar_init(&head.acc_full, 1);
     mbar_init(&head.acc_empty, 256);
+    mbar_init(&head.mma_done, 1);
     head.abort = 0;
     fence_barrier_init();
     prefetch_tmap(&map_x);
@@ -227,7 +231,7 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
     // the last copies into every stage must land before the CTA may leave
     for (uint32_t st = 0; st < static_cast<uint32_t>(n_st) && st < g; ++st) {
       const uint32_t last = ((g - 1 - st) / n_st) * n_st + st;
-      mbar_wait(&full[st], (last / n_st) & 1u, wd, a.status, kStatusTimeout);
+      mbar_wait(&full[st], (last / n_st) & 1u, kDrainCycles, a.status, kStatusTimeout);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -270,6 +274,9 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
         mma_commit(&head.acc_full);
         if (!ok) break;
       }
+      // every MMA must have finished before TMEM may be freed
+      mma_commit(&head.mma_done);
+      mbar_wait(&head.mma_done, 0, kDrainCycles, a.status, kStatusTimeout);
     }
   } else if (warp >= 4) {
     // ---------------- epilogue: + b1, GELU, . w2, + b2, logsigmoid ----------------
