@@ -217,26 +217,32 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(128, kD, 0, 1);
+      // shared-memory descriptors are built once; a K step only advances the
+      // start-address field (the low bits, in 16-byte units)
+      const uint64_t qd0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t qd1 = smem_desc_sw128(smem_u32(sm.q[1]), 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t kd1 = smem_desc_sw128(smem_u32(sm.k[1]), 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(smem_u32(sm.v[0]), kBoxBytes, 1024);
+      const uint64_t vd1 = smem_desc_sw128(smem_u32(sm.v[1]), kBoxBytes, 1024);
       auto issue_s = [&](int t, int st) {
-        const uint32_t qa = smem_u32(sm.q[t]);
-        const uint32_t ka = smem_u32(sm.k[st]);
+        const uint64_t qd = t ? qd1 : qd0;
+        const uint64_t kd = st ? kd1 : kd0;
         const uint32_t tS = tmem + static_cast<uint32_t>(t) * 128u;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kBoxBytes + (ks & 3) * 32;
-          mma_ss(tS, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc_qk,
-                 ks > 0 ? 1u : 0u);
+          const uint32_t off = ((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4;
+          mma_ss(tS, qd + off, kd + off, idesc_qk, ks > 0 ? 1u : 0u);
         }
         mma_commit(&sm.s_full[t]);
       };
       auto issue_pv = [&](int t, int st, int j) {
-        const uint32_t va = smem_u32(sm.v[st]);
+        const uint64_t vd = st ? vd1 : vd0;
         const uint32_t tS = tmem + static_cast<uint32_t>(t) * 128u;
         const uint32_t tO = tmem + 256u + static_cast<uint32_t>(t) * 128u;
 #pragma unroll
         for (int ks = 0; ks < kTileRows / 16; ++ks)
-          mma_ts(tO, tS + ks * 8, smem_desc_sw128(va + ks * 2048, kBoxBytes, 1024), idesc_pv,
-                 (j > 0 || ks > 0) ? 1u : 0u);
+          mma_ts(tO, tS + ks * 8, vd + ((ks * 2048) >> 4), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&sm.o_done[t]);
       };
       bool ok = mbar_wait(&sm.q_full, 0, wd, a.status, kStatusTimeout);
