@@ -319,6 +319,7 @@ tg_status tg_gated_attention_fwd(const void* q, const void* k, const void* v, co
   a.pos = pos_kept; a.s_kept = s_kept; a.gain = gain; a.cu_kept = cu_kept; a.batch = batch;
   a.n_kept = n_kept; a.max_kept = max_kept; a.hq = hq; a.hkv = hkv; a.head_dim = head_dim;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / (std::sqrt(static_cast<double>(head_dim)) * tau));
+  a.bias_unit = static_cast<float>(std::sqrt(static_cast<double>(head_dim)) * tau);
   a.o = o; a.lse = lse; a.status = di->status; a.watchdog = g_watchdog_cycles;
   e = launch_attention(mq, mk, mv, a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");

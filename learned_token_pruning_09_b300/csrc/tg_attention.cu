@@ -11,14 +11,18 @@
 //     consecutive row blocks of one head (hq/hkv odd);
 //   * warp 8 streams K and V tiles (128 keys x D) with TMA into a 2-stage
 //     ring, plus each key's score and original position;
-//   * warp 9 issues the MMAs: S_t = Q_t K^T into TMEM (fp32, 128 columns per
-//     tile), then O_t += P_t V with P_t read straight from TMEM;
+//   * warp 9 issues the MMAs: S_t = Q_t K^T + (gain_h sqrt(D) tau) s_j into
+//     TMEM (fp32, 128 columns per tile), then O_t += P_t V with P_t read
+//     straight from TMEM.  The score bias rides in one extra 16-wide K step:
+//     Q_t gets the columns (g_hi, g_hi, g_lo) and K the columns (s_hi, s_lo,
+//     s_hi), bf16 hi/lo splits of g = gain_h sqrt(D) tau and s_j, so the
+//     product carries g s_j to about 2^-16 relative;
 //   * warps 0-3 / 4-7 are the softmax warpgroups of tile 0 / tile 1, one
-//     thread per query row: they read S from TMEM, fold scale, log2(e), the
-//     gain-scaled score bias and the causal mask on ORIGINAL positions into
-//     the logits, keep the running max/sum (the max only moves when it grows
-//     by more than 2^8, so O is rarely rescaled), write P as bf16 back into
-//     TMEM over S, and finally normalise O and store it.
+//     thread per query row: they read S from TMEM, fold scale and log2(e)
+//     and the causal mask on ORIGINAL positions into the logits, keep the
+//     running max/sum (the max only moves when it grows by more than 2^8, so
+//     O is rarely rescaled), write P as bf16 back into TMEM over S, and
+//     finally normalise O and store it.
 //   TMEM: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [384,384+D).
 //
 // Keys are visited only up to the query tile's diagonal: positions strictly
@@ -31,14 +35,19 @@ namespace tg {
 constexpr int kAttnThreads = 384;   // 2 softmax warpgroups + producer/MMA warpgroup
 // Register split by setmaxnreg: the kernel launches with kLaunchRegs per
 // thread (384 x 168 = 64512); the softmax warpgroups grow to kSoftmaxRegs and
-// the producer/MMA warpgroup shrinks to kCtrlRegs, 2*128*200 + 128*96 = 63488.
+// the producer/MMA warpgroup shrinks to kCtrlRegs, 2*128*192 + 128*112 = 63488.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 200;
-constexpr int kCtrlRegs = 96;
+constexpr int kSoftmaxRegs = 192;
+constexpr int kCtrlRegs = 112;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kCtrlRegs <= kAttnThreads * kLaunchRegs, "register split");
 constexpr int kTileRows = 128;
 constexpr int kKvStages = 2;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+// byte offset of row r's first 16-byte core-matrix row in a bias K step
+__device__ __forceinline__ uint32_t bias_row_offset(int r) {
+  return static_cast<uint32_t>((r >> 3) * 256 + (r & 7) * 16);
+}
 
 template <int kD>
 struct AttnSmem {
@@ -46,17 +55,20 @@ struct AttnSmem {
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t k[kKvStages][kTileBytes];
   alignas(1024) uint8_t v[kKvStages][kTileBytes];
-  float bias[kKvStages][2][kTileRows];     // gain_h * log2(e) * s_j per tile
+  // the bias K step, bf16 in no-swizzle K-major core matrices (8 rows x
+  // 16 B; the two 8-column halves of a row group 128 B apart, row groups
+  // 256 B apart): Q side per tile, K side per stage
+  alignas(256) uint8_t qx[2][kTileRows * 32];
+  alignas(256) uint8_t kx[kKvStages][kTileRows * 32];
   int32_t kpos[kKvStages][kTileRows];
   int32_t kmax[kKvStages];
   uint64_t q_full;
   uint64_t k_full[kKvStages];
   uint64_t v_full[kKvStages];
-  uint64_t kv_empty[kKvStages];
-  uint64_t meta_full[kKvStages];   // per-key scores/positions of a stage written
-  uint64_t s_full[2];
+  uint64_t meta_full[kKvStages];   // key positions of a stage written
+  uint64_t s_full[2][2];            // [tile][step parity]: S_t(j) in TMEM
   uint64_t p_full[2];
-  uint64_t o_done[2];
+  uint64_t o_done[2];              // the last product into O_t done
   uint64_t mma_final[2];
   uint32_t tmem_base;
   volatile int abort;
@@ -113,11 +125,11 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     for (int s = 0; s < kKvStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
       mbar_init(&sm.meta_full[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.s_full[t][0], 1);
+      mbar_init(&sm.s_full[t][1], 1);
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_done[t], 1);
     }
@@ -127,6 +139,26 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     fence_barrier_init();
   }
   if (warp == 9) { tmem_alloc(&sm.tmem_base, 512); tmem_relinquish(); }
+  {
+    // Q-side bias columns of both tiles; the K side's upper half stays zero
+    const int i = threadIdx.x;
+    if (i < 2 * kTileRows) {
+      const int t = i / kTileRows, r = i % kTileRows;
+      const float g = __ldg(a.gain + (t ? head[1] : head[0])) * a.bias_unit;
+      const __nv_bfloat16 g_hi = __float2bfloat16_rn(g);
+      const __nv_bfloat16 g_lo = __float2bfloat16_rn(g - __bfloat162float(g_hi));
+      uint8_t* row = sm.qx[t] + bias_row_offset(r);
+      const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(g_hi));
+      const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(g_lo));
+      *reinterpret_cast<uint4*>(row) = make_uint4(hi | (hi << 16), lo, 0u, 0u);
+      *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      const int r = i - 2 * kTileRows;
+      for (int s = 0; s < kKvStages; ++s)
+        *reinterpret_cast<uint4*>(sm.kx[s] + bias_row_offset(r) + 128) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -136,8 +168,6 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
   if (warp == 8) {
     // ======================= producer =======================
-    const float gh0 = __ldg(a.gain + head[0]) * 1.4426950408889634f;
-    const float gh1 = __ldg(a.gain + head[1]) * 1.4426950408889634f;
     if (lane == 0) {
       prefetch_tmap(&map_q); prefetch_tmap(&map_k); prefetch_tmap(&map_v);
       mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
@@ -146,9 +176,9 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
           tma_load_3d(sm.q[t] + bx * kBoxBytes, &map_q, &sm.q_full, bx * 64, t ? head[1] : head[0],
                       seq_start + (t ? row0[1] : row0[0]));
     }
-    // Each key's score and position (read by the softmax warps only) are
-    // fetched into registers one tile ahead, so that the K/V copies of a
-    // freed stage are issued without waiting for those loads.
+    // Each key's score (for the bias columns) and position (for the causal
+    // mask) are fetched into registers one tile ahead, so that the K/V
+    // copies of a freed stage are issued without waiting for those loads.
     float sv[kTileRows / 32];
     int pv[kTileRows / 32];
     auto load_meta = [&](int j) {
@@ -164,31 +194,55 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       }
     };
     load_meta(0);
-    int issued = 0;
+    int issued_k = 0, issued_v = 0;   // tiles whose K / V copies were issued
     for (int j = 0; j < n_kv; ++j) {
       const int st = j & 1;
-      const uint32_t use = j >> 1;
+      // The MMAs of one thread complete in issue order, so S_1(m) done
+      // implies every earlier product done.  K of tile j (and its bias
+      // columns) may replace tile j-2's once S_1(j-2) is done; V (and the key
+      // positions, which the softmax of tile j-2 reads) once PV_1(j-2) is,
+      // i.e. once S_1(j-1) is.
+      // Each S_1 barrier completes every other step, and the MMAs cannot run
+      // two of its phases ahead of this warp (S_1(j) needs the K copy issued
+      // here), so a parity wait is unambiguous.
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&sm.kv_empty[st], (use & 1u) ^ 1u, wd, a.status, kStatusTimeout);
+      const int krow = seq_start + j * kTileRows;
+      if (lane == 0 && j >= 2) ok = mbar_wait(&sm.s_full[1][st], ((j - 2) >> 1) & 1u, wd, a.status, kStatusTimeout);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || sm.abort) { sm.abort = 1; break; }
+      // K-side bias columns (s_hi, s_lo, s_hi) of this tile's keys; an
+      // infinite score keeps (s, 0, 0) so that no 0 * inf appears
+#pragma unroll
+      for (int u = 0; u < kTileRows / 32; ++u) {
+        const float s = sv[u];
+        const __nv_bfloat16 s_hi = __float2bfloat16_rn(s);
+        const __nv_bfloat16 s_lo = isinf(s) ? __float2bfloat16_rn(0.0f) : __float2bfloat16_rn(s - __bfloat162float(s_hi));
+        const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(s_hi));
+        const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(s_lo));
+        const uint32_t third = isinf(s) ? 0u : hi;
+        *reinterpret_cast<uint4*>(sm.kx[st] + bias_row_offset(u * 32 + lane)) = make_uint4(hi | (lo << 16), third, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
       if (lane == 0) {
-        const int krow = seq_start + j * kTileRows;
         mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
         for (int bx = 0; bx < kBoxes; ++bx)
           tma_load_3d(sm.k[st] + bx * kBoxBytes, &map_k, &sm.k_full[st], bx * 64, kvh, krow);
-        mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-        for (int bx = 0; bx < kBoxes; ++bx)
-          tma_load_3d(sm.v[st] + bx * kBoxBytes, &map_v, &sm.v_full[st], bx * 64, kvh, krow);
+        issued_k = j + 1;
+        if (j >= 2) ok = mbar_wait(&sm.s_full[1][st ^ 1], ((j - 1) >> 1) & 1u, wd, a.status, kStatusTimeout);
+        if (ok) {
+          mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+          for (int bx = 0; bx < kBoxes; ++bx)
+            tma_load_3d(sm.v[st] + bx * kBoxBytes, &map_v, &sm.v_full[st], bx * 64, kvh, krow);
+          issued_v = j + 1;
+        }
       }
-      issued = j + 1;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || sm.abort) { sm.abort = 1; break; }
       int kmax = INT_MIN;
 #pragma unroll
       for (int u = 0; u < kTileRows / 32; ++u) {
-        const int c = u * 32 + lane;
-        sm.bias[st][0][c] = gh0 * sv[u];
-        sm.bias[st][1][c] = gh1 * sv[u];
-        sm.kpos[st][c] = pv[u];
+        sm.kpos[st][u * 32 + lane] = pv[u];
         kmax = max(kmax, pv[u]);
       }
       for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
@@ -200,21 +254,24 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     if (lane == 0) {
       // every issued copy must land before the CTA may leave
       mbar_wait(&sm.q_full, 0, kDrainCycles, a.status, kStatusTimeout);
-      for (int st = 0; st < kKvStages && st < issued; ++st) {
-        const int last = ((issued - 1 - st) / kKvStages) * kKvStages + st;
-        const uint32_t par = static_cast<uint32_t>(last >> 1) & 1u;
-        mbar_wait(&sm.k_full[st], par, kDrainCycles, a.status, kStatusTimeout);
-        mbar_wait(&sm.v_full[st], par, kDrainCycles, a.status, kStatusTimeout);
-      }
+      auto drain = [&](uint64_t* full, int issued) {
+        for (int st = 0; st < kKvStages && st < issued; ++st) {
+          const int last = ((issued - 1 - st) / kKvStages) * kKvStages + st;
+          mbar_wait(&full[st], static_cast<uint32_t>(last >> 1) & 1u, kDrainCycles, a.status, kStatusTimeout);
+        }
+      };
+      drain(sm.k_full, issued_k);
+      drain(sm.v_full, issued_v);
     }
   } else if (warp == 9) {
     // ======================= MMA issuer =======================
     // tcgen05.mma operations of one thread execute in issue order, so
     // S_t(j+1), issued after O_t += P_t(j) V_j, overwrites the TMEM columns
-    // of P_t(j) only after that product has read them.  The single issuing
-    // thread polls its barriers without suspending (test_wait), which keeps
-    // its reaction to a finished softmax short.
-    if (lane == 0) {
+    // of P_t(j) only after that product has read them.  The whole warp runs
+    // this loop, so that the descriptors stay warp-uniform, and one elected
+    // lane issues; it polls its barriers without suspending (test_wait),
+    // which keeps its reaction to a finished softmax short.
+    {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(128, kD, 0, 1);
       // shared-memory descriptors are built once; a K step only advances the
@@ -225,16 +282,21 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const uint64_t kd1 = smem_desc_sw128(smem_u32(sm.k[1]), 16, 1024);
       const uint64_t vd0 = smem_desc_sw128(smem_u32(sm.v[0]), kBoxBytes, 1024);
       const uint64_t vd1 = smem_desc_sw128(smem_u32(sm.v[1]), kBoxBytes, 1024);
-      auto issue_s = [&](int t, int st) {
+      const uint64_t qxd0 = smem_desc_interleave(smem_u32(sm.qx[0]), 128, 256);
+      const uint64_t qxd1 = smem_desc_interleave(smem_u32(sm.qx[1]), 128, 256);
+      const uint64_t kxd0 = smem_desc_interleave(smem_u32(sm.kx[0]), 128, 256);
+      const uint64_t kxd1 = smem_desc_interleave(smem_u32(sm.kx[1]), 128, 256);
+      auto issue_s = [&](int t, int st, int j) {
         const uint64_t qd = t ? qd1 : qd0;
         const uint64_t kd = st ? kd1 : kd0;
         const uint32_t tS = tmem + static_cast<uint32_t>(t) * 128u;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
           const uint32_t off = ((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tS, qd + off, kd + off, idesc_qk, ks > 0 ? 1u : 0u);
+          mma_ss_warp(tS, qd + off, kd + off, idesc_qk, ks > 0 ? 1u : 0u);
         }
-        mma_commit(&sm.s_full[t]);
+        mma_ss_warp(tS, t ? qxd1 : qxd0, st ? kxd1 : kxd0, idesc_qk, 1u);   // + g s_j
+        mma_commit_warp(&sm.s_full[t][j & 1]);
       };
       auto issue_pv = [&](int t, int st, int j) {
         const uint64_t vd = st ? vd1 : vd0;
@@ -242,15 +304,18 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const uint32_t tO = tmem + 256u + static_cast<uint32_t>(t) * 128u;
 #pragma unroll
         for (int ks = 0; ks < kTileRows / 16; ++ks)
-          mma_ts(tO, tS + ks * 8, vd + ((ks * 2048) >> 4), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(&sm.o_done[t]);
+          mma_ts_warp(tO, tS + ks * 8, vd + ((ks * 2048) >> 4), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+        if (j == n_kv - 1) mma_commit_warp(&sm.o_done[t]);
       };
-      bool ok = mbar_wait(&sm.q_full, 0, wd, a.status, kStatusTimeout);
-      ok = ok && mbar_wait(&sm.k_full[0], 0, wd, a.status, kStatusTimeout);
+      // every lane polls; the verdict is made warp-uniform
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait_spin(bar, parity, wd, a.status, kStatusTimeout) && !sm.abort);
+      };
+      bool ok = wait(&sm.q_full, 0) && wait(&sm.k_full[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
+        issue_s(0, 0, 0);
+        issue_s(1, 0, 0);
       }
       for (int j = 0; j < n_kv && ok; ++j) {
         const int st = j & 1;
@@ -259,25 +324,23 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const bool more = j + 1 < n_kv;
         const int st2 = (j + 1) & 1;
         const uint32_t use2 = (j + 1) >> 1;
-        ok = mbar_wait_spin(&sm.v_full[st], use & 1u, wd, a.status, kStatusTimeout) && !sm.abort;
-        ok = ok && mbar_wait_spin(&sm.p_full[0], pj, wd, a.status, kStatusTimeout) && !sm.abort;
+        ok = wait(&sm.v_full[st], use & 1u) && wait(&sm.p_full[0], pj);
         if (!ok) break;
         tc_fence_after();
         issue_pv(0, st, j);
         if (more) {
-          ok = mbar_wait_spin(&sm.k_full[st2], use2 & 1u, wd, a.status, kStatusTimeout);
+          ok = wait(&sm.k_full[st2], use2 & 1u);
           if (!ok) break;
-          issue_s(0, st2);
+          issue_s(0, st2, j + 1);
         }
-        ok = mbar_wait_spin(&sm.p_full[1], pj, wd, a.status, kStatusTimeout) && !sm.abort;
+        ok = wait(&sm.p_full[1], pj);
         if (!ok) break;
         tc_fence_after();
         issue_pv(1, st, j);
-        mma_commit(&sm.kv_empty[st]);
-        if (more) issue_s(1, st2);
+        if (more) issue_s(1, st2, j + 1);
       }
       if (!ok) sm.abort = 1;
-      mma_commit(&sm.mma_final[0]);
+      mma_commit_warp(&sm.mma_final[0]);
       mbar_wait(&sm.mma_final[0], 0, kDrainCycles, a.status, kStatusTimeout);
     }
   }
@@ -301,24 +364,24 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const int st = j & 1;
       const uint32_t use = j >> 1;
       bool w = mbar_wait(&sm.meta_full[st], use & 1u, wd, a.status, kStatusTimeout);
-      w = w && mbar_wait(&sm.s_full[t], j & 1u, wd, a.status, kStatusTimeout);
+      w = w && mbar_wait(&sm.s_full[t][st], use & 1u, wd, a.status, kStatusTimeout);
       ok = __all_sync(0xffffffffu, w) && !sm.abort;
       if (!ok) break;
       tc_fence_after();
-      // logits in log2 units: x = S * log2(e)/(sqrt(D) tau) + gain_h log2(e) s_j,
-      // one TMEM read of the whole 128-column row, then max, exp2 and P.
+      // logits in log2 units: x = S * log2(e)/(sqrt(D) tau) (the score bias
+      // is already in S), one TMEM read of the whole 128-column row, then
+      // max, exp2 and P.
       uint32_t rr[kTileRows];
 #pragma unroll
       for (int c = 0; c < kTileRows / 32; ++c)
         tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[c * 32]));
-      const float2* bias2 = reinterpret_cast<const float2*>(sm.bias[st][t]);
       const bool masked = __any_sync(0xffffffffu, sm.kmax[st] > qpos);
       const int* kp = sm.kpos[st];
       tmem_ld_wait();
       float2 x[kTileRows / 2];
 #pragma unroll
       for (int i = 0; i < kTileRows / 2; ++i)
-        x[i] = __ffma2_rn(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sl, bias2[i]);
+        x[i] = __fmul2_rn(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sl);
       if (masked) {
 #pragma unroll
         for (int i = 0; i < kTileRows / 2; ++i) {
@@ -352,12 +415,9 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       }
       l = l * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
       m = m_new;
-      // rescale O when this row's max moved (warp-uniform TMEM access)
+      // rescale O when this row's max moved (warp-uniform TMEM access); the
+      // product into O of step j-1 was issued before S_t(j), so it is done
       if (__any_sync(0xffffffffu, j > 0 && alpha != 1.0f)) {
-        const bool w2 = __all_sync(0xffffffffu,
-                                   mbar_wait(&sm.o_done[t], (j - 1) & 1u, wd, a.status, kStatusTimeout));
-        if (!w2) { ok = false; break; }
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kD / 16; ++c) {
           uint32_t o16[16];
@@ -375,7 +435,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     if (!ok) sm.abort = 1;
     // ---- epilogue: O / l -> bf16 ----
     const bool w3 = ok && __all_sync(0xffffffffu,
-                                     mbar_wait(&sm.o_done[t], (n_kv - 1) & 1u, wd, a.status, kStatusTimeout));
+                                     mbar_wait(&sm.o_done[t], 0, wd, a.status, kStatusTimeout));
     if (w3) {
       tc_fence_after();
       const float inv = 1.0f / l;

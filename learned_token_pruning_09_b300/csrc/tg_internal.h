@@ -98,6 +98,7 @@ struct AttnArgs {
   int32_t max_kept;
   int32_t hq, hkv, head_dim;
   float scale_log2;     // log2(e) / (sqrt(D) * tau)
+  float bias_unit;      // sqrt(D) * tau: the score bias in units of q.k
   void* o;
   float* lse;
   unsigned int* status;
