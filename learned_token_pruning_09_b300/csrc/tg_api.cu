@@ -166,7 +166,8 @@ tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d, const int
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(h)};
     const uint64_t str[1] = {static_cast<uint64_t>(d) * 2};
-    const uint32_t box[2] = {64, static_cast<uint32_t>(h)};
+    // each CTA of a pair stages one half of W1's rows
+    const uint32_t box[2] = {64, static_cast<uint32_t>(h / 2)};
     if ((s = make_map(&mw, w1_bf16, 2, dims, str, box, "w1")) != TG_OK) return s;
   }
   GateArgs a{};

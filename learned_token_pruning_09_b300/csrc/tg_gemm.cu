@@ -2,15 +2,15 @@
 // memory stages:
 //
 //  * gate_kernel  -- TokenGate's gate MLP scorer (gate module: "an MLP scores
-//    every token from its post-attention residual at layer L").  One CTA
-//    takes 128 residual rows; the tensor cores compute U = X W1^T (128 x h,
-//    fp32 in TMEM) and the epilogue fuses + b1, exact-erf GELU, the 1-wide
-//    projection with w2, + b2 and logsigmoid, writing one fp32 score per row
-//    (0 for question rows).
+//    every token from its post-attention residual at layer L").  A pair of
+//    CTAs takes 256 residual rows at a time; the pair's tensor cores compute
+//    U = X W1^T (256 x h, fp32 in TMEM) and the epilogue fuses + b1,
+//    exact-erf GELU, the 1-wide projection with w2, + b2 and logsigmoid,
+//    writing one fp32 score per row (0 for question rows).
 //  * linear_kernel -- out = A W^T (+ residual) in bf16, the per-layer Q/K/V and
 //    output projections of the stacked long-context workload.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 allocates TMEM
+// linear_kernel's warp roles (192 threads): warp 0 issues TMA loads, warp 1 allocates TMEM
 // and issues the MMAs (one elected lane), warps 2..5 run the epilogue, one
 // thread per accumulator row (warp w reads TMEM lanes 32*(w%4)..+31).
 #include "tg_common.cuh"
@@ -108,31 +108,35 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
 // ---------------------------------------------------------------------------
 // gate
 // ---------------------------------------------------------------------------
-// Persistent: one CTA per SM.  The residual rows are cut into 128-row blocks;
-// CTA c owns blocks c, c + G, c + 2G, ... (G CTAs) and takes them two at a
-// time.  The two blocks of a pass accumulate into two TMEM accumulators and
-// share every W1 stage, which halves the W1 reads from L2 compared with one
-// block per pass; a CTA left with one block runs a half pass.  Each pass
-// walks its K blocks from a different starting block so that the CTAs do not
-// all read the same W1 block at the same moment.  The epilogue (8 warps:
-// warps 4-7 take the first block, warps 8-11 the second) releases TMEM
-// before its final transform and store, so the next pass's MMAs start while
-// it finishes; the producer runs ahead across passes.
-constexpr int kGateThreads = 384;
-constexpr int kGateM = 256;
+// CTA pairs (clusters of two CTAs, one per SM): the two tensor cores of a pair
+// compute U = X W1^T for 256 residual rows at a time with M=256 pair MMAs.
+// Each CTA stages its own 128 rows of X and one half of W1's h rows (the B
+// operand is split across the pair), which halves the shared-memory traffic
+// per SM compared with one SM holding all of W1.  The accumulators (h fp32
+// columns per row) are double-buffered in TMEM, so that the epilogue of one
+// 256-row block runs while the MMAs of the next one fill the other buffer.
+// Pair q takes blocks q, q + P, q + 2P, ... (P pairs) and walks each block's K
+// from a different starting point, so that the pairs do not all read the same
+// W1 block from L2 at the same moment.
+//
+// Warp roles (256 threads per CTA): warp 0 lane 0 issues this CTA's TMA loads,
+// whose completion both CTAs count on the leader's (rank 0) stage barrier; in
+// the leader warp 1 lane 0 issues the pair MMAs; warp 1 of each CTA takes part
+// in the pair's TMEM allocation; warps 4-7 run the epilogue on the CTA's own
+// 128 rows, one thread per row.
+constexpr int kGateThreads = 256;
 constexpr int kGateMaxStages = 8;
-constexpr int kGateATileBytes = kGateM * kBK * 2;   // 32 KB
 constexpr int kGateSmemBudget = 200 * 1024;
+constexpr uint32_t kGateXBytes = kBM * kBK * 2;     // 16 KB: 128 rows of one K block
 
 struct GateSmemHead {
-  uint64_t a_full[kGateMaxStages];
-  uint64_t a_empty[kGateMaxStages];
-  uint64_t b_full[kGateMaxStages];
-  uint64_t b_empty[kGateMaxStages];
-  uint64_t acc_full;
-  uint64_t acc_empty;
+  uint64_t full[kGateMaxStages];        // leader: both CTAs' copies of a stage landed
+  uint64_t empty[kGateMaxStages];       // the pair's MMAs are done with a stage
+  uint64_t acc_full[2];                 // accumulator buffer complete
+  uint64_t acc_empty[2];                // leader: both epilogues have read a buffer
   uint64_t mma_done;
   uint32_t tmem_base;
+  uint32_t peer_issued;                 // leader: stages the other CTA issued
   volatile int abort;
 };
 
@@ -154,176 +158,158 @@ __device__ __forceinline__ bool row_is_doc(const GateArgs& a, long long row) {
 
 __global__ void __launch_bounds__(kGateThreads, 1)
 gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w1,
-            GateArgs a, int n_a, int n_b) {
+            GateArgs a, int n_st) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ GateSmemHead head;
   __shared__ __align__(16) float sb1[256];
   __shared__ __align__(16) float sw2[256];
-  // two rings: residual rows (from HBM, deeper) and W1 (L2-resident)
-  uint8_t* ring_a = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = warp_id();
   const int lane = lane_id();
-  const uint32_t half_cols = tmem_cols_for(a.h);
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t half_cols = tmem_cols_for(a.h);   // one accumulator buffer
   const uint32_t ncols = 2 * half_cols;
-  const int n_blocks = static_cast<int>((a.n_rows + kBM - 1) / kBM);
-  const int G = gridDim.x;
-  const int c = blockIdx.x;
-  // pass p of this CTA covers blocks c + 2pG and c + (2p+1)G (if it exists)
-  const int n_pass = (n_blocks - c + 2 * G - 1) / (2 * G);
+  const int hb = a.h / 2;                          // W1 rows staged by each CTA
+  const uint32_t stage_bytes = kGateXBytes + static_cast<uint32_t>(hb) * kBK * 2;
+  const long long n_blocks = (a.n_rows + 2 * kBM - 1) / (2 * kBM);   // 256-row blocks
+  const int n_pairs = static_cast<int>(gridDim.x >> 1);
+  const int q = static_cast<int>(blockIdx.x >> 1);
+  const int n_pass = (q < n_blocks) ? static_cast<int>((n_blocks - q + n_pairs - 1) / n_pairs) : 0;
   const int nk = a.d / kBK;
-  const uint32_t b_bytes = static_cast<uint32_t>(a.h) * kBK * 2;
-  uint8_t* ring_b = ring_a + static_cast<size_t>(n_a) * kGateATileBytes;
   const long long wd = a.watchdog;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < n_a; ++i) { mbar_init(&head.a_full[i], 1); mbar_init(&head.a_empty[i], 1); }
-    for (int i = 0; i < n_b; ++i) { mbar_init(&head.b_full[i], 1); mbar_init(&head.b_empty[i], 1); }
-    mbar_init(&head.acc_full, 1);
-    mbar_init(&head.acc_empty, 256);
+    for (int i = 0; i < n_st; ++i) {
+      mbar_init(&head.full[i], 1);
+      mbar_init(&head.empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&head.acc_full[b], 1);
+      mbar_init(&head.acc_empty[b], 2 * 4);   // one arrive per epilogue warp of both CTAs
+    }
     mbar_init(&head.mma_done, 1);
     head.abort = 0;
     fence_barrier_init();
     prefetch_tmap(&map_x);
     prefetch_tmap(&map_w1);
   }
-  if (warp == 1) { tmem_alloc(&head.tmem_base, ncols); tmem_relinquish(); }
+  if (warp == 1) { tmem_alloc_pair(&head.tmem_base, ncols); tmem_relinquish_pair(); }
   for (int i = threadIdx.x; i < a.h; i += kGateThreads) {
     sb1[i] = a.b1 ? a.b1[i] : 0.0f;
     sw2[i] = __bfloat162float(a.w2[i]);
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();      // both CTAs' barriers exist before either signals the other
   tc_fence_after();
 
-  if ((warp == 0 || warp == 2) && lane == 0) {
-    // ---------------- TMA producers: warp 0 residual rows, warp 2 W1 ----------------
-    const bool rows = warp == 0;
-    const int n_st = rows ? n_a : n_b;
-    uint64_t* full = rows ? head.a_full : head.b_full;
-    uint64_t* empty = rows ? head.a_empty : head.b_empty;
-    uint32_t g = 0;                 // k blocks issued (the rings run across passes)
+  uint32_t issued = 0;                 // warp 0 lane 0: stages this CTA issued
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer: this CTA's X rows and W1 half ----------------
+    const uint32_t full0 = mapa_shared(smem_u32(&head.full[0]), 0);
     for (int p = 0; p < n_pass && !head.abort; ++p) {
-      const int blk0 = c + 2 * p * G;
-      const int blk1 = blk0 + G;
-      const bool has1 = blk1 < n_blocks;
-      const int kb0 = (c + p) % nk;
+      const long long blk = q + static_cast<long long>(p) * n_pairs;
+      const int row0 = static_cast<int>(blk * 2 * kBM) + static_cast<int>(rank) * kBM;
+      const int kb0 = (q + p) % nk;
       for (int i = 0; i < nk; ++i) {
         int kb = kb0 + i;
         if (kb >= nk) kb -= nk;
+        const int st = static_cast<int>(issued % n_st);
+        const uint32_t use = issued / n_st;
+        if (!mbar_wait(&head.empty[st], (use & 1u) ^ 1u, wd, a.status, kStatusTimeout) || head.abort) {
+          head.abort = 1;
+          break;
+        }
+        uint8_t* s = ring + st * stage_bytes;
+        if (leader) mbar_arrive_expect_tx(&head.full[st], 2 * stage_bytes);
+        tma_load_2d_pair(s, &map_x, full0 + st * 8u, kb * kBK, row0);
+        tma_load_2d_pair(s + kGateXBytes, &map_w1, full0 + st * 8u, kb * kBK, static_cast<int>(rank) * hb);
+        ++issued;
+      }
+    }
+    if (!leader) st_cluster_u32(mapa_shared(smem_u32(&head.peer_issued), 0), issued);
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ---------------- pair MMA issuer ----------------
+    const uint32_t idesc = idesc_bf16_f32(2 * kBM, static_cast<uint32_t>(a.h), 0, 0);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int p = 0; p < n_pass && ok; ++p) {
+      const int b = p & 1;
+      // the epilogues of both CTAs must have read this buffer's previous block
+      ok = mbar_wait(&head.acc_empty[b], ((static_cast<uint32_t>(p) >> 1) & 1u) ^ 1u, wd, a.status, kStatusTimeout) &&
+           !head.abort;
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = head.tmem_base + static_cast<uint32_t>(b) * half_cols;
+      for (int i = 0; i < nk; ++i, ++g) {
         const int st = static_cast<int>(g % n_st);
-        const uint32_t use = g / n_st;
-        if (!mbar_wait(&empty[st], (use & 1u) ^ 1u, wd, a.status, kStatusTimeout) || head.abort) {
-          head.abort = 1;
-          break;
-        }
-        if (rows) {
-          uint8_t* sa = ring_a + st * kGateATileBytes;
-          mbar_arrive_expect_tx(&full[st], (has1 ? 2u : 1u) * kATileBytes);
-          tma_load_2d(sa, &map_x, &full[st], kb * kBK, blk0 * kBM);
-          if (has1) tma_load_2d(sa + kATileBytes, &map_x, &full[st], kb * kBK, blk1 * kBM);
-        } else {
-          mbar_arrive_expect_tx(&full[st], b_bytes);
-          tma_load_2d(ring_b + st * b_bytes, &map_w1, &full[st], kb * kBK, 0);
-        }
-        ++g;
-      }
-    }
-    // the last copies into every stage must land before the CTA may leave
-    for (uint32_t st = 0; st < static_cast<uint32_t>(n_st) && st < g; ++st) {
-      const uint32_t last = ((g - 1 - st) / n_st) * n_st + st;
-      mbar_wait(&full[st], (last / n_st) & 1u, kDrainCycles, a.status, kStatusTimeout);
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(a.h), 0, 0);
-      const uint32_t acc0 = head.tmem_base;
-      const uint32_t acc1 = head.tmem_base + half_cols;
-      uint32_t g = 0;
-      for (int it = 0; it < n_pass && !head.abort; ++it) {
-        const bool has1 = c + (2 * it + 1) * G < n_blocks;
-        // the epilogue must have read the previous pass's accumulators
-        if (!mbar_wait(&head.acc_empty, (static_cast<uint32_t>(it) & 1u) ^ 1u, wd, a.status, kStatusTimeout)) {
-          head.abort = 1;
-          break;
-        }
-        tc_fence_after();
-        bool ok = true;
-        for (int i = 0; i < nk; ++i, ++g) {
-          const int sa_i = static_cast<int>(g % n_a);
-          const int sb_i = static_cast<int>(g % n_b);
-          if (!mbar_wait(&head.a_full[sa_i], (g / n_a) & 1u, wd, a.status, kStatusTimeout) ||
-              !mbar_wait(&head.b_full[sb_i], (g / n_b) & 1u, wd, a.status, kStatusTimeout) || head.abort) {
-            head.abort = 1;
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(ring_a + sa_i * kGateATileBytes);
-          const uint32_t sb = smem_u32(ring_b + sb_i * b_bytes);
-#pragma unroll
-          for (int ks = 0; ks < kBK / 16; ++ks) {
-            const uint64_t db = smem_desc_sw128(sb + ks * 32, 16, 1024);
-            const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
-            mma_ss(acc0, smem_desc_sw128(sa + ks * 32, 16, 1024), db, idesc, acc);
-            if (has1) mma_ss(acc1, smem_desc_sw128(sa + kATileBytes + ks * 32, 16, 1024), db, idesc, acc);
-          }
-          mma_commit(&head.a_empty[sa_i]);
-          mma_commit(&head.b_empty[sb_i]);
-        }
-        mma_commit(&head.acc_full);
+        const uint32_t par = (g / n_st) & 1u;
+        ok = mbar_wait(&head.full[st], par, wd, a.status, kStatusTimeout) && !head.abort;
         if (!ok) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(ring + st * stage_bytes);
+        const uint32_t sb = sa + kGateXBytes;
+#pragma unroll
+        for (int ks = 0; ks < kBK / 16; ++ks)
+          mma_ss_pair(d, smem_desc_sw128(sa + ks * 32, 16, 1024), smem_desc_sw128(sb + ks * 32, 16, 1024), idesc,
+                      (i > 0 || ks > 0) ? 1u : 0u);
+        mma_commit_pair_mc(&head.empty[st], 0x3);
       }
-      // every MMA must have finished before TMEM may be freed
-      mma_commit(&head.mma_done);
-      mbar_wait(&head.mma_done, 0, kDrainCycles, a.status, kStatusTimeout);
+      if (ok) mma_commit_pair_mc(&head.acc_full[b], 0x3);
     }
+    if (!ok) head.abort = 1;
+    // every MMA must have finished before TMEM may be freed
+    mma_commit_pair_mc(&head.mma_done, 0x1);
+    mbar_wait(&head.mma_done, 0, kDrainCycles, a.status, kStatusTimeout);
   } else if (warp >= 4) {
     // ---------------- epilogue: + b1, GELU, . w2, + b2, logsigmoid ----------------
-    const int half = (warp - 4) >> 2;
     const int sub = warp & 3;                               // TMEM lane quarter
-    const uint32_t taddr = head.tmem_base + half * half_cols + (static_cast<uint32_t>(sub * 32) << 16);
-    for (int it = 0; it < n_pass; ++it) {
-      const int blk = c + (2 * it + half) * G;
-      const long long row = static_cast<long long>(blk) * kBM + sub * 32 + lane;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&head.acc_full, static_cast<uint32_t>(it) & 1u, wd,
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(&head.acc_empty[0]), 0);
+    for (int p = 0; p < n_pass; ++p) {
+      const int b = p & 1;
+      const long long blk = q + static_cast<long long>(p) * n_pairs;
+      const long long row = blk * 2 * kBM + static_cast<long long>(rank) * kBM + sub * 32 + lane;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&head.acc_full[b], (static_cast<uint32_t>(p) >> 1) & 1u, wd,
                                                          a.status, kStatusTimeout));
       if (!ok || head.abort) { head.abort = 1; break; }
       tc_fence_after();
+      const uint32_t taddr = head.tmem_base + static_cast<uint32_t>(b) * half_cols +
+                             (static_cast<uint32_t>(sub * 32) << 16);
       // Branch-free 32-column chunks (then one 16-column tail when h % 32 ==
-      // 16) so the GELU chains of a chunk interleave; four partial sums.
+      // 16) so the GELU chains of a chunk interleave; two partial sums.
       float2 zp[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
       const float2* b1p = reinterpret_cast<const float2*>(sb1);
       const float2* w2p = reinterpret_cast<const float2*>(sw2);
-      if (blk < n_blocks) {
-        int c0 = 0;
-        for (; c0 + 32 <= a.h; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c0, r);
-          tmem_ld_wait();
+      int c0 = 0;
+      for (; c0 + 32 <= a.h; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c0, r);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 u = __fadd2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
-                                        b1p[(c0 >> 1) + i]);
-            zp[i & 1] = __ffma2_rn(w2p[(c0 >> 1) + i], gelu_erf2(u), zp[i & 1]);
-          }
+        for (int i = 0; i < 16; ++i) {
+          const float2 u = __fadd2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                      b1p[(c0 >> 1) + i]);
+          zp[i & 1] = __ffma2_rn(w2p[(c0 >> 1) + i], gelu_erf2(u), zp[i & 1]);
         }
-        if (c0 < a.h) {
-          uint32_t r[16];
-          tmem_ld16(taddr + c0, r);
-          tmem_ld_wait();
+      }
+      if (c0 < a.h) {
+        uint32_t r[16];
+        tmem_ld16(taddr + c0, r);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float2 u = __fadd2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
-                                        b1p[(c0 >> 1) + i]);
-            zp[i & 1] = __ffma2_rn(w2p[(c0 >> 1) + i], gelu_erf2(u), zp[i & 1]);
-          }
+        for (int i = 0; i < 8; ++i) {
+          const float2 u = __fadd2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                      b1p[(c0 >> 1) + i]);
+          zp[i & 1] = __ffma2_rn(w2p[(c0 >> 1) + i], gelu_erf2(u), zp[i & 1]);
         }
       }
       float z = (zp[0].x + zp[0].y) + (zp[1].x + zp[1].y);
+      // this warp is done with the buffer: tell the leader's MMA issuer
       tc_fence_before();
-      mbar_arrive(&head.acc_empty);      // accumulators may be overwritten now
-      if (blk < n_blocks && row < a.n_rows) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(b) * 8u);
+      if (row < a.n_rows) {
         z += a.b2;
         // logsigmoid(z) = -log1p(exp(-z)) (z >= 0), z - log1p(exp(z)) (z < 0)
         const float sc = (z >= 0.0f) ? -log1pf(expf(-z)) : z - log1pf(expf(z));
@@ -333,26 +319,57 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) { tc_fence_after(); tmem_dealloc(head.tmem_base, ncols); }
+  cluster_sync();      // every role is done; the other CTA's issue count is in place
+  if (leader && warp == 0 && lane == 0) {
+    // Every copy either CTA issued must land before the pair may leave.  The
+    // two producers stop together unless a wait ran out; then the leader
+    // settles the difference: it arrives for a stage only the other CTA
+    // issued, and counts off the other CTA's share of a stage it issued alone.
+    const uint32_t peer = head.peer_issued;
+    for (uint32_t g = issued; g < peer; ++g) mbar_arrive_expect_tx(&head.full[g % n_st], stage_bytes);
+    for (uint32_t g = peer; g < issued; ++g) mbar_complete_tx(&head.full[g % n_st], stage_bytes);
+    const uint32_t last_g = issued > peer ? issued : peer;
+    for (uint32_t st = 0; st < static_cast<uint32_t>(n_st) && st < last_g; ++st) {
+      const uint32_t last = ((last_g - 1 - st) / n_st) * n_st + st;
+      mbar_wait(&head.full[st], (last / n_st) & 1u, kDrainCycles, a.status, kStatusTimeout);
+    }
+  }
+  __syncthreads();
+  cluster_sync();      // no CTA leaves while the other may still signal it
+  if (warp == 1) { tc_fence_after(); tmem_dealloc_pair(head.tmem_base, ncols); }
 }
 
 cudaError_t launch_gate(const CUtensorMap& map_x, const CUtensorMap& map_w1, const GateArgs& a,
                         cudaStream_t st) {
   if (a.n_rows == 0) return cudaSuccess;
-  // W1 stages come from L2 (two suffice); the rest of the budget holds
-  // residual-row stages, which come from HBM
-  const size_t b_bytes = static_cast<size_t>(a.h) * kBK * 2;
-  const int n_b = 2;
-  int n_a = static_cast<int>((kGateSmemBudget - n_b * b_bytes) / kGateATileBytes);
-  if (n_a > kGateMaxStages) n_a = kGateMaxStages;
-  const size_t smem = 1024 + static_cast<size_t>(n_a) * kGateATileBytes + n_b * b_bytes;
+  const size_t stage_bytes = kGateXBytes + static_cast<size_t>(a.h / 2) * kBK * 2;
+  int n_st = static_cast<int>(kGateSmemBudget / stage_bytes);
+  if (n_st > kGateMaxStages) n_st = kGateMaxStages;
+  const size_t smem = 1024 + static_cast<size_t>(n_st) * stage_bytes;
   cudaError_t e = cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long blocks = (a.n_rows + kBM - 1) / kBM;
-  const unsigned grid = static_cast<unsigned>(blocks < a.num_sms ? blocks : a.num_sms);
-  gate_kernel<<<grid, kGateThreads, smem, st>>>(map_x, map_w1, a, n_a, n_b);
-  return cudaGetLastError();
+  const long long blocks = (a.n_rows + 2 * kBM - 1) / (2 * kBM);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kGateThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // one pair per two SMs at most; a persistent pair takes several blocks
+  cfg.gridDim = dim3(2u * static_cast<unsigned>(a.num_sms / 2));
+  int n_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&n_clusters, gate_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n_clusters < 1) return cudaErrorInvalidConfiguration;
+  const long long pairs = blocks < n_clusters ? blocks : n_clusters;
+  cfg.gridDim = dim3(2u * static_cast<unsigned>(pairs));
+  return cudaLaunchKernelEx(&cfg, gate_kernel, map_x, map_w1, a, n_st);
 }
 
 // ---------------------------------------------------------------------------
