@@ -15,8 +15,9 @@
  *
  * The calls below are the steps of that path, in order:
  *   tg_gate_score -> tg_topk_select -> tg_gather_kept -> (per layer)
- *   [tg_linear_bf16 for Q/K/V] -> tg_gated_attention_fwd -> [tg_linear_bf16
- *   for the output projection with the residual add].
+ *   [tg_linear_bf16 for Q/K/V] -> tg_gated_attention_fwd (= tg_rope_qk ->
+ *   tg_gated_attention_rotated) -> [tg_linear_bf16 for the output projection
+ *   with the residual add].
  *
  * Conventions shared by every call
  * --------------------------------
@@ -167,6 +168,39 @@ TG_API tg_status tg_gated_attention_fwd(const void* q, const void* k, const void
                                  void* o, float* lse, void* k_cache,
                                  void* workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
+
+/*
+ * The two steps of tg_gated_attention_fwd as separate calls, for a caller
+ * that keeps the rotated keys (a kept-only KV cache) or times the steps.
+ *
+ * tg_rope_qk: q' and k', q and k rotated by rotate-half RoPE at the ORIGINAL
+ * positions pos_kept with base rope_theta (the angle pos * theta^(-2i/D) is
+ * formed and reduced in fp64, its sine and cosine taken in fp32), rounded to
+ * bf16.  Also checks that pos_kept is non-negative and strictly increasing
+ * within each sequence; otherwise TG_ERR_DEVICE_INDEX.
+ *   q [n_kept, hq, head_dim], k [n_kept, hkv, head_dim] bf16 inputs;
+ *   q_out, k_out of the same shapes, bf16 outputs (must not alias the inputs);
+ *   cu_kept [batch+1] int32 (device); head_dim in {64, 128}.
+ */
+TG_API tg_status tg_rope_qk(const void* q, const void* k, const int32_t* pos_kept, float rope_theta,
+                     const int32_t* cu_kept, int32_t batch, int64_t n_kept, int32_t hq,
+                     int32_t hkv, int32_t head_dim, void* q_out, void* k_out,
+                     cudaStream_t stream);
+
+/*
+ * tg_gated_attention_rotated: the attention of tg_gated_attention_fwd on
+ * inputs already rotated by tg_rope_qk (q_rot [n_kept, hq, head_dim], k_rot
+ * [n_kept, hkv, head_dim] bf16); every other argument as there.  Needs no
+ * workspace.  The kernel also checks that pos_kept strictly increases within
+ * each sequence (its causal tile skipping relies on it); otherwise
+ * TG_ERR_DEVICE_INDEX.
+ */
+TG_API tg_status tg_gated_attention_rotated(const void* q_rot, const void* k_rot, const void* v,
+                                     const int32_t* pos_kept, const float* s_kept,
+                                     const float* gain, float tau, const int32_t* cu_kept,
+                                     int32_t batch, int64_t n_kept, int32_t max_kept,
+                                     int32_t hq, int32_t hkv, int32_t head_dim, void* o,
+                                     float* lse, cudaStream_t stream);
 
 /* Bytes of workspace tg_gated_attention_fwd needs (q' and, if no k_cache is
  * given, k').  Host-only, no CUDA call. */

@@ -261,48 +261,58 @@ size_t tg_attention_workspace_size(int64_t n_kept, int32_t hq, int32_t hkv, int3
   return b;
 }
 
-tg_status tg_gated_attention_fwd(const void* q, const void* k, const void* v, const int32_t* pos_kept,
-                                 const float* s_kept, const float* gain, float tau, float rope_theta,
-                                 const int32_t* cu_kept, int32_t batch, int64_t n_kept, int32_t max_kept,
-                                 int32_t hq, int32_t hkv, int32_t head_dim, void* o, float* lse,
-                                 void* k_cache, void* workspace, size_t workspace_bytes,
-                                 cudaStream_t stream) {
+// shared argument checks of the attention calls
+static tg_status check_attention_shape(int32_t batch, int64_t n_kept, int32_t hq, int32_t hkv, int32_t head_dim,
+                                       const int32_t* cu_kept) {
   if (batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
   if (n_kept < 0 || n_kept > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_kept out of range");
-  if (max_kept < 0) return fail(TG_ERR_INVALID_ARG, "max_kept must be >= 0");
   if (hq < 1 || hkv < 1 || hq % hkv != 0) return fail(TG_ERR_INVALID_ARG, "hq must be a positive multiple of hkv");
   if (head_dim != 64 && head_dim != 128) return fail(TG_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
-  if (!(tau > 0.0f) || !std::isfinite(tau)) return fail(TG_ERR_INVALID_ARG, "tau must be positive and finite");
-  if (!(rope_theta > 0.0f) || !std::isfinite(rope_theta)) return fail(TG_ERR_INVALID_ARG, "rope_theta must be positive");
   if (!cu_kept) return fail(TG_ERR_INVALID_ARG, "null cu_kept");
-  if (n_kept == 0) return ok();
-  if (!q || !k || !v || !pos_kept || !s_kept || !gain || !o) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (k_cache && !aligned16(k_cache)))
-    return fail(TG_ERR_INVALID_ARG, "q, k, v, o and k_cache must be 16-byte aligned");
-  const size_t need = tg_attention_workspace_size(n_kept, hq, hkv, head_dim, k_cache ? 1 : 0);
-  if (!workspace || workspace_bytes < need)
-    return fail(TG_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(TG_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  if (max_kept == 0) return ok();
-  DeviceInfo* di = nullptr;
-  tg_status st = device_info(&di);
+  return TG_OK;
+}
+
+tg_status tg_rope_qk(const void* q, const void* k, const int32_t* pos_kept, float rope_theta, const int32_t* cu_kept,
+                     int32_t batch, int64_t n_kept, int32_t hq, int32_t hkv, int32_t head_dim, void* q_out,
+                     void* k_out, cudaStream_t stream) {
+  tg_status st = check_attention_shape(batch, n_kept, hq, hkv, head_dim, cu_kept);
   if (st != TG_OK) return st;
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* q_rot = ws;
-  void* k_rot = k_cache;
-  if (!k_rot) k_rot = ws + ((static_cast<size_t>(n_kept) * hq * head_dim * 2 + 255) & ~static_cast<size_t>(255));
-
+  if (!(rope_theta > 0.0f) || !std::isfinite(rope_theta)) return fail(TG_ERR_INVALID_ARG, "rope_theta must be positive");
+  if (n_kept == 0) return ok();
+  if (!q || !k || !pos_kept || !q_out || !k_out) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_out) || !aligned16(k_out))
+    return fail(TG_ERR_INVALID_ARG, "q, k, q_out and k_out must be 16-byte aligned");
+  if (q_out == q || k_out == k) return fail(TG_ERR_INVALID_ARG, "q_out and k_out must not alias q and k");
+  DeviceInfo* di = nullptr;
+  st = device_info(&di);
+  if (st != TG_OK) return st;
   RopeFreqs f{};
   for (int i = 0; i < head_dim / 2; ++i)
     f.inv_freq[i] = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim);
   RopeArgs ra{};
   ra.q = q; ra.k = k; ra.pos = pos_kept; ra.cu_kept = cu_kept; ra.batch = batch; ra.n_kept = n_kept;
-  ra.hq = hq; ra.hkv = hkv; ra.head_dim = head_dim; ra.q_out = q_rot; ra.k_out = k_rot;
+  ra.hq = hq; ra.hkv = hkv; ra.head_dim = head_dim; ra.q_out = q_out; ra.k_out = k_out;
   ra.status = di->status; ra.num_sms = di->num_sms;
-  cudaError_t e = launch_rope(ra, f, stream);
+  const cudaError_t e = launch_rope(ra, f, stream);
   if (e != cudaSuccess) return cuda_fail(e, "RoPE kernel launch");
+  return ok();
+}
 
+tg_status tg_gated_attention_rotated(const void* q_rot, const void* k_rot, const void* v, const int32_t* pos_kept,
+                                     const float* s_kept, const float* gain, float tau, const int32_t* cu_kept,
+                                     int32_t batch, int64_t n_kept, int32_t max_kept, int32_t hq, int32_t hkv,
+                                     int32_t head_dim, void* o, float* lse, cudaStream_t stream) {
+  tg_status st = check_attention_shape(batch, n_kept, hq, hkv, head_dim, cu_kept);
+  if (st != TG_OK) return st;
+  if (max_kept < 0) return fail(TG_ERR_INVALID_ARG, "max_kept must be >= 0");
+  if (!(tau > 0.0f) || !std::isfinite(tau)) return fail(TG_ERR_INVALID_ARG, "tau must be positive and finite");
+  if (n_kept == 0 || max_kept == 0) return ok();
+  if (!q_rot || !k_rot || !v || !pos_kept || !s_kept || !gain || !o) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q_rot) || !aligned16(k_rot) || !aligned16(v) || !aligned16(o))
+    return fail(TG_ERR_INVALID_ARG, "q_rot, k_rot, v and o must be 16-byte aligned");
+  DeviceInfo* di = nullptr;
+  st = device_info(&di);
+  if (st != TG_OK) return st;
   CUtensorMap mq, mk, mv;
   const uint32_t box[3] = {64, 1, 128};
   {
@@ -322,9 +332,39 @@ tg_status tg_gated_attention_fwd(const void* q, const void* k, const void* v, co
   a.scale_log2 = static_cast<float>(1.4426950408889634 / (std::sqrt(static_cast<double>(head_dim)) * tau));
   a.bias_unit = static_cast<float>(std::sqrt(static_cast<double>(head_dim)) * tau);
   a.o = o; a.lse = lse; a.status = di->status; a.watchdog = g_watchdog_cycles;
-  e = launch_attention(mq, mk, mv, a, stream);
+  const cudaError_t e = launch_attention(mq, mk, mv, a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   return ok();
+}
+
+tg_status tg_gated_attention_fwd(const void* q, const void* k, const void* v, const int32_t* pos_kept,
+                                 const float* s_kept, const float* gain, float tau, float rope_theta,
+                                 const int32_t* cu_kept, int32_t batch, int64_t n_kept, int32_t max_kept,
+                                 int32_t hq, int32_t hkv, int32_t head_dim, void* o, float* lse,
+                                 void* k_cache, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+  tg_status st = check_attention_shape(batch, n_kept, hq, hkv, head_dim, cu_kept);
+  if (st != TG_OK) return st;
+  if (max_kept < 0) return fail(TG_ERR_INVALID_ARG, "max_kept must be >= 0");
+  if (!(tau > 0.0f) || !std::isfinite(tau)) return fail(TG_ERR_INVALID_ARG, "tau must be positive and finite");
+  if (!(rope_theta > 0.0f) || !std::isfinite(rope_theta)) return fail(TG_ERR_INVALID_ARG, "rope_theta must be positive");
+  if (n_kept == 0) return ok();
+  if (!q || !k || !v || !pos_kept || !s_kept || !gain || !o) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (k_cache && !aligned16(k_cache)))
+    return fail(TG_ERR_INVALID_ARG, "q, k, v, o and k_cache must be 16-byte aligned");
+  const size_t need = tg_attention_workspace_size(n_kept, hq, hkv, head_dim, k_cache ? 1 : 0);
+  if (!workspace || workspace_bytes < need)
+    return fail(TG_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(TG_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (max_kept == 0) return ok();
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* q_rot = ws;
+  void* k_rot = k_cache;
+  if (!k_rot) k_rot = ws + ((static_cast<size_t>(n_kept) * hq * head_dim * 2 + 255) & ~static_cast<size_t>(255));
+  st = tg_rope_qk(q, k, pos_kept, rope_theta, cu_kept, batch, n_kept, hq, hkv, head_dim, q_rot, k_rot, stream);
+  if (st != TG_OK) return st;
+  return tg_gated_attention_rotated(q_rot, k_rot, v, pos_kept, s_kept, gain, tau, cu_kept, batch, n_kept, max_kept,
+                                    hq, hkv, head_dim, o, lse, stream);
 }
 
 tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual, void* out, int64_t m, int32_t n,

@@ -42,6 +42,7 @@ constexpr int kCtrlRegs = 112;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kCtrlRegs <= kAttnThreads * kLaunchRegs, "register split");
 constexpr int kTileRows = 128;
 constexpr int kKvStages = 2;
+constexpr int kMetaSlots = 3;       // key-position slots (one more than the K/V stages)
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 // byte offset of row r's first 16-byte core-matrix row in a bias K step
@@ -60,12 +61,12 @@ struct AttnSmem {
   // 256 B apart): Q side per tile, K side per stage
   alignas(256) uint8_t qx[2][kTileRows * 32];
   alignas(256) uint8_t kx[kKvStages][kTileRows * 32];
-  int32_t kpos[kKvStages][kTileRows];
-  int32_t kmax[kKvStages];
+  int32_t kpos[kMetaSlots][kTileRows];
+  int32_t kmax[kMetaSlots];
   uint64_t q_full;
   uint64_t k_full[kKvStages];
   uint64_t v_full[kKvStages];
-  uint64_t meta_full[kKvStages];   // key positions of a stage written
+  uint64_t meta_full[kMetaSlots];  // key positions of a tile written
   uint64_t s_full[2][2];            // [tile][step parity]: S_t(j) in TMEM
   uint64_t p_full[2];
   uint64_t o_done[2];              // the last product into O_t done
@@ -125,7 +126,6 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     for (int s = 0; s < kKvStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.meta_full[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t][0], 1);
@@ -133,6 +133,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_done[t], 1);
     }
+    for (int s = 0; s < kMetaSlots; ++s) mbar_init(&sm.meta_full[s], 1);
     mbar_init(&sm.mma_final[0], 1);
     mbar_init(&sm.mma_final[1], 1);
     sm.abort = 0;
@@ -195,13 +196,14 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     };
     load_meta(0);
     int issued_k = 0, issued_v = 0;   // tiles whose K / V copies were issued
+    int prev_last = -1;               // position of the previous tile's last key
+    const bool check_pos = hu == 0 && row_end == seq_len;
     for (int j = 0; j < n_kv; ++j) {
       const int st = j & 1;
       // The MMAs of one thread complete in issue order, so S_1(m) done
       // implies every earlier product done.  K of tile j (and its bias
-      // columns) may replace tile j-2's once S_1(j-2) is done; V (and the key
-      // positions, which the softmax of tile j-2 reads) once PV_1(j-2) is,
-      // i.e. once S_1(j-1) is.
+      // columns) may replace tile j-2's once S_1(j-2) is done; V once
+      // PV_1(j-2) is, i.e. once S_1(j-1) is.
       // Each S_1 barrier completes every other step, and the MMAs cannot run
       // two of its phases ahead of this warp (S_1(j) needs the K copy issued
       // here), so a parity wait is unambiguous.
@@ -222,9 +224,25 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const uint32_t third = isinf(s) ? 0u : hi;
         *reinterpret_cast<uint4*>(sm.kx[st] + bias_row_offset(u * 32 + lane)) = make_uint4(hi | (lo << 16), third, 0u, 0u);
       }
+      // key positions for the softmax, in slot j % 3: the slot's last reader,
+      // the softmax of tile j-3, arrived before PV_1(j-3), which precedes
+      // S_1(j-2), so the slot is free here, a whole step before the K/V
+      // stage is
+      {
+        const int ms = j % kMetaSlots;
+        int kmax = INT_MIN;
+#pragma unroll
+        for (int u = 0; u < kTileRows / 32; ++u) {
+          sm.kpos[ms][u * 32 + lane] = pv[u];
+          kmax = max(kmax, pv[u]);
+        }
+        for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+        if (lane == 0) sm.kmax[ms] = kmax;
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
+        mbar_arrive(&sm.meta_full[j % kMetaSlots]);
         mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
         for (int bx = 0; bx < kBoxes; ++bx)
           tma_load_3d(sm.k[st] + bx * kBoxBytes, &map_k, &sm.k_full[st], bx * 64, kvh, krow);
@@ -239,16 +257,26 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || sm.abort) { sm.abort = 1; break; }
-      int kmax = INT_MIN;
+      // Positions must be non-negative and strictly increase inside the
+      // sequence (the causal tile skipping relies on it).  One CTA per
+      // sequence, the first head unit of the row block that reaches the
+      // sequence end (it reads every key), checks each key against the next
+      // one once its copies are out.
+      if (check_pos) {
+        bool bad = false;
 #pragma unroll
-      for (int u = 0; u < kTileRows / 32; ++u) {
-        sm.kpos[st][u * 32 + lane] = pv[u];
-        kmax = max(kmax, pv[u]);
+        for (int u = 0; u < kTileRows / 32; ++u) {
+          const int kr = j * kTileRows + u * 32 + lane;
+          const int down = __shfl_down_sync(0xffffffffu, pv[u], 1);
+          const int wrap = __shfl_sync(0xffffffffu, pv[u + 1 < kTileRows / 32 ? u + 1 : u], 0);
+          const bool has_next = kr + 1 < seq_len && (lane < 31 || u + 1 < kTileRows / 32);
+          const int nxt = lane < 31 ? down : wrap;
+          if (kr < seq_len && (pv[u] < 0 || (has_next && nxt <= pv[u]))) bad = true;
+        }
+        if (lane == 0 && j > 0 && j * kTileRows < seq_len && pv[0] <= prev_last) bad = true;
+        if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(a.status, kStatusIndex);
+        prev_last = __shfl_sync(0xffffffffu, pv[kTileRows / 32 - 1], 31);
       }
-      for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-      if (lane == 0) sm.kmax[st] = kmax;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.meta_full[st]);
       load_meta(j + 1);
     }
     if (lane == 0) {
@@ -363,7 +391,8 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     for (int j = 0; j < n_kv; ++j) {
       const int st = j & 1;
       const uint32_t use = j >> 1;
-      bool w = mbar_wait(&sm.meta_full[st], use & 1u, wd, a.status, kStatusTimeout);
+      const int ms = j % kMetaSlots;
+      bool w = mbar_wait(&sm.meta_full[ms], static_cast<uint32_t>(j / kMetaSlots) & 1u, wd, a.status, kStatusTimeout);
       w = w && mbar_wait(&sm.s_full[t][st], use & 1u, wd, a.status, kStatusTimeout);
       ok = __all_sync(0xffffffffu, w) && !sm.abort;
       if (!ok) break;
@@ -375,8 +404,8 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 #pragma unroll
       for (int c = 0; c < kTileRows / 32; ++c)
         tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[c * 32]));
-      const bool masked = __any_sync(0xffffffffu, sm.kmax[st] > qpos);
-      const int* kp = sm.kpos[st];
+      const bool masked = __any_sync(0xffffffffu, sm.kmax[ms] > qpos);
+      const int* kp = sm.kpos[ms];
       tmem_ld_wait();
       float2 x[kTileRows / 2];
 #pragma unroll

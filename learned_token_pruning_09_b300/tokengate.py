@@ -53,6 +53,9 @@ _SIGS = {
     "tg_gather_kept": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp],
     "tg_gated_attention_fwd": [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _i32, _i64, _i32, _i32, _i32,
                                _i32, _vp, _vp, _vp, _vp, _sz, _vp],
+    "tg_rope_qk": [_vp, _vp, _vp, _f32, _vp, _i32, _i64, _i32, _i32, _i32, _vp, _vp, _vp],
+    "tg_gated_attention_rotated": [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
+                                   _vp, _vp, _vp],
     "tg_attention_workspace_size": [_i64, _i32, _i32, _i32, _i32],
     "tg_linear_bf16": [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp],
     "tg_check_device_status": [_vp],
@@ -184,6 +187,53 @@ def tg_gather_kept(x: Optional[torch.Tensor], s: Optional[torch.Tensor], cu_seql
 
 def tg_attention_workspace_size(n_kept: int, hq: int, hkv: int, head_dim: int, has_k_cache: bool) -> int:
     return int(lib.tg_attention_workspace_size(int(n_kept), hq, hkv, head_dim, 1 if has_k_cache else 0))
+
+
+def tg_rope_qk(q: torch.Tensor, k: torch.Tensor, pos_kept: torch.Tensor, rope_theta: float, cu_kept: torch.Tensor,
+               q_out: Optional[torch.Tensor] = None, k_out: Optional[torch.Tensor] = None, stream=None):
+    """(q', k'): q [T, hq, D] and k [T, hkv, D] bf16 rotated by RoPE at pos_kept."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k, torch.bfloat16, "k", 3)
+    _need(pos_kept, torch.int32, "pos_kept", 1)
+    _need(cu_kept, torch.int32, "cu_kept", 1)
+    t, hq, dh = q.shape
+    hkv = k.shape[1]
+    if k.shape != (t, hkv, dh):
+        raise ValueError("k must be [T, hkv, D] matching q")
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    k_out = torch.empty_like(k) if k_out is None else k_out
+    _need(q_out, torch.bfloat16, "q_out", 3)
+    _need(k_out, torch.bfloat16, "k_out", 3)
+    _check(lib.tg_rope_qk(_ptr(q), _ptr(k), _ptr(pos_kept), float(rope_theta), _ptr(cu_kept), cu_kept.shape[0] - 1,
+                          t, hq, hkv, dh, _ptr(q_out), _ptr(k_out), _stream(stream)), "tg_rope_qk")
+    return q_out, k_out
+
+
+def tg_gated_attention_rotated(q_rot: torch.Tensor, k_rot: torch.Tensor, v: torch.Tensor, pos_kept: torch.Tensor,
+                               s_kept: torch.Tensor, gain: torch.Tensor, tau: float, cu_kept: torch.Tensor,
+                               max_kept: int, o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                               want_lse: bool = False, stream=None):
+    """o [T, hq, D] bf16 (and lse [hq, T] fp32) from q', k' already rotated by tg_rope_qk."""
+    _need(q_rot, torch.bfloat16, "q_rot", 3)
+    _need(k_rot, torch.bfloat16, "k_rot", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    _need(pos_kept, torch.int32, "pos_kept", 1)
+    _need(s_kept, torch.float32, "s_kept", 1)
+    _need(gain, torch.float32, "gain", 1)
+    _need(cu_kept, torch.int32, "cu_kept", 1)
+    t, hq, dh = q_rot.shape
+    hkv = k_rot.shape[1]
+    if k_rot.shape != (t, hkv, dh) or v.shape != (t, hkv, dh):
+        raise ValueError("k_rot and v must be [T, hkv, D] matching q_rot")
+    if o is None:
+        o = torch.empty_like(q_rot)
+    if lse is None and want_lse:
+        lse = torch.empty((hq, t), dtype=torch.float32, device=q_rot.device)
+    _check(lib.tg_gated_attention_rotated(_ptr(q_rot), _ptr(k_rot), _ptr(v), _ptr(pos_kept), _ptr(s_kept),
+                                          _ptr(gain), float(tau), _ptr(cu_kept), cu_kept.shape[0] - 1, t,
+                                          int(max_kept), hq, hkv, dh, _ptr(o), _ptr(lse), _stream(stream)),
+           "tg_gated_attention_rotated")
+    return (o, lse) if lse is not None else o
 
 
 def tg_gated_attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pos_kept: torch.Tensor,

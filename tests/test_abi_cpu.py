@@ -100,6 +100,20 @@ def test_host_validation_rejects_before_launch(tg):
     assert attn(q=_c(264)) == tg.TG_ERR_INVALID_ARG         # not 16-byte aligned
     assert attn(b=0) == tg.TG_ERR_INVALID_ARG
     assert attn(t=0) == tg.TG_OK                            # nothing to do
+    # the two steps of the fused call
+    assert L.tg_rope_qk(p, p, p, 1e6, p, 1, 100, 16, 8, 96, p, _c(512), None) == tg.TG_ERR_UNSUPPORTED
+    assert L.tg_rope_qk(p, p, p, 0.0, p, 1, 100, 16, 8, 128, p, _c(512), None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_rope_qk(p, p, p, 1e6, p, 1, 100, 16, 8, 128, p, p, None) == tg.TG_ERR_INVALID_ARG  # k_out aliases k
+    assert L.tg_rope_qk(p, p, p, 1e6, None, 1, 100, 16, 8, 128, _c(512), _c(768), None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_rope_qk(p, p, p, 1e6, p, 1, 0, 16, 8, 128, _c(512), _c(768), None) == tg.TG_OK
+    rot = lambda **kw: L.tg_gated_attention_rotated(
+        *(lambda a: (a["q"], a["k"], a["v"], a["pos"], a["s"], a["g"], a["tau"], a["cu"], a["b"], a["t"], a["mk"],
+                     a["hq"], a["hkv"], a["d"], a["o"], a["lse"], None))(dict(args, **kw)))
+    assert rot(hq=12, hkv=8) == tg.TG_ERR_INVALID_ARG
+    assert rot(tau=-1.0) == tg.TG_ERR_INVALID_ARG
+    assert rot(v=None) == tg.TG_ERR_INVALID_ARG
+    assert rot(k=_c(264)) == tg.TG_ERR_INVALID_ARG
+    assert rot(mk=0) == tg.TG_OK
     # linear
     assert L.tg_linear_bf16(p, p, None, p, 10, 24, 64, None) == tg.TG_ERR_INVALID_ARG
     assert L.tg_linear_bf16(p, p, None, p, 10, 32, 96, None) == tg.TG_ERR_INVALID_ARG

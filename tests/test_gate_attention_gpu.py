@@ -204,6 +204,68 @@ def test_attention_rejects_unsorted_positions(tg):
     assert tg.tg_check_device_status() == tg.TG_ERR_DEVICE_INDEX
 
 
+def _random_attention(rng, lens, hq, hkv, d):
+    t = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    pos = np.concatenate([np.sort(rng.choice(4 * n + 10, n, replace=False)) for n in lens]).astype(np.int32)
+    s_kept = -np.abs(rng.normal(0, 2, t)).astype(np.float32)
+    bf = lambda a: synth.f32_to_bf16_bits(a.astype(np.float32))
+    ai = {"q": bf(rng.standard_normal((t, hq, d))), "k": bf(rng.standard_normal((t, hkv, d))),
+          "v": bf(rng.standard_normal((t, hkv, d))), "gain": rng.uniform(0.5, 2, hq).astype(np.float32),
+          "tau": 0.93}
+    return ai, pos, s_kept, cu
+
+
+@pytest.mark.parametrize("hq,hkv,d,lens", [(8, 2, 128, [127, 128, 129]), (3, 1, 64, [300, 5, 257]),
+                                           (16, 8, 128, [1000])])
+def test_rope_then_rotated_equals_fused_call(tg, hq, hkv, d, lens):
+    """tg_rope_qk followed by tg_gated_attention_rotated is the fused call,
+    bit for bit, and its k' is the fused call's K cache."""
+    ai, pos, s_kept, cu = _random_attention(np.random.default_rng(hq + d + len(lens)), lens, hq, hkv, d)
+    q, k, v = dev_bf16(ai["q"]), dev_bf16(ai["k"]), dev_bf16(ai["v"])
+    pos_d, s_d, g_d, cu_d = dev_i32(pos), dev_f32(s_kept), dev_f32(ai["gain"]), dev_i32(cu)
+    mk = int(max(lens))
+    kc = torch.empty_like(k)
+    o1, l1 = tg.tg_gated_attention_fwd(q, k, v, pos_d, s_d, g_d, ai["tau"], 1e6, cu_d, mk, want_lse=True, k_cache=kc)
+    q2, k2 = tg.tg_rope_qk(q, k, pos_d, 1e6, cu_d)
+    o2, l2 = tg.tg_gated_attention_rotated(q2, k2, v, pos_d, s_d, g_d, ai["tau"], cu_d, mk, want_lse=True)
+    assert tg.tg_check_device_status() == tg.TG_OK
+    assert np.array_equal(host_bits(o1), host_bits(o2))
+    assert torch.equal(l1.cpu(), l2.cpu())
+    assert np.array_equal(host_bits(kc), host_bits(k2))
+    # q' and k' are the oracle's rotation at the original positions, rounded once to bf16
+    for got, src in ((q2, ai["q"]), (k2, ai["k"])):
+        ref = oracle.rope(oracle.bf16_decode(src), pos)
+        assert np.all(np.abs(host_f64(got) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
+@pytest.mark.parametrize("case", ["swap_inside_tile", "swap_across_tiles", "negative"])
+def test_rotated_attention_flags_bad_positions(tg, case):
+    """Without the RoPE prologue's check, the attention kernel itself flags
+    positions that do not strictly increase (its causal tile skipping relies
+    on them)."""
+    rng = np.random.default_rng(7)
+    t, hq, hkv, d = 300, 2, 1, 64
+    pos = np.arange(t, dtype=np.int32) * 2
+    if case == "swap_inside_tile":
+        pos[10], pos[11] = pos[11], pos[10]
+    elif case == "swap_across_tiles":
+        pos[127], pos[128] = pos[128], pos[127]
+    else:
+        pos[0] = -5
+    bf = lambda a: synth.f32_to_bf16_bits(a.astype(np.float32))
+    q, k, v = (dev_bf16(bf(rng.standard_normal(s))) for s in ((t, hq, d), (t, hkv, d), (t, hkv, d)))
+    tg.tg_check_device_status()
+    tg.tg_gated_attention_rotated(q, k, v, dev_i32(pos), dev_f32(np.zeros(t)), dev_f32(np.ones(hq)), 1.0,
+                                  dev_i32([0, t]), t)
+    assert tg.tg_check_device_status() == tg.TG_ERR_DEVICE_INDEX
+    # well-formed positions leave the status clean
+    good = np.arange(t, dtype=np.int32) * 2
+    tg.tg_gated_attention_rotated(q, k, v, dev_i32(good), dev_f32(np.zeros(t)), dev_f32(np.ones(hq)), 1.0,
+                                  dev_i32([0, t]), t)
+    assert tg.tg_check_device_status() == tg.TG_OK
+
+
 # ---------------------------------------------------------------------------
 # projections and the stacked layer
 # ---------------------------------------------------------------------------
