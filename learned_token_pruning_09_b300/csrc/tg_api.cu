@@ -287,8 +287,11 @@ tg_status tg_rope_qk(const void* q, const void* k, const int32_t* pos_kept, floa
   st = device_info(&di);
   if (st != TG_OK) return st;
   RopeFreqs f{};
-  for (int i = 0; i < head_dim / 2; ++i)
-    f.inv_freq[i] = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim);
+  for (int i = 0; i < head_dim / 2; ++i) {
+    const double t = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim) / (2.0 * 3.141592653589793);
+    f.turns_hi[i] = static_cast<float>(t);
+    f.turns_lo[i] = static_cast<float>(t - static_cast<double>(f.turns_hi[i]));
+  }
   RopeArgs ra{};
   ra.q = q; ra.k = k; ra.pos = pos_kept; ra.cu_kept = cu_kept; ra.batch = batch; ra.n_kept = n_kept;
   ra.hq = hq; ra.hkv = hkv; ra.head_dim = head_dim; ra.q_out = q_out; ra.k_out = k_out;

@@ -17,7 +17,9 @@ constexpr unsigned int kStatusIndex = 6;
 constexpr int kMaxHeadDimHalf = 64;
 
 struct RopeFreqs {
-  double inv_freq[kMaxHeadDimHalf];   // theta^(-2i/D), i < D/2
+  // theta^(-2i/D) / (2 pi), i < D/2, in turns per position, as hi + lo fp32
+  float turns_hi[kMaxHeadDimHalf];
+  float turns_lo[kMaxHeadDimHalf];
 };
 
 // ---- gate ------------------------------------------------------------------

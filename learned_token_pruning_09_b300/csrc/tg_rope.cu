@@ -1,41 +1,113 @@
 // RoPE prologue of token-gated attention: rotates q and k by rotate-half
 // RoPE at the ORIGINAL positions of the kept tokens (base theta, 1e6 for
-// Qwen3) and writes them as bf16: q' into the workspace, k' into the
-// kept-only KV cache.  Also checks that positions strictly increase inside
-// each sequence, which the attention kernel's causal tile skipping relies on.
+// Qwen3) and writes them as bf16.  Also checks that positions strictly
+// increase inside each sequence, which the attention kernel's causal tile
+// skipping relies on.
 //
-// Angles: a = pos * theta^(-2i/D) can reach 1.3e5 rad at 128k context, where
-// an fp32 angle would be off by ~1e-2 rad.  The product and its reduction to
-// [-pi, pi] are done in fp64 (inverse frequencies precomputed on the host in
-// fp64), then sin/cos in fp32 of the reduced angle.
+// Angles: a = pos * theta^(-2i/D) reaches 1.3e5 rad at 128k context, where a
+// plain fp32 product would be off by ~1e-2 rad.  The angle is formed in turns,
+// pos * t with t = theta^(-2i/D) / (2 pi) held as an unevaluated sum of two
+// fp32 numbers (t_hi + t_lo, split on the host in fp64).  The position is
+// split as p1 + p2 (p1 a multiple of 4096, p2 < 4096), both exact in fp32 for
+// any int32; each p_k * t_hi is taken exactly as a rounded product plus its
+// FMA-recovered error (Dekker's two-product), its integer part is dropped
+// exactly, and the small terms are added back.  The fractional turn is good
+// to ~1e-7 of a turn for positions below 2^24 (~2e-6 at 2^31), and its sine
+// and cosine come from sincospif.  No fp64 arithmetic on the device.
+//
+// One warp per token (grid-stride), no block-wide synchronisation: every lane
+// of the warp handles the same 8-element column v of several heads (the
+// token's vector pairs are dealt round-robin and 32 is a multiple of the
+// column count), so each lane needs the 8 frequencies of column v.  The
+// lanes of a column compute one share of them each and exchange them by
+// shuffles; every load of a lane is issued before the angle math.
 #include "tg_common.cuh"
 
 namespace tg {
 
-constexpr int kRopeThreads = 128;
+constexpr int kRopeThreads = 256;
+constexpr int kRopeChunk = 4;     // vector pairs per lane per pass
 
+template <int kD>
 __global__ void __launch_bounds__(kRopeThreads)
 rope_kernel(RopeArgs a, RopeFreqs f) {
-  __shared__ float cs[kMaxHeadDimHalf];
-  __shared__ float sn[kMaxHeadDimHalf];
-  const int D = a.head_dim;
-  const int half = D >> 1;
-  const int vph = half >> 3;                    // 8-element vectors per half-head
-  const int nqv = a.hq * vph;
-  const int ntot = nqv + a.hkv * vph;
-  const double kTwoPi = 6.283185307179586;
-  const double kInvTwoPi = 0.15915494309189535;
-  for (long long t = blockIdx.x; t < a.n_kept; t += gridDim.x) {
+  constexpr int kHalf = kD / 2;
+  constexpr int kVph = kHalf / 8;              // 8-element columns per half-head
+  constexpr int kShare = 8 * kVph / 32;        // frequencies each lane computes
+  __shared__ float th_s[kHalf], tl_s[kHalf];
+  for (int i = threadIdx.x; i < kHalf; i += kRopeThreads) { th_s[i] = f.turns_hi[i]; tl_s[i] = f.turns_lo[i]; }
+  __syncthreads();
+  const int lane = lane_id();
+  const int v = lane % kVph;                   // this lane's column, the same in all its pairs
+  const int grp = lane / kVph;
+  const int nqv = a.hq * kVph;
+  const int per_tok = nqv + a.hkv * kVph;
+  const long long wg = static_cast<long long>(blockIdx.x) * (kRopeThreads / 32) + warp_id();
+  const long long nwarps = static_cast<long long>(gridDim.x) * (kRopeThreads / 32);
+  for (long long t = wg; t < a.n_kept; t += nwarps) {
     const int p = __ldg(a.pos + t);
-    if (threadIdx.x < half) {
-      const double ang = static_cast<double>(p) * f.inv_freq[threadIdx.x];
-      const double r = fma(-rint(ang * kInvTwoPi), kTwoPi, ang);
-      float sv, cv;
-      sincosf(static_cast<float>(r), &sv, &cv);
-      cs[threadIdx.x] = cv;
-      sn[threadIdx.x] = sv;
+    for (int c0 = 0; c0 < per_tok; c0 += 32 * kRopeChunk) {
+      uint4 lo4[kRopeChunk], hi4[kRopeChunk];
+#pragma unroll
+      for (int u = 0; u < kRopeChunk; ++u) {
+        const int r = c0 + u * 32 + lane;
+        if (r < per_tok) {
+          const bool isq = r < nqv;
+          const int head = (isq ? r : r - nqv) / kVph;
+          const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(isq ? a.q : a.k) +
+                                                            (t * (isq ? a.hq : a.hkv) + head) * kD);
+          lo4[u] = __ldg(src + v);
+          hi4[u] = __ldg(src + kVph + v);
+        }
+      }
+      // cos and sin of the column's 8 frequencies: this lane's share, then
+      // the rest from the lanes of the same column
+      float cc[kShare], ss[kShare];
+#pragma unroll
+      for (int q = 0; q < kShare; ++q) {
+        const int i = v * 8 + grp * kShare + q;
+        const float th = th_s[i];
+        const float p1 = static_cast<float>(p & ~4095);     // exact: at most 19 significant bits
+        const float p2 = static_cast<float>(p & 4095);
+        const float x1 = p1 * th, x2 = p2 * th;
+        const float e = fmaf(p1, th, -x1) + fmaf(p2, th, -x2);   // the products' rounding errors, exactly
+        const float frac = ((x1 - rintf(x1)) + (x2 - rintf(x2))) + fmaf(static_cast<float>(p), tl_s[i], e);
+        sincospif(2.0f * frac, &ss[q], &cc[q]);
+      }
+      float cs[8], sn[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int src_lane = v + kVph * (e / kShare);
+        cs[e] = __shfl_sync(0xffffffffu, cc[e % kShare], src_lane);
+        sn[e] = __shfl_sync(0xffffffffu, ss[e % kShare], src_lane);
+      }
+#pragma unroll
+      for (int u = 0; u < kRopeChunk; ++u) {
+        const int r = c0 + u * 32 + lane;
+        if (r < per_tok) {
+          const bool isq = r < nqv;
+          const int head = (isq ? r : r - nqv) / kVph;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(isq ? a.q_out : a.k_out) +
+                                                (t * (isq ? a.hq : a.hkv) + head) * kD);
+          const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&lo4[u]);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hi4[u]);
+          uint4 olo, ohi;
+          uint32_t* ol = reinterpret_cast<uint32_t*>(&olo);
+          uint32_t* oh = reinterpret_cast<uint32_t*>(&ohi);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 xl = __bfloat1622float2(l2[e]);
+            const float2 xh = __bfloat1622float2(h2[e]);
+            const float c0f = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
+            ol[e] = pack_bf16x2(xl.x * c0f - xh.x * s0, xl.y * c1 - xh.y * s1);
+            oh[e] = pack_bf16x2(xh.x * c0f + xl.x * s0, xh.y * c1 + xl.y * s1);
+          }
+          dst[v] = olo;
+          dst[kVph + v] = ohi;
+        }
+      }
     }
-    if (threadIdx.x == 0) {
+    if (lane == 0) {
       // positions: non-negative and strictly increasing within a sequence
       int lo = 0, hi = a.batch;
       while (lo < hi) {
@@ -45,45 +117,16 @@ rope_kernel(RopeArgs a, RopeFreqs f) {
       const bool first = static_cast<long long>(__ldg(a.cu_kept + lo)) == t;
       if (p < 0 || (!first && __ldg(a.pos + t - 1) >= p)) record_error(a.status, kStatusIndex);
     }
-    __syncthreads();
-    for (int w = threadIdx.x; w < ntot; w += kRopeThreads) {
-      const bool isq = w < nqv;
-      const int ww = isq ? w : w - nqv;
-      const int head = ww / vph;
-      const int v = ww - head * vph;
-      const int nh = isq ? a.hq : a.hkv;
-      const size_t row = (static_cast<size_t>(t) * nh + head) * D;
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(isq ? a.q : a.k) + row);
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(isq ? a.q_out : a.k_out) + row);
-      const uint4 lo4 = __ldg(src + v);
-      const uint4 hi4 = __ldg(src + vph + v);
-      const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&lo4);
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hi4);
-      uint4 olo, ohi;
-      uint32_t* ol = reinterpret_cast<uint32_t*>(&olo);
-      uint32_t* oh = reinterpret_cast<uint32_t*>(&ohi);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 xl = __bfloat1622float2(l2[e]);
-        const float2 xh = __bfloat1622float2(h2[e]);
-        const int i0 = v * 8 + 2 * e;
-        const float c0 = cs[i0], s0 = sn[i0], c1 = cs[i0 + 1], s1 = sn[i0 + 1];
-        ol[e] = pack_bf16x2(xl.x * c0 - xh.x * s0, xl.y * c1 - xh.y * s1);
-        oh[e] = pack_bf16x2(xh.x * c0 + xl.x * s0, xh.y * c1 + xl.y * s1);
-      }
-      dst[v] = olo;
-      dst[vph + v] = ohi;
-    }
-    __syncthreads();
   }
 }
 
 cudaError_t launch_rope(const RopeArgs& a, const RopeFreqs& f, cudaStream_t st) {
   if (a.n_kept == 0) return cudaSuccess;
-  long long blocks = a.n_kept;
-  const long long cap = static_cast<long long>(a.num_sms) * 16;
+  long long blocks = (a.n_kept + kRopeThreads / 32 - 1) / (kRopeThreads / 32);
+  const long long cap = static_cast<long long>(a.num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  rope_kernel<<<static_cast<unsigned>(blocks), kRopeThreads, 0, st>>>(a, f);
+  if (a.head_dim == 128) rope_kernel<128><<<static_cast<unsigned>(blocks), kRopeThreads, 0, st>>>(a, f);
+  else rope_kernel<64><<<static_cast<unsigned>(blocks), kRopeThreads, 0, st>>>(a, f);
   return cudaGetLastError();
 }
 
