@@ -382,48 +382,44 @@ def run_gpu(args, shape):
     torch.cuda.synchronize()
     if tg.tg_check_device_status() != tg.TG_OK:
         raise RuntimeError("device status after warm-up: " + tg.lib.tg_last_error_string().decode())
-    graphs = []
-    for name, f in segs:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+    # The whole step is one CUDA graph, with timing events recorded inside it
+    # between the segments, so that no launch gap sits between two kernels.
+    nseg = len(segs)
+    names = [n for n, _ in segs]
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nseg + 1)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for k, (_, f) in enumerate(segs):
+            evs[k].record()
             f()
-        graphs.append((name, g))
+        evs[-1].record()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        for k, (_, g) in enumerate(graphs):
-            if ev is not None:
-                ev[k].record(stream)
-            g.replay()
-        if ev is not None:
-            ev[-1].record(stream)
-
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
-        step()
+        graph.replay()
     torch.cuda.synchronize()
 
-    nseg = len(graphs)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    per = []
     for i in range(args.steps):
         flush.zero_()
-        step(evs[i])
-    torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()     # the events are re-recorded by the next replay
+        per.append([evs[k].elapsed_time(evs[k + 1]) for k in range(nseg)])
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
     if tg.tg_check_device_status() != tg.TG_OK:
         raise RuntimeError("device status after timed steps: " + tg.lib.tg_last_error_string().decode())
 
-    per = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(nseg)] for i in range(args.steps)])
-    names = [n for n, _ in graphs]
+    per = np.array(per)
     seg_ms = dict(zip(names, per.mean(axis=0)))
     step_ms = float(per.sum(axis=1).mean())
     # the token-gated attention layer: its RoPE prologue and the attention kernel
