@@ -126,7 +126,6 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
 // 128 rows, one thread per row.
 constexpr int kGateThreads = 256;
 constexpr int kGateMaxStages = 8;
-constexpr int kGateSmemBudget = 200 * 1024;
 constexpr uint32_t kGateXBytes = kBM * kBK * 2;     // 16 KB: 128 rows of one K block
 
 struct GateSmemHead {
@@ -138,6 +137,15 @@ struct GateSmemHead {
   uint32_t tmem_base;
   uint32_t peer_issued;                 // leader: stages the other CTA issued
   volatile int abort;
+};
+
+// Placed after the stage ring in dynamic shared memory (the kernel has no
+// static shared memory, so the ring starts at the 1024-byte aligned base and
+// needs no alignment slack: one more stage fits).
+struct GateSmemTail {
+  GateSmemHead head;
+  alignas(16) float b1[256];
+  alignas(16) float w2[256];
 };
 
 __device__ __forceinline__ bool row_is_doc(const GateArgs& a, long long row) {
@@ -160,11 +168,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
 gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w1,
             GateArgs a, int n_st) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ GateSmemHead head;
-  __shared__ __align__(16) float sb1[256];
-  __shared__ __align__(16) float sw2[256];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int warp = warp_id();
+  uint8_t* ring = smem_raw;
   const int lane = lane_id();
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
@@ -172,7 +176,17 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   const uint32_t ncols = 2 * half_cols;
   const int hb = a.h / 2;                          // W1 rows staged by each CTA
   const uint32_t stage_bytes = kGateXBytes + static_cast<uint32_t>(hb) * kBK * 2;
-  const long long n_blocks = (a.n_rows + 2 * kBM - 1) / (2 * kBM);   // 256-row blocks
+  GateSmemTail& tail = *reinterpret_cast<GateSmemTail*>(smem_raw + static_cast<size_t>(n_st) * stage_bytes);
+  GateSmemHead& head = tail.head;
+  float* sb1 = tail.b1;
+  float* sw2 = tail.w2;
+  // 128-byte swizzled TMA and MMA tiles need a 1024-byte aligned ring; both
+  // CTAs of a pair see the same base, so both leave here together
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(a.status, kStatusIndex);
+    return;
+  }
+  const int warp = warp_id();  const long long n_blocks = (a.n_rows + 2 * kBM - 1) / (2 * kBM);   // 256-row blocks
   const int n_pairs = static_cast<int>(gridDim.x >> 1);
   const int q = static_cast<int>(blockIdx.x >> 1);
   const int n_pass = (q < n_blocks) ? static_cast<int>((n_blocks - q + n_pairs - 1) / n_pairs) : 0;
@@ -343,11 +357,16 @@ cudaError_t launch_gate(const CUtensorMap& map_x, const CUtensorMap& map_w1, con
                         cudaStream_t st) {
   if (a.n_rows == 0) return cudaSuccess;
   const size_t stage_bytes = kGateXBytes + static_cast<size_t>(a.h / 2) * kBK * 2;
-  int n_st = static_cast<int>(kGateSmemBudget / stage_bytes);
+  int dev = 0, max_smem = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  int n_st = static_cast<int>((static_cast<size_t>(max_smem) - sizeof(GateSmemTail)) / stage_bytes);
   if (n_st > kGateMaxStages) n_st = kGateMaxStages;
-  const size_t smem = 1024 + static_cast<size_t>(n_st) * stage_bytes;
-  cudaError_t e = cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  if (n_st < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = static_cast<size_t>(n_st) * stage_bytes + sizeof(GateSmemTail);
+  e = cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long blocks = (a.n_rows + 2 * kBM - 1) / (2 * kBM);
   cudaLaunchConfig_t cfg = {};
