@@ -382,7 +382,7 @@ tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual,
   DeviceInfo* di = nullptr;
   tg_status st = device_info(&di);
   if (st != TG_OK) return st;
-  const int bn = n >= 256 ? 256 : n;
+  const int bn = linear_tile_n(n);
   CUtensorMap ma, mw;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(kdim), static_cast<uint64_t>(m)};
@@ -393,12 +393,13 @@ tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual,
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(kdim), static_cast<uint64_t>(n)};
     const uint64_t str[1] = {static_cast<uint64_t>(kdim) * 2};
-    const uint32_t box[2] = {64, static_cast<uint32_t>(bn)};
+    // each CTA of a pair stages one half of a tile's W rows
+    const uint32_t box[2] = {64, static_cast<uint32_t>(bn / 2)};
     if ((st = make_map(&mw, w, 2, dims, str, box, "w")) != TG_OK) return st;
   }
   LinearArgs la{};
   la.residual = residual; la.out = out; la.m = m; la.n = n; la.kdim = kdim;
-  la.status = di->status; la.watchdog = g_watchdog_cycles;
+  la.status = di->status; la.watchdog = g_watchdog_cycles; la.num_sms = di->num_sms;
   cudaError_t e = launch_linear(ma, mw, la, stream);
   if (e != cudaSuccess) return cuda_fail(e, "linear kernel launch");
   return ok();

@@ -1,5 +1,6 @@
 // Tensor-core GEMMs on tcgen05 with TMEM accumulators and TMA-fed shared
-// memory stages:
+// memory stages, both run by CTA pairs (clusters of two CTAs on two SMs whose
+// tensor cores execute one M=256 MMA together, cta_group::2):
 //
 //  * gate_kernel  -- TokenGate's gate MLP scorer (gate module: "an MLP scores
 //    every token from its post-attention residual at layer L").  A pair of
@@ -8,96 +9,24 @@
 //    exact-erf GELU, the 1-wide projection with w2, + b2 and logsigmoid,
 //    writing one fp32 score per row (0 for question rows).
 //  * linear_kernel -- out = A W^T (+ residual) in bf16, the per-layer Q/K/V and
-//    output projections of the stacked long-context workload.
+//    output projections of the stacked long-context workload, 256 x 256 tiles.
 //
-// linear_kernel's warp roles (192 threads): warp 0 issues TMA loads, warp 1 allocates TMEM
-// and issues the MMAs (one elected lane), warps 2..5 run the epilogue, one
-// thread per accumulator row (warp w reads TMEM lanes 32*(w%4)..+31).
+// The shared scheme: each CTA stages its own 128 rows of the A operand and one
+// half of the B operand's rows (the pair splits B), so the shared-memory
+// traffic per SM is that of an M=128, N=128 MMA while the tensor cores run
+// M=256, N=256; every copy of either CTA completes on the leader's (rank 0)
+// stage barrier; the leader's MMA commits are multicast to both CTAs; the
+// accumulators are double-buffered in TMEM so that the epilogue of one tile
+// overlaps the MMAs of the next.
 #include "tg_common.cuh"
 
 namespace tg {
 
-constexpr int kGemmThreads = 192;
-constexpr int kBM = 128;
+constexpr int kBM = 128;                   // rows of A per CTA
 constexpr int kBK = 64;                    // one 128-byte swizzle row of bf16
-constexpr int kATileBytes = kBM * kBK * 2; // 16 KB
-
-struct GemmSmemHead {
-  uint64_t full[8];
-  uint64_t empty[8];
-  uint64_t acc_full;
-  uint32_t tmem_base;
-  volatile int abort;
-};
-
-// Shared by both kernels: TMA producer + MMA issuer over the K dimension.
-// A rows [m0, m0+128), B rows [n0, n0+bn), K = kdim.  Accumulates into TMEM
-// columns [0, bn).  Returns (in every thread) after the roles are done with
-// the mainloop; epilogue threads then wait on head->acc_full.
-template <int kStages>
-__device__ __forceinline__ void gemm_mainloop(const CUtensorMap* map_a, const CUtensorMap* map_b,
-                                              GemmSmemHead* head, uint8_t* stages, int bn,
-                                              int m0, int n0, int kdim, unsigned int* status,
-                                              long long watchdog) {
-  const int warp = warp_id();
-  const int lane = lane_id();
-  const int nk = kdim / kBK;
-  const uint32_t b_bytes = static_cast<uint32_t>(bn) * kBK * 2;
-  const uint32_t stage_bytes = kATileBytes + b_bytes;
-  if (warp == 0 && lane == 0) {
-    int issued = 0;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int st = kb % kStages;
-      const uint32_t use = kb / kStages;
-      if (!mbar_wait(&head->empty[st], (use & 1u) ^ 1u, watchdog, status, kStatusTimeout)) {
-        head->abort = 1;
-        break;
-      }
-      if (head->abort) break;
-      uint8_t* sa = stages + st * stage_bytes;
-      mbar_arrive_expect_tx(&head->full[st], stage_bytes);
-      tma_load_2d(sa, map_a, &head->full[st], kb * kBK, m0);
-      tma_load_2d(sa + kATileBytes, map_b, &head->full[st], kb * kBK, n0);
-      issued = kb + 1;
-    }
-    // wait for the last loads of every stage to land before anyone may leave
-    for (int st = 0; st < kStages && st < issued; ++st) {
-      const int last = ((issued - 1 - st) / kStages) * kStages + st;
-      mbar_wait(&head->full[st], (static_cast<uint32_t>(last / kStages)) & 1u, kDrainCycles, status, kStatusTimeout);
-    }
-  } else if (warp == 1 && lane == 0) {
-    const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(bn), 0, 0);
-    const uint32_t d_tmem = head->tmem_base;
-    bool ok = true;
-    for (int kb = 0; kb < nk && ok; ++kb) {
-      const int st = kb % kStages;
-      const uint32_t use = kb / kStages;
-      if (!mbar_wait(&head->full[st], use & 1u, watchdog, status, kStatusTimeout) || head->abort) {
-        head->abort = 1;
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t sa = smem_u32(stages + st * stage_bytes);
-      const uint32_t sb = sa + kATileBytes;
-#pragma unroll
-      for (int ks = 0; ks < kBK / 16; ++ks) {
-        const uint64_t da = smem_desc_sw128(sa + ks * 32, 16, 1024);
-        const uint64_t db = smem_desc_sw128(sb + ks * 32, 16, 1024);
-        mma_ss(d_tmem, da, db, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
-      }
-      mma_commit(&head->empty[st]);
-    }
-    mma_commit(&head->acc_full);
-    // every MMA must have finished before TMEM may be freed
-    mbar_wait(&head->acc_full, 0, kDrainCycles, status, kStatusTimeout);
-  }
-}
-
-template <int kStages>
-__device__ __forceinline__ size_t gemm_smem_bytes(int bn) {
-  return 1024 + static_cast<size_t>(kStages) * (kATileBytes + bn * kBK * 2);
-}
+constexpr uint32_t kPairABytes = kBM * kBK * 2;   // 16 KB: 128 rows of one K block
+constexpr int kPairThreads = 256;
+constexpr int kPairMaxStages = 8;
 
 __host__ __device__ inline uint32_t tmem_cols_for(int n) {
   uint32_t c = 32;
@@ -105,32 +34,12 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
   return c;
 }
 
-// ---------------------------------------------------------------------------
-// gate
-// ---------------------------------------------------------------------------
-// CTA pairs (clusters of two CTAs, one per SM): the two tensor cores of a pair
-// compute U = X W1^T for 256 residual rows at a time with M=256 pair MMAs.
-// Each CTA stages its own 128 rows of X and one half of W1's h rows (the B
-// operand is split across the pair), which halves the shared-memory traffic
-// per SM compared with one SM holding all of W1.  The accumulators (h fp32
-// columns per row) are double-buffered in TMEM, so that the epilogue of one
-// 256-row block runs while the MMAs of the next one fill the other buffer.
-// Pair q takes blocks q, q + P, q + 2P, ... (P pairs) and walks each block's K
-// from a different starting point, so that the pairs do not all read the same
-// W1 block from L2 at the same moment.
-//
-// Warp roles (256 threads per CTA): warp 0 lane 0 issues this CTA's TMA loads,
-// whose completion both CTAs count on the leader's (rank 0) stage barrier; in
-// the leader warp 1 lane 0 issues the pair MMAs; warp 1 of each CTA takes part
-// in the pair's TMEM allocation; warps 4-7 run the epilogue on the CTA's own
-// 128 rows, one thread per row.
-constexpr int kGateThreads = 256;
-constexpr int kGateMaxStages = 8;
-constexpr uint32_t kGateXBytes = kBM * kBK * 2;     // 16 KB: 128 rows of one K block
-
-struct GateSmemHead {
-  uint64_t full[kGateMaxStages];        // leader: both CTAs' copies of a stage landed
-  uint64_t empty[kGateMaxStages];       // the pair's MMAs are done with a stage
+// Barriers of a pair's stage ring and accumulators.  Placed after the ring in
+// dynamic shared memory: the kernels have no static shared memory, so the
+// ring starts at the 1024-byte aligned base and needs no alignment slack.
+struct PairHead {
+  uint64_t full[kPairMaxStages];        // leader: both CTAs' copies of a stage landed
+  uint64_t empty[kPairMaxStages];       // the pair's MMAs are done with a stage
   uint64_t acc_full[2];                 // accumulator buffer complete
   uint64_t acc_empty[2];                // leader: both epilogues have read a buffer
   uint64_t mma_done;
@@ -139,11 +48,121 @@ struct GateSmemHead {
   volatile int abort;
 };
 
-// Placed after the stage ring in dynamic shared memory (the kernel has no
-// static shared memory, so the ring starts at the 1024-byte aligned base and
-// needs no alignment slack: one more stage fits).
-struct GateSmemTail {
-  GateSmemHead head;
+// Stages that fit the device's per-block shared memory next to `tail` bytes.
+static cudaError_t pair_stages(size_t stage_bytes, size_t tail, int* n_st) {
+  int dev = 0, max_smem = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  int n = static_cast<int>((static_cast<size_t>(max_smem) - tail) / stage_bytes);
+  if (n > kPairMaxStages) n = kPairMaxStages;
+  if (n < 2) return cudaErrorInvalidConfiguration;
+  *n_st = n;
+  return cudaSuccess;
+}
+
+// Barrier setup by thread 0 (the acc_empty count is one arrive per epilogue
+// warp of both CTAs).
+__device__ __forceinline__ void pair_init(PairHead& h, int n_st, int epi_warps) {
+  for (int i = 0; i < n_st; ++i) { mbar_init(&h.full[i], 1); mbar_init(&h.empty[i], 1); }
+  for (int b = 0; b < 2; ++b) { mbar_init(&h.acc_full[b], 1); mbar_init(&h.acc_empty[b], 2 * epi_warps); }
+  mbar_init(&h.mma_done, 1);
+  h.abort = 0;
+  fence_barrier_init();
+}
+
+// Producer step: wait until stage `issued % n_st` is free, then copy this
+// CTA's A rows and B half into it; both copies complete on the leader's
+// barrier.  Returns false when the wait ran out (or another role aborted).
+__device__ __forceinline__ bool pair_issue(PairHead& h, uint8_t* ring, uint32_t issued, uint32_t n_st,
+                                           uint32_t stage_bytes, bool leader, uint32_t full0,
+                                           const CUtensorMap* map_a, int ax, int ay,
+                                           const CUtensorMap* map_b, int bx, int by,
+                                           long long wd, unsigned int* status) {
+  const uint32_t st = issued % n_st;
+  const uint32_t use = issued / n_st;
+  if (!mbar_wait(&h.empty[st], (use & 1u) ^ 1u, wd, status, kStatusTimeout) || h.abort) {
+    h.abort = 1;
+    return false;
+  }
+  uint8_t* s = ring + st * stage_bytes;
+  if (leader) mbar_arrive_expect_tx(&h.full[st], 2 * stage_bytes);
+  tma_load_2d_pair(s, map_a, full0 + st * 8u, ax, ay);
+  tma_load_2d_pair(s + kPairABytes, map_b, full0 + st * 8u, bx, by);
+  return true;
+}
+
+// The leader's MMAs of one K block (4 x K16 steps) into accumulator `d`.
+__device__ __forceinline__ void pair_mma_kblock(uint32_t d, const uint8_t* stage, uint32_t idesc, bool first) {
+  const uint32_t sa = smem_u32(stage);
+  const uint32_t sb = sa + kPairABytes;
+#pragma unroll
+  for (int ks = 0; ks < kBK / 16; ++ks)
+    mma_ss_pair(d, smem_desc_sw128(sa + ks * 32, 16, 1024), smem_desc_sw128(sb + ks * 32, 16, 1024), idesc,
+                (!first || ks > 0) ? 1u : 0u);
+}
+
+// The leader's share of the final drain: every copy either CTA issued must
+// land before the pair may leave.  The two producers stop together unless a
+// wait ran out; then the leader settles the difference: it arrives for a
+// stage only the other CTA issued, and counts off the other CTA's share of a
+// stage it issued alone.  Called after a cluster barrier that follows the
+// other CTA's store of its count.
+__device__ __forceinline__ void pair_drain(PairHead& h, uint32_t own, uint32_t n_st, uint32_t stage_bytes,
+                                           unsigned int* status) {
+  const uint32_t peer = h.peer_issued;
+  for (uint32_t g = own; g < peer; ++g) mbar_arrive_expect_tx(&h.full[g % n_st], stage_bytes);
+  for (uint32_t g = peer; g < own; ++g) mbar_complete_tx(&h.full[g % n_st], stage_bytes);
+  const uint32_t last_g = own > peer ? own : peer;
+  for (uint32_t st = 0; st < n_st && st < last_g; ++st) {
+    const uint32_t last = ((last_g - 1 - st) / n_st) * n_st + st;
+    mbar_wait(&h.full[st], (last / n_st) & 1u, kDrainCycles, status, kStatusTimeout);
+  }
+}
+
+// Launch a pair kernel on as many pairs as the device co-schedules, at most
+// `units` (the persistent pairs take the units round-robin).
+template <typename... Args>
+static cudaError_t launch_pairs(void (*kernel)(Args...), size_t smem, long long units, cudaStream_t st,
+                                int num_sms, Args... args) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2u * static_cast<unsigned>(num_sms / 2));
+  int n_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&n_clusters, kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n_clusters < 1) return cudaErrorInvalidConfiguration;
+  const long long pairs = units < n_clusters ? units : n_clusters;
+  cfg.gridDim = dim3(2u * static_cast<unsigned>(pairs));
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// ---------------------------------------------------------------------------
+// gate
+// ---------------------------------------------------------------------------
+// Pair q takes 256-row blocks q, q + P, q + 2P, ... (P pairs) and walks each
+// block's K from a different starting point, so that the pairs do not all
+// read the same W1 block from L2 at the same moment.  B = W1: each CTA stages
+// W1 rows [rank h/2, rank h/2 + h/2).
+//
+// Warp roles (256 threads per CTA): warp 0 lane 0 issues this CTA's copies; in
+// the leader warp 1 lane 0 issues the pair MMAs; warp 1 of each CTA takes part
+// in the pair's TMEM allocation; warps 4-7 run the epilogue on the CTA's own
+// 128 rows, one thread per row.
+struct GateTail {
+  PairHead head;
   alignas(16) float b1[256];
   alignas(16) float w2[256];
 };
@@ -164,29 +183,28 @@ __device__ __forceinline__ bool row_is_doc(const GateArgs& a, long long row) {
   return row - start < nd;
 }
 
-__global__ void __launch_bounds__(kGateThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
 gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w1,
             GateArgs a, int n_st) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
-  const int lane = lane_id();
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  const uint32_t half_cols = tmem_cols_for(a.h);   // one accumulator buffer
-  const uint32_t ncols = 2 * half_cols;
   const int hb = a.h / 2;                          // W1 rows staged by each CTA
-  const uint32_t stage_bytes = kGateXBytes + static_cast<uint32_t>(hb) * kBK * 2;
-  GateSmemTail& tail = *reinterpret_cast<GateSmemTail*>(smem_raw + static_cast<size_t>(n_st) * stage_bytes);
-  GateSmemHead& head = tail.head;
-  float* sb1 = tail.b1;
-  float* sw2 = tail.w2;
+  const uint32_t stage_bytes = kPairABytes + static_cast<uint32_t>(hb) * kBK * 2;
+  GateTail& tail = *reinterpret_cast<GateTail*>(smem_raw + static_cast<size_t>(n_st) * stage_bytes);
+  PairHead& head = tail.head;
   // 128-byte swizzled TMA and MMA tiles need a 1024-byte aligned ring; both
   // CTAs of a pair see the same base, so both leave here together
   if ((smem_u32(smem_raw) & 1023u) != 0) {
     if (threadIdx.x == 0) record_error(a.status, kStatusIndex);
     return;
   }
-  const int warp = warp_id();  const long long n_blocks = (a.n_rows + 2 * kBM - 1) / (2 * kBM);   // 256-row blocks
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t half_cols = tmem_cols_for(a.h);   // one accumulator buffer
+  const uint32_t ncols = 2 * half_cols;
+  const long long n_blocks = (a.n_rows + 2 * kBM - 1) / (2 * kBM);   // 256-row blocks
   const int n_pairs = static_cast<int>(gridDim.x >> 1);
   const int q = static_cast<int>(blockIdx.x >> 1);
   const int n_pass = (q < n_blocks) ? static_cast<int>((n_blocks - q + n_pairs - 1) / n_pairs) : 0;
@@ -194,24 +212,14 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   const long long wd = a.watchdog;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < n_st; ++i) {
-      mbar_init(&head.full[i], 1);
-      mbar_init(&head.empty[i], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&head.acc_full[b], 1);
-      mbar_init(&head.acc_empty[b], 2 * 4);   // one arrive per epilogue warp of both CTAs
-    }
-    mbar_init(&head.mma_done, 1);
-    head.abort = 0;
-    fence_barrier_init();
+    pair_init(head, n_st, 4);
     prefetch_tmap(&map_x);
     prefetch_tmap(&map_w1);
   }
   if (warp == 1) { tmem_alloc_pair(&head.tmem_base, ncols); tmem_relinquish_pair(); }
-  for (int i = threadIdx.x; i < a.h; i += kGateThreads) {
-    sb1[i] = a.b1 ? a.b1[i] : 0.0f;
-    sw2[i] = __bfloat162float(a.w2[i]);
+  for (int i = threadIdx.x; i < a.h; i += kPairThreads) {
+    tail.b1[i] = a.b1 ? a.b1[i] : 0.0f;
+    tail.w2[i] = __bfloat162float(a.w2[i]);
   }
   tc_fence_before();
   __syncthreads();
@@ -222,24 +230,17 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer: this CTA's X rows and W1 half ----------------
     const uint32_t full0 = mapa_shared(smem_u32(&head.full[0]), 0);
-    for (int p = 0; p < n_pass && !head.abort; ++p) {
+    bool ok = true;
+    for (int p = 0; p < n_pass && ok; ++p) {
       const long long blk = q + static_cast<long long>(p) * n_pairs;
       const int row0 = static_cast<int>(blk * 2 * kBM) + static_cast<int>(rank) * kBM;
       const int kb0 = (q + p) % nk;
-      for (int i = 0; i < nk; ++i) {
+      for (int i = 0; i < nk && ok; ++i) {
         int kb = kb0 + i;
         if (kb >= nk) kb -= nk;
-        const int st = static_cast<int>(issued % n_st);
-        const uint32_t use = issued / n_st;
-        if (!mbar_wait(&head.empty[st], (use & 1u) ^ 1u, wd, a.status, kStatusTimeout) || head.abort) {
-          head.abort = 1;
-          break;
-        }
-        uint8_t* s = ring + st * stage_bytes;
-        if (leader) mbar_arrive_expect_tx(&head.full[st], 2 * stage_bytes);
-        tma_load_2d_pair(s, &map_x, full0 + st * 8u, kb * kBK, row0);
-        tma_load_2d_pair(s + kGateXBytes, &map_w1, full0 + st * 8u, kb * kBK, static_cast<int>(rank) * hb);
-        ++issued;
+        ok = pair_issue(head, ring, issued, n_st, stage_bytes, leader, full0, &map_x, kb * kBK, row0, &map_w1,
+                        kb * kBK, static_cast<int>(rank) * hb, wd, a.status);
+        if (ok) ++issued;
       }
     }
     if (!leader) st_cluster_u32(mapa_shared(smem_u32(&head.peer_issued), 0), issued);
@@ -258,16 +259,10 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
       const uint32_t d = head.tmem_base + static_cast<uint32_t>(b) * half_cols;
       for (int i = 0; i < nk; ++i, ++g) {
         const int st = static_cast<int>(g % n_st);
-        const uint32_t par = (g / n_st) & 1u;
-        ok = mbar_wait(&head.full[st], par, wd, a.status, kStatusTimeout) && !head.abort;
+        ok = mbar_wait(&head.full[st], (g / n_st) & 1u, wd, a.status, kStatusTimeout) && !head.abort;
         if (!ok) break;
         tc_fence_after();
-        const uint32_t sa = smem_u32(ring + st * stage_bytes);
-        const uint32_t sb = sa + kGateXBytes;
-#pragma unroll
-        for (int ks = 0; ks < kBK / 16; ++ks)
-          mma_ss_pair(d, smem_desc_sw128(sa + ks * 32, 16, 1024), smem_desc_sw128(sb + ks * 32, 16, 1024), idesc,
-                      (i > 0 || ks > 0) ? 1u : 0u);
+        pair_mma_kblock(d, ring + st * stage_bytes, idesc, i == 0);
         mma_commit_pair_mc(&head.empty[st], 0x3);
       }
       if (ok) mma_commit_pair_mc(&head.acc_full[b], 0x3);
@@ -293,8 +288,8 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
       // Branch-free 32-column chunks (then one 16-column tail when h % 32 ==
       // 16) so the GELU chains of a chunk interleave; two partial sums.
       float2 zp[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-      const float2* b1p = reinterpret_cast<const float2*>(sb1);
-      const float2* w2p = reinterpret_cast<const float2*>(sw2);
+      const float2* b1p = reinterpret_cast<const float2*>(tail.b1);
+      const float2* w2p = reinterpret_cast<const float2*>(tail.w2);
       int c0 = 0;
       for (; c0 + 32 <= a.h; c0 += 32) {
         uint32_t r[32];
@@ -334,20 +329,7 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   tc_fence_before();
   __syncthreads();
   cluster_sync();      // every role is done; the other CTA's issue count is in place
-  if (leader && warp == 0 && lane == 0) {
-    // Every copy either CTA issued must land before the pair may leave.  The
-    // two producers stop together unless a wait ran out; then the leader
-    // settles the difference: it arrives for a stage only the other CTA
-    // issued, and counts off the other CTA's share of a stage it issued alone.
-    const uint32_t peer = head.peer_issued;
-    for (uint32_t g = issued; g < peer; ++g) mbar_arrive_expect_tx(&head.full[g % n_st], stage_bytes);
-    for (uint32_t g = peer; g < issued; ++g) mbar_complete_tx(&head.full[g % n_st], stage_bytes);
-    const uint32_t last_g = issued > peer ? issued : peer;
-    for (uint32_t st = 0; st < static_cast<uint32_t>(n_st) && st < last_g; ++st) {
-      const uint32_t last = ((last_g - 1 - st) / n_st) * n_st + st;
-      mbar_wait(&head.full[st], (last / n_st) & 1u, kDrainCycles, a.status, kStatusTimeout);
-    }
-  }
+  if (leader && warp == 0 && lane == 0) pair_drain(head, issued, static_cast<uint32_t>(n_st), stage_bytes, a.status);
   __syncthreads();
   cluster_sync();      // no CTA leaves while the other may still signal it
   if (warp == 1) { tc_fence_after(); tmem_dealloc_pair(head.tmem_base, ncols); }
@@ -356,81 +338,119 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
 cudaError_t launch_gate(const CUtensorMap& map_x, const CUtensorMap& map_w1, const GateArgs& a,
                         cudaStream_t st) {
   if (a.n_rows == 0) return cudaSuccess;
-  const size_t stage_bytes = kGateXBytes + static_cast<size_t>(a.h / 2) * kBK * 2;
-  int dev = 0, max_smem = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const size_t stage_bytes = kPairABytes + static_cast<size_t>(a.h / 2) * kBK * 2;
+  int n_st = 0;
+  cudaError_t e = pair_stages(stage_bytes, sizeof(GateTail), &n_st);
   if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e != cudaSuccess) return e;
-  int n_st = static_cast<int>((static_cast<size_t>(max_smem) - sizeof(GateSmemTail)) / stage_bytes);
-  if (n_st > kGateMaxStages) n_st = kGateMaxStages;
-  if (n_st < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = static_cast<size_t>(n_st) * stage_bytes + sizeof(GateSmemTail);
-  e = cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  const size_t smem = static_cast<size_t>(n_st) * stage_bytes + sizeof(GateTail);
   const long long blocks = (a.n_rows + 2 * kBM - 1) / (2 * kBM);
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kGateThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // one pair per two SMs at most; a persistent pair takes several blocks
-  cfg.gridDim = dim3(2u * static_cast<unsigned>(a.num_sms / 2));
-  int n_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&n_clusters, gate_kernel, &cfg);
-  if (e != cudaSuccess) return e;
-  if (n_clusters < 1) return cudaErrorInvalidConfiguration;
-  const long long pairs = blocks < n_clusters ? blocks : n_clusters;
-  cfg.gridDim = dim3(2u * static_cast<unsigned>(pairs));
-  return cudaLaunchKernelEx(&cfg, gate_kernel, map_x, map_w1, a, n_st);
+  return launch_pairs(gate_kernel, smem, blocks, st, a.num_sms, map_x, map_w1, a, n_st);
 }
 
 // ---------------------------------------------------------------------------
 // linear: out = A W^T (+ residual), bf16 out
 // ---------------------------------------------------------------------------
-constexpr int kLinStages = 4;
-constexpr int kLinBN = 256;
+// Tiles of 256 rows x bn columns (bn = 256, or n when smaller); pair q takes
+// tiles q, q + P, ... in row-major tile order.  B = W: each CTA stages W rows
+// [n0 + rank bn/2, + bn/2).  Epilogue: 4 warps per CTA, one thread per row,
+// fp32 accumulators rounded once to bf16 after the residual add.
+struct LinearTail {
+  PairHead head;
+};
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
 linear_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
-              LinearArgs a, int bn) {
+              LinearArgs a, int bn, int n_st) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ GemmSmemHead head;
-  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem_raw;
+  const uint32_t stage_bytes = kPairABytes + static_cast<uint32_t>(bn / 2) * kBK * 2;
+  PairHead& head = reinterpret_cast<LinearTail*>(smem_raw + static_cast<size_t>(n_st) * stage_bytes)->head;
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(a.status, kStatusIndex);
+    return;
+  }
   const int warp = warp_id();
   const int lane = lane_id();
-  const int m0 = blockIdx.x * kBM;
-  const int n0 = blockIdx.y * bn;
-  const uint32_t ncols = tmem_cols_for(bn);
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t half_cols = tmem_cols_for(bn);
+  const uint32_t ncols = 2 * half_cols;
+  const long long n_mt = (a.m + 2 * kBM - 1) / (2 * kBM);
+  const int n_nt = (a.n + bn - 1) / bn;
+  const long long n_tiles = n_mt * n_nt;
+  const int n_pairs = static_cast<int>(gridDim.x >> 1);
+  const int q = static_cast<int>(blockIdx.x >> 1);
+  const int n_mine = (q < n_tiles) ? static_cast<int>((n_tiles - q + n_pairs - 1) / n_pairs) : 0;
+  const int nk = a.kdim / kBK;
+  const long long wd = a.watchdog;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kLinStages; ++i) { mbar_init(&head.full[i], 1); mbar_init(&head.empty[i], 1); }
-    mbar_init(&head.acc_full, 1);
-    head.abort = 0;
-    fence_barrier_init();
+    pair_init(head, n_st, 4);
     prefetch_tmap(&map_a);
     prefetch_tmap(&map_w);
   }
-  if (warp == 1) { tmem_alloc(&head.tmem_base, ncols); tmem_relinquish(); }
+  if (warp == 1) { tmem_alloc_pair(&head.tmem_base, ncols); tmem_relinquish_pair(); }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   tc_fence_after();
 
-  gemm_mainloop<kLinStages>(&map_a, &map_w, &head, stages, bn, m0, n0, a.kdim, a.status, a.watchdog);
-
-  if (warp >= 2) {
+  uint32_t issued = 0;
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer: this CTA's A rows and W half ----------------
+    const uint32_t full0 = mapa_shared(smem_u32(&head.full[0]), 0);
+    bool ok = true;
+    for (int p = 0; p < n_mine && ok; ++p) {
+      const long long tile = q + static_cast<long long>(p) * n_pairs;
+      const int m0 = static_cast<int>((tile / n_nt) * 2 * kBM) + static_cast<int>(rank) * kBM;
+      const int n0 = static_cast<int>(tile % n_nt) * bn + static_cast<int>(rank) * (bn / 2);
+      for (int kb = 0; kb < nk && ok; ++kb) {
+        ok = pair_issue(head, ring, issued, n_st, stage_bytes, leader, full0, &map_a, kb * kBK, m0, &map_w,
+                        kb * kBK, n0, wd, a.status);
+        if (ok) ++issued;
+      }
+    }
+    if (!leader) st_cluster_u32(mapa_shared(smem_u32(&head.peer_issued), 0), issued);
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ---------------- pair MMA issuer ----------------
+    const uint32_t idesc = idesc_bf16_f32(2 * kBM, static_cast<uint32_t>(bn), 0, 0);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int p = 0; p < n_mine && ok; ++p) {
+      const int b = p & 1;
+      ok = mbar_wait(&head.acc_empty[b], ((static_cast<uint32_t>(p) >> 1) & 1u) ^ 1u, wd, a.status, kStatusTimeout) &&
+           !head.abort;
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d = head.tmem_base + static_cast<uint32_t>(b) * half_cols;
+      for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int st = static_cast<int>(g % n_st);
+        ok = mbar_wait(&head.full[st], (g / n_st) & 1u, wd, a.status, kStatusTimeout) && !head.abort;
+        if (!ok) break;
+        tc_fence_after();
+        pair_mma_kblock(d, ring + st * stage_bytes, idesc, kb == 0);
+        mma_commit_pair_mc(&head.empty[st], 0x3);
+      }
+      if (ok) mma_commit_pair_mc(&head.acc_full[b], 0x3);
+    }
+    if (!ok) head.abort = 1;
+    mma_commit_pair_mc(&head.mma_done, 0x1);
+    mbar_wait(&head.mma_done, 0, kDrainCycles, a.status, kStatusTimeout);
+  } else if (warp >= 4) {
+    // ---------------- epilogue: (+ residual), bf16 ----------------
     const int sub = warp & 3;
-    const long long row = m0 + sub * 32 + lane;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(&head.acc_full, 0, a.watchdog, a.status, kStatusTimeout));
-    tc_fence_after();
-    const uint32_t tbase = head.tmem_base + (static_cast<uint32_t>(sub * 32) << 16);
-    if (ok) {
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(&head.acc_empty[0]), 0);
+    for (int p = 0; p < n_mine; ++p) {
+      const int b = p & 1;
+      const long long tile = q + static_cast<long long>(p) * n_pairs;
+      const long long row = (tile / n_nt) * 2 * kBM + static_cast<long long>(rank) * kBM + sub * 32 + lane;
+      const int n0 = static_cast<int>(tile % n_nt) * bn;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&head.acc_full[b], (static_cast<uint32_t>(p) >> 1) & 1u, wd,
+                                                         a.status, kStatusTimeout));
+      if (!ok || head.abort) { head.abort = 1; break; }
+      tc_fence_after();
+      const uint32_t tbase = head.tmem_base + static_cast<uint32_t>(b) * half_cols +
+                             (static_cast<uint32_t>(sub * 32) << 16);
       const int ncols_here = min(bn, a.n - n0);
       for (int c0 = 0; c0 < ncols_here; c0 += 32) {
         uint32_t r[32];
@@ -444,6 +464,12 @@ linear_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
           for (int i = 0; i < 16; ++i) { r[i] = r16[i]; r[16 + i] = 0u; }
         }
         tmem_ld_wait();
+        if (c0 + 32 >= ncols_here) {
+          // the last TMEM read of this buffer: tell the leader's MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(b) * 8u);
+        }
         if (row < a.m) {
           const size_t off = static_cast<size_t>(row) * a.n + n0 + c0;
           const int nv = full32 ? 4 : 2;              // 16-byte vectors (8 bf16)
@@ -476,20 +502,24 @@ linear_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) { tc_fence_after(); tmem_dealloc(head.tmem_base, ncols); }
+  cluster_sync();
+  if (leader && warp == 0 && lane == 0) pair_drain(head, issued, static_cast<uint32_t>(n_st), stage_bytes, a.status);
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) { tc_fence_after(); tmem_dealloc_pair(head.tmem_base, ncols); }
 }
 
 cudaError_t launch_linear(const CUtensorMap& map_a, const CUtensorMap& map_w, const LinearArgs& a,
                           cudaStream_t st) {
   if (a.m == 0 || a.n == 0) return cudaSuccess;
-  const int bn = a.n >= kLinBN ? kLinBN : a.n;
-  const size_t smem = 1024 + static_cast<size_t>(kLinStages) * (kATileBytes + bn * kBK * 2);
-  cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  const int bn = linear_tile_n(a.n);
+  const size_t stage_bytes = kPairABytes + static_cast<size_t>(bn / 2) * kBK * 2;
+  int n_st = 0;
+  cudaError_t e = pair_stages(stage_bytes, sizeof(LinearTail), &n_st);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>((a.m + kBM - 1) / kBM), static_cast<unsigned>((a.n + bn - 1) / bn));
-  linear_kernel<<<grid, kGemmThreads, smem, st>>>(map_a, map_w, a, bn);
-  return cudaGetLastError();
+  const size_t smem = static_cast<size_t>(n_st) * stage_bytes + sizeof(LinearTail);
+  const long long tiles = ((a.m + 2 * kBM - 1) / (2 * kBM)) * ((a.n + bn - 1) / bn);
+  return launch_pairs(linear_kernel, smem, tiles, st, a.num_sms, map_a, map_w, a, bn, n_st);
 }
 
 }  // namespace tg

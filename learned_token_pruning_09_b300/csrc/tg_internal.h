@@ -118,7 +118,11 @@ struct LinearArgs {
   int32_t kdim;
   unsigned int* status;
   long long watchdog;
+  int num_sms;
 };
+// Columns of a linear tile: 256, or n itself when smaller (n is a multiple
+// of 16, so each CTA of a pair stages a multiple of 8 rows of W).
+inline int linear_tile_n(int n) { return n >= 256 ? 256 : n; }
 cudaError_t launch_linear(const CUtensorMap& map_a, const CUtensorMap& map_w, const LinearArgs& a,
                           cudaStream_t st);
 
