@@ -165,7 +165,7 @@ def custom(name: str, n_doc, n_q, k, d=256, h=64, hq=4, hkv=2, head_dim=64,
 # ---------------------------------------------------------------------------
 
 # sub-stream ids (stable: adding a stream never changes another's draws)
-_S_X, _S_W1, _S_W2, _S_QKV, _S_GAIN, _S_TAU, _S_PLANT, _S_SCORES, _S_LAYERS = range(9)
+_S_X, _S_W1, _S_W2, _S_QKV, _S_GAIN, _S_TAU, _S_PLANT, _S_SCORES, _S_LAYERS, _S_SPANS = range(10)
 
 
 def _stream(shape: Shape, sid: int) -> np.random.Generator:
@@ -254,6 +254,42 @@ def score_draws(shape: Shape, tie_frac: float = 0.05) -> np.ndarray:
             s[lo + z[len(z) // 2:]] = np.float32(0.0)
         s[lo + nd: lo + nd + shape.n_q[b]] = 0.0
     return s
+
+
+def prunable_spans(shape: Shape, spans_per_seq: int = 4, frac: float = 0.85,
+                   seed_offset: int = 0) -> np.ndarray:
+    """A per-row prunable mask (uint8 [n_rows]) with several marked spans per
+    sequence, the way a prompt template can mark more than one block of
+    retrieved text: each sequence's rows are cut at ``2 spans_per_seq - 1``
+    random points into alternating fixed / prunable / fixed / ... blocks
+    (the first and last blocks fixed), the prunable blocks covering about
+    ``frac`` of the sequence.  Sequences shorter than the span count get one
+    prunable block in the middle (or none when empty)."""
+    r = np.random.default_rng(np.random.SeedSequence(
+        [BASE_SEED, _S_SPANS, seed_offset, shape.n_rows, shape.batch]))
+    mask = np.zeros(shape.n_rows, dtype=np.uint8)
+    cu = shape.cu_seqlens
+    for b in range(shape.batch):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        n = hi - lo
+        if n == 0:
+            continue
+        if n < 4 * spans_per_seq:
+            mask[lo + n // 4: lo + n - n // 4] = 1
+            continue
+        # fixed blocks share (1 - frac) of the rows, prunable blocks frac
+        n_fix = spans_per_seq + 1
+        fix_w = r.dirichlet(np.ones(n_fix)) * (1.0 - frac) * n
+        prun_w = r.dirichlet(np.ones(spans_per_seq)) * frac * n
+        widths = np.empty(2 * spans_per_seq + 1)
+        widths[0::2] = fix_w
+        widths[1::2] = prun_w
+        edges = np.concatenate([[0], np.round(np.cumsum(widths)).astype(np.int64)])
+        edges[-1] = n
+        for sp in range(spans_per_seq):
+            a, e = edges[2 * sp + 1], edges[2 * sp + 2]
+            mask[lo + a: lo + e] = 1
+    return mask
 
 
 def budgets(shape: Shape) -> np.ndarray:

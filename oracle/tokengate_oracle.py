@@ -29,6 +29,12 @@ the exact algebra that they leave open is taken as follows:
           floor(h / G), G = hq / hkv.
 * stacked layer (long-context workload): qkv = x W_qkv^T, attention as above,
           x_out = x + o W_o^T.  No norm and no MLP.
+* general prunable spans (the prompt template marks the prunable document
+          with {state}; several marked spans, anywhere in a sequence): the gate
+          scores the prunable rows (0 elsewhere), the top-K budget of a
+          sequence goes to its prunable rows, every other row is kept, and the
+          kept rows come out in ascending row order.  With the mask equal to
+          the document prefix this is the document/question case above.
 
 Every function is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_pins.py`` against closed forms, brute force on tiny inputs,
@@ -49,7 +55,7 @@ from scipy.special import erf as _erf
 __all__ = [
     "bf16_decode", "gelu", "logsigmoid", "gate_score", "score_from_logit",
     "topk_select", "gather_kept", "rope", "gated_attention",
-    "stacked_layer", "project_qkv",
+    "stacked_layer", "project_qkv", "gate_score_masked", "topk_select_masked",
 ]
 
 
@@ -98,15 +104,30 @@ def gate_score(x_bits: np.ndarray, cu_seqlens: Sequence[int], n_doc: Sequence[in
     float64 from the bf16 inputs and rounded once to float32.  Question rows:
     exactly 0.0.  ``rows`` restricts the work to the given row ids (the other
     entries are returned as NaN)."""
+    n_rows = np.asarray(x_bits).shape[0]
+    is_doc = np.zeros(n_rows, dtype=bool)
+    for b in range(len(n_doc)):
+        lo = int(cu_seqlens[b])
+        is_doc[lo: lo + int(n_doc[b])] = True
+    return _gate_on_rows(x_bits, is_doc, w1_bits, b1, w2_bits, b2, rows)
+
+
+def gate_score_masked(x_bits: np.ndarray, prunable: np.ndarray, w1_bits: np.ndarray,
+                      b1: Optional[np.ndarray], w2_bits: np.ndarray, b2: float,
+                      rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """Gate scores with the prunable rows given by a per-row mask (any
+    number of spans, anywhere in a sequence): s = logsigmoid(w2 . GELU(W1 x +
+    b1) + b2) on prunable rows, exactly 0 on the others."""
+    return _gate_on_rows(x_bits, np.asarray(prunable).astype(bool), w1_bits, b1, w2_bits, b2, rows)
+
+
+def _gate_on_rows(x_bits, is_doc, w1_bits, b1, w2_bits, b2, rows):
+    """The gate MLP on the rows where ``is_doc`` holds, 0 on the others."""
     x_bits = np.asarray(x_bits)
     n_rows = x_bits.shape[0]
     w1 = bf16_decode(w1_bits)                      # [h, d]
     w2 = bf16_decode(w2_bits)                      # [h]
     bias1 = np.zeros(w1.shape[0]) if b1 is None else np.asarray(b1, np.float64)
-    is_doc = np.zeros(n_rows, dtype=bool)
-    for b in range(len(n_doc)):
-        lo = int(cu_seqlens[b])
-        is_doc[lo: lo + int(n_doc[b])] = True
     want = np.arange(n_rows) if rows is None else np.asarray(rows, np.int64)
     s = np.full(n_rows, np.nan, dtype=np.float32)
     doc_rows = want[is_doc[want]]
@@ -164,6 +185,34 @@ def topk_select(s: np.ndarray, cu_seqlens: Sequence[int], n_doc: Sequence[int],
         kept.extend(range(lo + nd, hi))
         cu.append(len(kept))
     return np.asarray(kept, dtype=np.int32), np.asarray(cu, dtype=np.int32)
+
+
+def topk_select_masked(s: np.ndarray, cu_seqlens: Sequence[int], prunable: np.ndarray,
+                       k: Sequence[int]):
+    """Kept rows per sequence with general prunable spans.
+
+    Returns (kept_idx int32 [sum T_b], cu_kept int32 [B+1], n_prunable int32
+    [B]).  For sequence b: the min(k_b, n_prunable_b) prunable rows with the
+    largest score (ties: lower row index first), together with every row that
+    is not prunable, all in ascending row order."""
+    s = np.asarray(s, dtype=np.float32)
+    prunable = np.asarray(prunable).astype(bool)
+    kept, cu, n_prun = [], [0], []
+    for b in range(len(k)):
+        lo = int(cu_seqlens[b])
+        hi = int(cu_seqlens[b + 1])
+        kb = int(k[b])
+        if kb < 0:
+            raise ValueError("negative budget")
+        cand = [r for r in range(lo, hi) if prunable[r]]
+        ke = min(kb, len(cand))
+        best = heapq.nsmallest(ke, cand, key=lambda r: _rank_key(float(s[r]), r))
+        fixed = [r for r in range(lo, hi) if not prunable[r]]
+        kept.extend(sorted(best + fixed))
+        cu.append(len(kept))
+        n_prun.append(len(cand))
+    return (np.asarray(kept, dtype=np.int32), np.asarray(cu, dtype=np.int32),
+            np.asarray(n_prun, dtype=np.int32))
 
 
 # ---------------------------------------------------------------------------

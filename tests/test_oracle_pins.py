@@ -220,6 +220,105 @@ def test_topk_invariants_on_workload_draws():
 
 
 # ---------------------------------------------------------------------------
+# general prunable spans
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_masked_select_with_prefix_mask_is_the_document_case(seed):
+    """A mask equal to each sequence's document prefix reduces the masked
+    selector and gate to the document/question ones (written separately)."""
+    rng = np.random.default_rng(100 + seed)
+    n_doc = rng.integers(0, 80, size=4).tolist()
+    n_q = rng.integers(0, 6, size=4).tolist()
+    k = rng.integers(0, 90, size=4).tolist()
+    shape = synth.custom("p", n_doc, n_q, k)
+    cu = shape.cu_seqlens
+    mask = np.zeros(shape.n_rows, np.uint8)
+    for b in range(4):
+        mask[cu[b]: cu[b] + n_doc[b]] = 1
+    s = synth.score_draws(shape)
+    kept, cu_kept = oracle.topk_select(s, cu, n_doc, k)
+    kept_m, cu_m, n_prun = oracle.topk_select_masked(s, cu, mask, k)
+    np.testing.assert_array_equal(kept_m, kept)
+    np.testing.assert_array_equal(cu_m, cu_kept)
+    np.testing.assert_array_equal(n_prun, n_doc)
+    x, p = synth.residuals(shape), synth.gate_weights(shape)
+    np.testing.assert_array_equal(
+        oracle.gate_score_masked(x, mask, p["w1"], p["b1"], p["w2"], p["b2"]),
+        oracle.gate_score(x, cu, n_doc, p["w1"], p["b1"], p["w2"], p["b2"]))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_masked_select_matches_rank_counting(seed):
+    """Random masks with several spans and many exact ties, against counting
+    for each prunable row how many prunable rows of its sequence beat it."""
+    rng = np.random.default_rng(200 + seed)
+    lens = rng.integers(0, 70, size=3)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    n = int(cu[-1])
+    mask = (rng.random(n) < 0.6).astype(np.uint8)
+    k = rng.integers(0, 50, size=3).tolist()
+    pool = np.array([-3.5, -1.0, -0.25, -0.0, 0.0, -7.0], dtype=np.float32)
+    s = pool[rng.integers(0, len(pool), size=n)]
+    kept, cu_kept, n_prun = oracle.topk_select_masked(s, cu, mask, k)
+    expect, ecu = [], [0]
+    for b in range(3):
+        rows = range(int(cu[b]), int(cu[b + 1]))
+        cand = [r for r in rows if mask[r]]
+        for r in rows:
+            if not mask[r]:
+                expect.append(r)
+                continue
+            beaten = sum(1 for i in cand if s[i] > s[r] or (s[i] == s[r] and i < r))
+            if beaten < k[b]:
+                expect.append(r)
+        ecu.append(len(expect))
+        assert n_prun[b] == len(cand)
+    np.testing.assert_array_equal(kept, expect)
+    np.testing.assert_array_equal(cu_kept, ecu)
+
+
+def test_masked_select_special_cases():
+    s = np.array([-1.0, -2.0, -0.5, -3.0, -0.1, -4.0], np.float32)
+    cu = [0, 6]
+    # nothing prunable: every row kept, whatever the budget
+    none = np.zeros(6, np.uint8)
+    assert oracle.topk_select_masked(s, cu, none, [0])[0].tolist() == list(range(6))
+    assert oracle.topk_select_masked(s, cu, none, [3])[0].tolist() == list(range(6))
+    # everything prunable: K = 0 keeps nothing, K >= n keeps everything
+    allp = np.ones(6, np.uint8)
+    assert oracle.topk_select_masked(s, cu, allp, [0])[0].tolist() == []
+    assert oracle.topk_select_masked(s, cu, allp, [9])[0].tolist() == list(range(6))
+    assert oracle.topk_select_masked(s, cu, allp, [2])[0].tolist() == [2, 4]
+    # fixed rows interleaved with two spans keep their place in row order
+    two = np.array([1, 1, 0, 1, 1, 0], np.uint8)
+    assert oracle.topk_select_masked(s, cu, two, [2])[0].tolist() == [0, 2, 4, 5]
+    assert oracle.topk_select_masked(s, cu, two, [1])[0].tolist() == [2, 4, 5]
+
+
+def test_masked_select_invariants_on_span_draws():
+    shape = synth.ragged_batch()
+    shape = synth.custom("r", [n // 64 for n in shape.n_doc], shape.n_q,
+                         [k // 64 for k in shape.k])
+    mask = synth.prunable_spans(shape)
+    s = synth.score_draws(shape)
+    kept, cu_kept, n_prun = oracle.topk_select_masked(s, shape.cu_seqlens, mask, shape.k)
+    cu = shape.cu_seqlens
+    for b in range(shape.batch):
+        ks = kept[cu_kept[b]: cu_kept[b + 1]]
+        rows = np.arange(cu[b], cu[b + 1])
+        assert np.all(np.diff(ks) > 0)
+        fixed = rows[mask[rows] == 0]
+        assert set(fixed.tolist()) <= set(ks.tolist())
+        prun_kept = ks[mask[ks] == 1]
+        assert len(prun_kept) == min(shape.k[b], int(n_prun[b]))
+        dropped = np.setdiff1d(rows[mask[rows] == 1], prun_kept)
+        if len(prun_kept) and len(dropped):
+            assert s[prun_kept].min() >= s[dropped].max()
+
+
+# ---------------------------------------------------------------------------
 # gather
 # ---------------------------------------------------------------------------
 
