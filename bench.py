@@ -69,6 +69,69 @@ def path_bytes(shape):
     return float(n * 2 * d + n * 8 + t * 8 + t * 4 * d + t * 8)
 
 
+def masked_path_bytes(shape, n_kept):
+    """The same algorithmic bytes for the general prunable-span path, plus
+    the mask read twice (counting and selecting, 1 + 1 per row); n_kept is
+    that path's kept count."""
+    n, d = shape.n_rows, shape.d
+    return float(n * 2 * d + n * 8 + 2 * n + n_kept * 8 + n_kept * 4 * d + n_kept * 8)
+
+
+def measure_masked(P, shape, flush, steps):
+    """General prunable spans: the masked gate, top-K and gather on a seeded
+    multi-span mask whose prunable share is the workload's document share
+    (so the kept count stays close to the workload's), timed like the step:
+    one CUDA graph with events between the three calls, L2 flushed first."""
+    import torch
+    from learned_token_pruning_09_b300 import synth
+    tg = P.tg
+    frac = float(sum(shape.n_doc)) / max(shape.n_rows, 1)
+    mask_h = synth.prunable_spans(shape, frac=frac)
+    mask = torch.as_tensor(mask_h).to(P.dev)
+    max_len = int(np.diff(shape.cu_seqlens).max())
+    kept = torch.empty(shape.n_rows, dtype=torch.int32, device=P.dev)
+    cu_kept = torch.empty(shape.batch + 1, dtype=torch.int32, device=P.dev)
+    n_prun = torch.empty(shape.batch, dtype=torch.int32, device=P.dev)
+    s = torch.empty(shape.n_rows, dtype=torch.float32, device=P.dev)
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+
+    def calls(n_kept):
+        ev[0].record()
+        tg.tg_gate_score_masked(P.X, mask, P.W1, None, P.W2, P.b2, s_out=s)
+        ev[1].record()
+        tg.tg_topk_select_masked(s, P.cu, mask, P.kk, max_len, kept_idx=kept, cu_kept=cu_kept, n_prunable=n_prun)
+        ev[2].record()
+        tg.tg_gather_kept(P.X, s, P.cu, kept[:n_kept], cu_kept, n_kept, x_kept=P.xk_masked[:n_kept],
+                          pos_kept=P.pos_masked[:n_kept], s_kept=P.s_masked[:n_kept])
+        ev[3].record()
+
+    # the kept count is device data: learn it once, eagerly, then capture
+    tg.tg_gate_score_masked(P.X, mask, P.W1, None, P.W2, P.b2, s_out=s)
+    tg.tg_topk_select_masked(s, P.cu, mask, P.kk, max_len, kept_idx=kept, cu_kept=cu_kept, n_prunable=n_prun)
+    n_kept = int(cu_kept[-1].item())
+    P.xk_masked = torch.empty((n_kept, shape.d), dtype=torch.bfloat16, device=P.dev)
+    P.pos_masked = torch.empty(n_kept, dtype=torch.int32, device=P.dev)
+    P.s_masked = torch.empty(n_kept, dtype=torch.float32, device=P.dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        calls(n_kept)
+    per = []
+    for i in range(3 + steps):
+        flush.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        if i >= 3:
+            per.append([ev[k].elapsed_time(ev[k + 1]) for k in range(3)])
+    if tg.tg_check_device_status() != tg.TG_OK:
+        raise RuntimeError("device status after the masked path: " + tg.lib.tg_last_error_string().decode())
+    per = np.array(per).mean(axis=0)
+    us = float(per.sum()) * 1e3
+    byts = masked_path_bytes(shape, n_kept)
+    return {"us": us, "gbs": byts / (us * 1e-6) / 1e9, "bytes": byts, "n_kept": n_kept,
+            "spans_per_seq": 4, "prunable_rows": int(mask_h.sum()),
+            "gate_us": float(per[0]) * 1e3, "topk_us": float(per[1]) * 1e3, "gather_us": float(per[2]) * 1e3}
+
+
 def max_over_ranks(values, device):
     """Each value's maximum over the ranks of the default process group (the
     values unchanged when there is one rank): the slowest rank's time."""
@@ -437,6 +500,10 @@ def run_gpu(args, shape):
     byts = path_bytes(shape)
     peaks = load_peaks()
 
+    # ---- general prunable spans (the next row after the path) ----
+    masked = measure_masked(P, shape, flush, args.steps)
+    masked["frac_of_measured_hbm"] = masked["gbs"] / peaks["hbm_gbs"]
+
     # ---- end to end through the public API, host buffers ----
     import torch as _t
     x_h = _t.from_numpy(np.ascontiguousarray(inputs["x"]).view(np.int16)).view(_t.bfloat16).pin_memory()
@@ -503,6 +570,7 @@ def run_gpu(args, shape):
                           "gflop_per_layer": flops_layer / 1e9,
                           "kernel_ms_per_layer": kern_ms / nl, "kernel_tflops": kern_tflops,
                           "rope_us_per_layer": rope_ms / nl * 1e3},
+            "masked_gate_topk_gather": masked,
             "gate_topk_gather": {"us": gtg_ms * 1e3, "gbs": byts / (gtg_ms * 1e-3) / 1e9, "bytes": byts,
                                  "frac_of_measured_hbm": byts / (gtg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                  "gate_us": seg_ms["gate"] * 1e3, "topk_us": seg_ms["topk"] * 1e3,

@@ -116,6 +116,40 @@ TG_API tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* c
                          cudaStream_t stream);
 
 /*
+ * General prunable spans (the prompt template marks the prunable text; with
+ * several marked spans, the document need not be a prefix).  A per-row mask
+ * replaces n_doc: prunable [n_rows] uint8, nonzero = prunable.  The reading
+ * taken: the gate scores the prunable rows (0 on every other row), a
+ * sequence's budget k[b] goes to its prunable rows, and every other row is
+ * kept; with the mask equal to the document prefix both calls give exactly
+ * the results of tg_gate_score and tg_topk_select.
+ *
+ * tg_gate_score_masked: as tg_gate_score, with s = 0 on rows outside the
+ *   mask; no sequence arguments (the mask is per row).
+ *
+ * tg_topk_select_masked: per sequence b, the min(k[b], n_prunable[b])
+ *   prunable rows with the largest score (ties: lower row first) together with
+ *   every row outside the mask, in ascending row order; cu_kept as in
+ *   tg_topk_select.
+ *   max_len        host upper bound on every sequence's length (sizes the launch)
+ *   kept_capacity  length of kept_idx; a sequence whose kept rows would end
+ *                  past it writes nothing and sets TG_ERR_DEVICE_INDEX
+ *   n_prunable     [batch] int32 output: prunable rows per sequence (also the
+ *                  call's scratch: written by a counting kernel, then read)
+ *   The total kept count is cu_kept[batch] = sum_b min(k[b], n_prunable[b]) +
+ *   (length_b - n_prunable[b]); a caller that does not know the mask on the
+ *   host can size kept_idx by n_rows.
+ */
+TG_API tg_status tg_gate_score_masked(const void* x_bf16, int64_t n_rows, int32_t d,
+                               const uint8_t* prunable, const void* w1_bf16,
+                               const float* b1, const void* w2_bf16, float b2, int32_t h,
+                               float* s_out, cudaStream_t stream);
+TG_API tg_status tg_topk_select_masked(const float* s, int64_t n_rows, const int32_t* cu_seqlens,
+                                const uint8_t* prunable, const int32_t* k, int32_t batch,
+                                int32_t max_len, int64_t kept_capacity, int32_t* kept_idx,
+                                int32_t* cu_kept, int32_t* n_prunable, cudaStream_t stream);
+
+/*
  * Gather of the kept rows (third phase: the layers above L run on the kept
  * tokens only).  For kept slot i of sequence b:
  *     x_kept[i] = X[kept_idx[i]],  pos_kept[i] = kept_idx[i] - cu_seqlens[b],

@@ -141,15 +141,20 @@ tg_status tg_check_device_status(cudaStream_t stream) {
   return ok();
 }
 
-tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d, const int32_t* cu_seqlens,
-                        const int32_t* n_doc, int32_t batch, const void* w1_bf16, const float* b1,
-                        const void* w2_bf16, float b2, int32_t h, float* s_out, cudaStream_t stream) {
+// the gate on the document prefix (prunable null) or on a per-row mask
+static tg_status gate_score_any(const void* x_bf16, int64_t n_rows, int32_t d, const int32_t* cu_seqlens,
+                                const int32_t* n_doc, int32_t batch, bool masked, const uint8_t* prunable,
+                                const void* w1_bf16,
+                                const float* b1, const void* w2_bf16, float b2, int32_t h, float* s_out,
+                                cudaStream_t stream) {
   if (n_rows < 0 || n_rows > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_rows out of range");
-  if (batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
+  if (!masked && batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
   if (d < 64 || d % 64 != 0 || d > (1 << 20)) return fail(TG_ERR_INVALID_ARG, "d must be a positive multiple of 64");
   if (h < 16 || h > 256 || h % 16 != 0) return fail(TG_ERR_INVALID_ARG, "h must be a multiple of 16 in [16, 256]");
-  if (!cu_seqlens || !n_doc || !w1_bf16 || !w2_bf16) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if ((!masked && (!cu_seqlens || !n_doc)) || !w1_bf16 || !w2_bf16)
+    return fail(TG_ERR_INVALID_ARG, "null pointer argument");
   if (n_rows == 0) return ok();
+  if (masked && !prunable) return fail(TG_ERR_INVALID_ARG, "null prunable mask");
   if (!x_bf16 || !s_out) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(x_bf16) || !aligned16(w1_bf16)) return fail(TG_ERR_INVALID_ARG, "x and w1 must be 16-byte aligned");
   if (!std::isfinite(b2)) return fail(TG_ERR_INVALID_ARG, "b2 must be finite");
@@ -171,6 +176,7 @@ tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d, const int
     if ((s = make_map(&mw, w1_bf16, 2, dims, str, box, "w1")) != TG_OK) return s;
   }
   GateArgs a{};
+  a.prunable = prunable;
   a.b1 = b1;
   a.w2 = static_cast<const __nv_bfloat16*>(w2_bf16);
   a.b2 = b2;
@@ -187,6 +193,20 @@ tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d, const int
   cudaError_t e = launch_gate(mx, mw, a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gate kernel launch");
   return ok();
+}
+
+tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d, const int32_t* cu_seqlens,
+                        const int32_t* n_doc, int32_t batch, const void* w1_bf16, const float* b1,
+                        const void* w2_bf16, float b2, int32_t h, float* s_out, cudaStream_t stream) {
+  return gate_score_any(x_bf16, n_rows, d, cu_seqlens, n_doc, batch, false, nullptr, w1_bf16, b1, w2_bf16, b2, h,
+                        s_out, stream);
+}
+
+tg_status tg_gate_score_masked(const void* x_bf16, int64_t n_rows, int32_t d, const uint8_t* prunable,
+                               const void* w1_bf16, const float* b1, const void* w2_bf16, float b2, int32_t h,
+                               float* s_out, cudaStream_t stream) {
+  return gate_score_any(x_bf16, n_rows, d, nullptr, nullptr, 0, true, prunable, w1_bf16, b1, w2_bf16, b2, h, s_out,
+                        stream);
 }
 
 tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* cu_seqlens, const int32_t* n_doc,
@@ -208,10 +228,44 @@ tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* cu_seqle
   a.k = k;
   a.batch = batch;
   a.max_n_doc = max_n_doc;
+  a.kept_capacity = INT64_MAX;
   a.kept_idx = kept_idx;
   a.cu_kept = cu_kept;
   a.status = di->status;
   cudaError_t e = launch_topk(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "top-K kernel launch");
+  return ok();
+}
+
+tg_status tg_topk_select_masked(const float* s, int64_t n_rows, const int32_t* cu_seqlens, const uint8_t* prunable,
+                                const int32_t* k, int32_t batch, int32_t max_len, int64_t kept_capacity,
+                                int32_t* kept_idx, int32_t* cu_kept, int32_t* n_prunable, cudaStream_t stream) {
+  if (batch < 0 || batch > (1 << 24)) return fail(TG_ERR_INVALID_ARG, "batch out of range");
+  if (n_rows < 0 || n_rows > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_rows out of range");
+  if (max_len < 0) return fail(TG_ERR_INVALID_ARG, "max_len must be >= 0");
+  if (kept_capacity < 0) return fail(TG_ERR_INVALID_ARG, "kept_capacity must be >= 0");
+  if (batch == 0) return ok();
+  if (!cu_seqlens || !k || !cu_kept || !n_prunable) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (n_rows > 0 && (!s || !prunable || (kept_capacity > 0 && !kept_idx)))
+    return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+  cudaError_t e = launch_topk_count(prunable, cu_seqlens, batch, n_prunable, di->status, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prunable count kernel launch");
+  TopkArgs a{};
+  a.s = s;
+  a.cu_seqlens = cu_seqlens;
+  a.n_doc = n_prunable;
+  a.prunable = prunable;
+  a.k = k;
+  a.batch = batch;
+  a.max_n_doc = max_len;
+  a.kept_capacity = kept_capacity;
+  a.kept_idx = kept_idx;
+  a.cu_kept = cu_kept;
+  a.status = di->status;
+  e = launch_topk(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "top-K kernel launch");
   return ok();
 }

@@ -7,7 +7,8 @@
 //    CTAs takes 256 residual rows at a time; the pair's tensor cores compute
 //    U = X W1^T (256 x h, fp32 in TMEM) and the epilogue fuses + b1,
 //    exact-erf GELU, the 1-wide projection with w2, + b2 and logsigmoid,
-//    writing one fp32 score per row (0 for question rows).
+//    writing one fp32 score per prunable row (document rows, or the rows of a
+//    per-row mask) and 0 for every other row.
 //  * linear_kernel -- out = A W^T (+ residual) in bf16, the per-layer Q/K/V and
 //    output projections of the stacked long-context workload, 256 x 256 tiles.
 //
@@ -322,7 +323,8 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
         z += a.b2;
         // logsigmoid(z) = -log1p(exp(-z)) (z >= 0), z - log1p(exp(z)) (z < 0)
         const float sc = (z >= 0.0f) ? -log1pf(expf(-z)) : z - log1pf(expf(z));
-        a.s_out[row] = row_is_doc(a, row) ? sc : 0.0f;
+        const bool prun = a.prunable ? __ldg(a.prunable + row) != 0 : row_is_doc(a, row);
+        a.s_out[row] = prun ? sc : 0.0f;
       }
     }
   }

@@ -24,6 +24,7 @@ struct RopeFreqs {
 
 // ---- gate ------------------------------------------------------------------
 struct GateArgs {
+  const uint8_t* prunable;  // [n_rows] per-row mask, or null: the document prefix (n_doc)
   const float* b1;          // [h] or null
   const __nv_bfloat16* w2;  // [h]
   float b2;
@@ -45,15 +46,24 @@ cudaError_t launch_gate(const CUtensorMap& map_x, const CUtensorMap& map_w1, con
 struct TopkArgs {
   const float* s;
   const int32_t* cu_seqlens;
+  // Prunable rows of each sequence: with `prunable` null, the first n_doc[b]
+  // rows (the document) and the rest (the question) always kept; with a
+  // per-row mask, the masked rows, n_doc[b] of them (counted by
+  // launch_topk_count first), anywhere in the sequence.
   const int32_t* n_doc;
+  const uint8_t* prunable;
   const int32_t* k;
   int32_t batch;
-  int32_t max_n_doc;
+  int32_t max_n_doc;        // host bound on the rows a sequence's slices cover
+  int64_t kept_capacity;    // length of kept_idx
   int32_t* kept_idx;
   int32_t* cu_kept;
   unsigned int* status;
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
+// n_prun[b] = number of prunable rows of sequence b
+cudaError_t launch_topk_count(const uint8_t* prunable, const int32_t* cu_seqlens, int32_t batch,
+                              int32_t* n_prun, unsigned int* status, cudaStream_t st);
 
 // ---- gather ----------------------------------------------------------------
 struct GatherArgs {

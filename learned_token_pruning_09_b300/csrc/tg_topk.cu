@@ -12,6 +12,13 @@
 // equal to it that are taken (lowest row index first).  A final ordered
 // compaction (warp ballots + prefix sums, slice offsets exchanged across the
 // cluster) writes the kept rows in ascending order, then the question rows.
+//
+// General prunable spans (a per-row mask instead of a document prefix): the
+// slices cover the whole sequence; a row outside the mask gets the key
+// 0xFFFFFFFF, which no score maps to (NaN maps to 0, +inf to 0xFF800000), so
+// it stays out of every histogram, ranks above the K-th key and is kept by
+// the same ordered compaction, in its place in row order.  The number of
+// prunable rows of each sequence comes from a counting kernel run first.
 #include <cooperative_groups.h>
 
 #include "tg_common.cuh"
@@ -25,6 +32,8 @@ constexpr int kTopkClusterPortable = 8;
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkMaxSmemKeys = (200 * 1024) / 4;
+constexpr uint32_t kFixedKey = 0xFFFFFFFFu;   // a row outside the prunable mask
+constexpr uint32_t kNoneKey = 0xFFFFFFFEu;    // "K-th key" when no prunable row is kept
 
 // Monotone map float -> uint32: a larger key means a larger score.  -0.0 is
 // folded onto +0.0 (so the two tie and the lower index wins), every NaN maps
@@ -49,7 +58,7 @@ struct TopkShared {
   long long base;           // first output slot of this sequence
 };
 
-template <bool kSmemKeys>
+template <bool kSmemKeys, bool kMasked>
 __global__ void __launch_bounds__(kTopkThreads, 1)
 topk_kernel(TopkArgs a) {
   extern __shared__ __align__(16) uint32_t keys_smem[];
@@ -67,7 +76,7 @@ topk_kernel(TopkArgs a) {
   const int nd = a.n_doc[b];
   const int kb = a.k[b];
   // every CTA of the cluster sees the same values, so all leave together
-  if (hi < lo || nd < 0 || nd > hi - lo || nd > a.max_n_doc || kb < 0) {
+  if (hi < lo || nd < 0 || nd > hi - lo || (kMasked ? hi - lo : nd) > a.max_n_doc || kb < 0) {
     if (rank == 0 && tid == 0) record_error(a.status, kStatusIndex);
     return;
   }
@@ -89,60 +98,72 @@ topk_kernel(TopkArgs a) {
   }
   __syncthreads();
   const long long base = sh.base;
+  if (base + ke + nq > a.kept_capacity) {   // the same verdict in every CTA of the cluster
+    if (rank == 0 && tid == 0) record_error(a.status, kStatusIndex);
+    return;
+  }
   if (rank == 0 && tid == 0) {
     a.cu_kept[b + 1] = static_cast<int32_t>(base + ke + nq);
     if (b == 0) a.cu_kept[0] = 0;
   }
-  // question rows, spread over the cluster
-  for (int t = rank * kTopkThreads + tid; t < nq; t += kTopkCluster * kTopkThreads)
-    a.kept_idx[base + ke + t] = lo + nd + t;
+  // question rows, spread over the cluster (with a mask they are placed by
+  // the compaction)
+  if (!kMasked)
+    for (int t = rank * kTopkThreads + tid; t < nq; t += kTopkCluster * kTopkThreads)
+      a.kept_idx[base + ke + t] = lo + nd + t;
 
-  // this CTA's slice of the document
-  const int chunk = (nd + kTopkCluster - 1) / kTopkCluster;
-  const int s0 = min(nd, rank * chunk);
-  const int n_loc = min(nd, s0 + chunk) - s0;
+  // this CTA's slice of the document (of the whole sequence with a mask)
+  const int span = kMasked ? hi - lo : nd;
+  const int chunk = (span + kTopkCluster - 1) / kTopkCluster;
+  const int s0 = min(span, rank * chunk);
+  const int n_loc = min(span, s0 + chunk) - s0;
   const float* src = a.s + lo + s0;
+  const uint8_t* msk = kMasked ? a.prunable + lo + s0 : nullptr;
   int32_t* out = a.kept_idx + base;
 
-  if (ke == nd) {             // whole document kept (also nd == 0)
+  if (ke == nd) {             // every prunable row kept, so every row (also nd == 0)
     for (int i = tid; i < n_loc; i += kTopkThreads) out[s0 + i] = lo + s0 + i;
     return;
   }
-  if (ke == 0) return;        // question only
+  if (!kMasked && ke == 0) return;   // question only
+  const bool none = kMasked && ke == 0;   // only the rows outside the mask
 
   if (kSmemKeys) {
     // eight loads in flight per thread before any is used (the scores were
     // just written and sit in L2; one at a time would serialise its latency)
     for (int i0 = tid; i0 < n_loc; i0 += 8 * kTopkThreads) {
       float v[8];
+      uint8_t m[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int i = i0 + u * kTopkThreads;
         v[u] = i < n_loc ? __ldg(src + i) : 0.0f;
+        m[u] = (kMasked && i < n_loc) ? __ldg(msk + i) : 1;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int i = i0 + u * kTopkThreads;
-        if (i < n_loc) keys_smem[i] = order_key(v[u]);
+        if (i < n_loc) keys_smem[i] = m[u] ? order_key(v[u]) : kFixedKey;
       }
     }
   }
   auto key_at = [&](int i) -> uint32_t {
     if (kSmemKeys) return keys_smem[i];
+    if (kMasked && __ldg(msk + i) == 0) return kFixedKey;
     return order_key(__ldg(src + i));
   };
 
   // ---- radix select, 4 passes of 8 bits --------------------------------
   uint32_t prefix = 0, mask = 0;
   int remaining = ke;
-  for (int pass = 0; pass < 4; ++pass) {
+  for (int pass = 0; pass < (none ? 0 : 4); ++pass) {
     const int shift = 24 - 8 * pass;
     uint32_t* h = sh.hist[pass & 1];
     if (tid < 256) h[tid] = 0;
     __syncthreads();
     for (int i = tid; i < n_loc; i += kTopkThreads) {
       const uint32_t key = key_at(i);
-      if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
+      if ((!kMasked || key != kFixedKey) && (key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
     }
     cluster.sync();
     // bin tid summed over the cluster; inclusive suffix sums over bins
@@ -180,8 +201,8 @@ topk_kernel(TopkArgs a) {
     mask |= 255u << shift;
     remaining = sh.remaining;
   }
-  const uint32_t kth = prefix;     // exact K-th largest key
-  const int take_eq = remaining;   // keys equal to kth that are kept
+  const uint32_t kth = none ? kNoneKey : prefix;   // exact K-th largest key
+  const int take_eq = none ? 0 : remaining;         // keys equal to kth that are kept
 
   // ---- ordered compaction ---------------------------------------------
   const int seg = ((n_loc + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
@@ -236,15 +257,15 @@ topk_kernel(TopkArgs a) {
 }
 
 // Launch with `csize` CTAs per cluster; returns the launch error.
-template <bool kSmemKeys>
+template <bool kSmemKeys, bool kMasked>
 static cudaError_t launch_topk_cluster(const TopkArgs& a, int csize, cudaStream_t st) {
+  auto kernel = topk_kernel<kSmemKeys, kMasked>;
   const int chunk = (a.max_n_doc + csize - 1) / csize;
   const size_t smem = kSmemKeys ? static_cast<size_t>(max(chunk, 4)) * sizeof(uint32_t) : 0;
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel<kSmemKeys>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (csize > kTopkClusterPortable) {
-    e = cudaFuncSetAttribute(topk_kernel<kSmemKeys>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -261,24 +282,90 @@ static cudaError_t launch_topk_cluster(const TopkArgs& a, int csize, cudaStream_
   cfg.numAttrs = 1;
   // a cluster size the device cannot co-schedule is refused here, not at run time
   int n_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&n_clusters, topk_kernel<kSmemKeys>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n_clusters, kernel, &cfg);
   if (e != cudaSuccess) return e;
   if (n_clusters < 1) return cudaErrorInvalidConfiguration;
-  return cudaLaunchKernelEx(&cfg, topk_kernel<kSmemKeys>, a);
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
-  if (a.batch == 0) return cudaSuccess;
+template <bool kMasked>
+static cudaError_t launch_topk_masked(const TopkArgs& a, cudaStream_t st) {
   // 16-CTA clusters halve the per-CTA slice when the device allows them
   for (int csize : {kTopkClusterMax, kTopkClusterPortable}) {
     const int chunk = (a.max_n_doc + csize - 1) / csize;
-    const cudaError_t e = chunk <= kTopkMaxSmemKeys ? launch_topk_cluster<true>(a, csize, st)
-                                                    : launch_topk_cluster<false>(a, csize, st);
+    const cudaError_t e = chunk <= kTopkMaxSmemKeys ? launch_topk_cluster<true, kMasked>(a, csize, st)
+                                                    : launch_topk_cluster<false, kMasked>(a, csize, st);
     if (e == cudaSuccess) return cudaSuccess;
     if (csize == kTopkClusterPortable) return e;
     (void)cudaGetLastError();   // clear the refusal of the larger cluster, try the portable size
   }
   return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
+  if (a.batch == 0) return cudaSuccess;
+  return a.prunable ? launch_topk_masked<true>(a, st) : launch_topk_masked<false>(a, st);
+}
+
+// ---------------------------------------------------------------------------
+// prunable rows per sequence (one block per sequence)
+// ---------------------------------------------------------------------------
+constexpr int kCountThreads = 1024;
+
+__global__ void __launch_bounds__(kCountThreads)
+topk_count_kernel(const uint8_t* __restrict__ prunable, const int32_t* __restrict__ cu_seqlens,
+                  int32_t* __restrict__ n_prun, unsigned int* status) {
+  __shared__ int part[kCountThreads / 32];
+  const int b = blockIdx.x;
+  const int lo = __ldg(cu_seqlens + b);
+  const int hi = __ldg(cu_seqlens + b + 1);
+  if (hi < lo) {
+    if (threadIdx.x == 0) { record_error(status, kStatusIndex); n_prun[b] = 0; }
+    return;
+  }
+  // the 16-byte aligned middle of the span as uint4 words, four in flight
+  // per thread; the unaligned head and tail byte by byte
+  const int head = static_cast<int>((16u - (reinterpret_cast<uintptr_t>(prunable + lo) & 15u)) & 15u);
+  const int a0 = min(hi, lo + head);                     // first 16-byte aligned row
+  const int a1 = a0 + (((hi - a0) >> 4) << 4);           // end of the whole words
+  int c = 0;
+  for (int i = lo + static_cast<int>(threadIdx.x); i < a0; i += kCountThreads) c += __ldg(prunable + i) != 0;
+  for (int i = a1 + static_cast<int>(threadIdx.x); i < hi; i += kCountThreads) c += __ldg(prunable + i) != 0;
+  const uint4* w = reinterpret_cast<const uint4*>(prunable + a0);
+  const int nw = (a1 - a0) >> 4;
+  auto nonzero_bytes = [](uint32_t x) {
+    // per byte: 1 when nonzero (x | x >> 1 | ... folds each byte's bits into its low bit)
+    x |= x >> 4;
+    x |= x >> 2;
+    x |= x >> 1;
+    return __popc(x & 0x01010101u);
+  };
+  for (int j0 = static_cast<int>(threadIdx.x); j0 < nw; j0 += 4 * kCountThreads) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * kCountThreads;
+      v[u] = j < nw ? __ldg(w + j) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      c += nonzero_bytes(v[u].x) + nonzero_bytes(v[u].y) + nonzero_bytes(v[u].z) + nonzero_bytes(v[u].w);
+  }
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_down_sync(0xffffffffu, c, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int t = part[threadIdx.x];
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
+    if (threadIdx.x == 0) n_prun[b] = t;
+  }
+}
+
+cudaError_t launch_topk_count(const uint8_t* prunable, const int32_t* cu_seqlens, int32_t batch,
+                              int32_t* n_prun, unsigned int* status, cudaStream_t st) {
+  if (batch == 0) return cudaSuccess;
+  topk_count_kernel<<<static_cast<unsigned>(batch), kCountThreads, 0, st>>>(prunable, cu_seqlens, n_prun, status);
+  return cudaGetLastError();
 }
 
 }  // namespace tg

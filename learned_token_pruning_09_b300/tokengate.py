@@ -50,6 +50,8 @@ _vp, _i64, _i32, _f32, _sz, _ll = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 _SIGS = {
     "tg_gate_score": [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _f32, _i32, _vp, _vp],
     "tg_topk_select": [_vp, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp],
+    "tg_gate_score_masked": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _f32, _i32, _vp, _vp],
+    "tg_topk_select_masked": [_vp, _i64, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
     "tg_gather_kept": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp],
     "tg_gated_attention_fwd": [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _i32, _i64, _i32, _i32, _i32,
                                _i32, _vp, _vp, _vp, _vp, _sz, _vp],
@@ -158,6 +160,57 @@ def tg_topk_select(s: torch.Tensor, cu_seqlens: torch.Tensor, n_doc: torch.Tenso
     _check(lib.tg_topk_select(_ptr(s), s.shape[0], _ptr(cu_seqlens), _ptr(n_doc), _ptr(k), batch,
                               int(max_n_doc), _ptr(kept_idx), _ptr(cu_kept), _stream(stream)), "tg_topk_select")
     return kept_idx, cu_kept
+
+
+def tg_gate_score_masked(x: torch.Tensor, prunable: torch.Tensor, w1: torch.Tensor, b1: Optional[torch.Tensor],
+                         w2: torch.Tensor, b2: float, s_out: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """Gate scores s [n_rows] fp32 on the rows of a per-row prunable mask
+    (uint8 [n_rows], nonzero = prunable), 0 on every other row."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(prunable, torch.uint8, "prunable", 1)
+    _need(w1, torch.bfloat16, "w1", 2)
+    _need(w2, torch.bfloat16, "w2", 1)
+    if b1 is not None:
+        _need(b1, torch.float32, "b1", 1)
+    n_rows, d = x.shape
+    h = w1.shape[0]
+    if w1.shape[1] != d or w2.shape[0] != h or prunable.shape[0] != n_rows:
+        raise ValueError("w1 must be [h, d], w2 [h] and prunable [n_rows]")
+    if s_out is None:
+        s_out = torch.empty(n_rows, dtype=torch.float32, device=x.device)
+    _need(s_out, torch.float32, "s_out", 1)
+    _check(lib.tg_gate_score_masked(_ptr(x), n_rows, d, _ptr(prunable), _ptr(w1), _ptr(b1), _ptr(w2), float(b2), h,
+                                    _ptr(s_out), _stream(stream)), "tg_gate_score_masked")
+    return s_out
+
+
+def tg_topk_select_masked(s: torch.Tensor, cu_seqlens: torch.Tensor, prunable: torch.Tensor, k: torch.Tensor,
+                          max_len: int, kept_capacity: Optional[int] = None, kept_idx: Optional[torch.Tensor] = None,
+                          cu_kept: Optional[torch.Tensor] = None, n_prunable: Optional[torch.Tensor] = None,
+                          stream=None):
+    """(kept_idx, cu_kept, n_prunable) with general prunable spans.  kept_idx
+    has ``kept_capacity`` entries (default n_rows); its first cu_kept[batch]
+    entries are the kept rows."""
+    _need(s, torch.float32, "s", 1)
+    _need(prunable, torch.uint8, "prunable", 1)
+    for t, nme in ((cu_seqlens, "cu_seqlens"), (k, "k")):
+        _need(t, torch.int32, nme, 1)
+    batch = k.shape[0]
+    n_rows = s.shape[0]
+    if prunable.shape[0] != n_rows:
+        raise ValueError("prunable must be [n_rows]")
+    if kept_idx is None:
+        cap = n_rows if kept_capacity is None else int(kept_capacity)
+        kept_idx = torch.empty(max(cap, 1), dtype=torch.int32, device=s.device)[:cap]
+    if cu_kept is None:
+        cu_kept = torch.empty(batch + 1, dtype=torch.int32, device=s.device)
+    if n_prunable is None:
+        n_prunable = torch.empty(batch, dtype=torch.int32, device=s.device)
+    _check(lib.tg_topk_select_masked(_ptr(s), n_rows, _ptr(cu_seqlens), _ptr(prunable), _ptr(k), batch,
+                                     int(max_len), kept_idx.shape[0], _ptr(kept_idx), _ptr(cu_kept),
+                                     _ptr(n_prunable), _stream(stream)), "tg_topk_select_masked")
+    return kept_idx, cu_kept, n_prunable
 
 
 def tg_gather_kept(x: Optional[torch.Tensor], s: Optional[torch.Tensor], cu_seqlens: torch.Tensor,
