@@ -27,6 +27,9 @@ the exact algebra that they leave open is taken as follows:
           o_i = sum_j p_ij v_j.  q' and k' carry rotate-half RoPE at the
           original positions, theta = 1e6; query head h reads KV head
           floor(h / G), G = hq / hkv.
+* attention backward (the gradient path from the attention loss to the gate):
+          for L = sum dO . o, the derivatives with respect to s_j, g_h and tau,
+          from dl_ij = p_ij (dO_i . v_j - sum_j' p_ij' dO_i . v_j').
 * stacked layer (long-context workload): qkv = x W_qkv^T, attention as above,
           x_out = x + o W_o^T.  No norm and no MLP.
 * general prunable spans (the prompt template marks the prunable document
@@ -56,6 +59,7 @@ __all__ = [
     "bf16_decode", "gelu", "logsigmoid", "gate_score", "score_from_logit",
     "topk_select", "gather_kept", "rope", "gated_attention",
     "stacked_layer", "project_qkv", "gate_score_masked", "topk_select_masked",
+    "gated_attention_bwd",
 ]
 
 
@@ -310,6 +314,73 @@ def gated_attention(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
             o[i, h, :] = (e / den) @ v[js, g, :]
             lse[h, i] = m + math.log(den)
     return o, lse
+
+
+def gated_attention_bwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
+                        pos: np.ndarray, s_kept: np.ndarray, gain: np.ndarray, tau: float,
+                        cu_kept: Sequence[int], do_bits: np.ndarray, theta: float = 1.0e6,
+                        q_is_f64: bool = False, block: int = 512):
+    """Gradient of L = sum_{i,h} dO_i,h . o_i,h with respect to the score-side
+    parameters of token-gated attention: the kept scores s, the per-head
+    gains and the temperature (the path from the attention loss back to the
+    gate, "What is token-gated attention?": the score enters the logits as
+    gain_h s_j, and the temperature divides q.k).
+
+    Same inputs as ``gated_attention`` plus dO [T, hq, D] (bf16 bits, or
+    float64 with ``q_is_f64``).  Per sequence and head h, with the logits
+    and P = softmax of ``gated_attention`` (rows over kept keys j with
+    pos_j <= pos_i):
+      dP_ij = dO_i . v_j,   D_i = sum_j P_ij dP_ij,   dl_ij = P_ij (dP_ij - D_i)
+      ds_j   += gain_h sum_i dl_ij
+      dgain_h = sum_ij s_j dl_ij
+      dtau   += sum_ij dl_ij * (-(q'_i . k'_j) / (sqrt(D) tau^2))
+    A key whose score is infinite has P = 0 in every row, and its s_j dl_ij
+    terms are taken as 0.  Query rows are taken ``block`` at a time (each row
+    is independent).  Returns (ds float64 [T], dgain float64 [hq], dtau)."""
+    dec = (lambda a: np.asarray(a, np.float64)) if q_is_f64 else bf16_decode
+    q, k, v, do = dec(q_bits), dec(k_bits), dec(v_bits), dec(do_bits)
+    t, hq, d = q.shape
+    hkv = k.shape[1]
+    group = hq // hkv
+    pos = np.asarray(pos, dtype=np.int64)
+    s_kept = np.asarray(s_kept, dtype=np.float64)
+    gain = np.asarray(gain, dtype=np.float64)
+    tau = float(tau)
+    qr = rope(q, pos, theta)
+    kr = rope(k, pos, theta)
+    ds = np.zeros(t)
+    dgain = np.zeros(hq)
+    dtau = 0.0
+    for b in range(len(cu_kept) - 1):
+        lo, hi = int(cu_kept[b]), int(cu_kept[b + 1])
+        if hi <= lo:
+            continue
+        ps = pos[lo:hi]
+        s_b = s_kept[lo:hi]
+        for h in range(hq):
+            g = h // group
+            kh, vh = kr[lo:hi, g, :], v[lo:hi, g, :]
+            col = np.zeros(hi - lo)          # sum_i dl_ij for this head
+            for r0 in range(lo, hi, block):
+                r1 = min(hi, r0 + block)
+                qk = qr[r0:r1, h, :] @ kh.T                          # [rows, keys]
+                logit = qk / (math.sqrt(d) * tau) + gain[h] * s_b[None, :]
+                visible = ps[None, :] <= pos[r0:r1, None]
+                logit = np.where(visible, logit, -np.inf)
+                m = logit.max(axis=1, keepdims=True)
+                m = np.where(np.isfinite(m), m, 0.0)
+                e = np.exp(logit - m)
+                den = e.sum(axis=1, keepdims=True)
+                p = np.divide(e, den, out=np.zeros_like(e), where=den > 0)
+                dp = do[r0:r1, h, :] @ vh.T
+                delta = (p * dp).sum(axis=1, keepdims=True)
+                dl = p * (dp - delta)
+                col += dl.sum(axis=0)
+                dtau += float((dl * (-qk / (math.sqrt(d) * tau * tau))).sum())
+            ds[lo:hi] += gain[h] * col
+            use = np.isfinite(s_b) & (col != 0.0)
+            dgain[h] += float((s_b[use] * col[use]).sum())
+    return ds, dgain, dtau
 
 
 # ---------------------------------------------------------------------------

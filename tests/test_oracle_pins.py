@@ -558,3 +558,144 @@ def test_stacked_layer_loops():
     xref = np.array([[x[i][r] + sum(flat[i][c] * Wo[r][c] for c in range(hq * dh))
                       for r in range(dm)] for i in range(t)])
     np.testing.assert_allclose(out, xref, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# attention backward with respect to s, gain and tau
+# ---------------------------------------------------------------------------
+
+
+def _bwd_case(seed, t=30, hq=4, hkv=2, d=16, cu=None):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((t, hq, d))
+    k = rng.standard_normal((t, hkv, d))
+    v = rng.standard_normal((t, hkv, d))
+    do = rng.standard_normal((t, hq, d))
+    pos = np.cumsum(rng.integers(1, 5, t))
+    s = -rng.uniform(0, 3, t)
+    gain = rng.uniform(0.5, 2.0, hq)
+    cu = [0, t] if cu is None else cu
+    return q, k, v, do, pos, s, gain, 1.15, cu
+
+
+def _loss(q, k, v, do, pos, s, gain, tau, cu):
+    o, _ = oracle.gated_attention(q, k, v, pos, s, gain, tau, cu, q_is_f64=True)
+    return float((o * do).sum())
+
+
+@pytest.mark.parametrize("seed,hq,hkv,shuffle", [(1, 4, 2, False), (2, 3, 3, False), (3, 4, 1, False),
+                                                 (4, 4, 2, True)])
+def test_attention_bwd_matches_central_differences(seed, hq, hkv, shuffle):
+    """The backward against central differences of the forward (itself
+    pinned to SDPA and brute force): every ds_j, every dgain_h and dtau;
+    once with positions out of row order, so that the mask is on positions."""
+    q, k, v, do, pos, s, gain, tau, cu = _bwd_case(seed, t=14, hq=hq, hkv=hkv, d=8, cu=[0, 6, 14])
+    if shuffle:
+        pos = np.random.default_rng(seed).permutation(pos)
+    ds, dg, dtau = oracle.gated_attention_bwd(q, k, v, pos, s, gain, tau, cu, do, q_is_f64=True)
+    eps = 1e-6
+    for j in range(len(s)):
+        sp, sm = s.copy(), s.copy()
+        sp[j] += eps
+        sm[j] -= eps
+        fd = (_loss(q, k, v, do, pos, sp, gain, tau, cu) - _loss(q, k, v, do, pos, sm, gain, tau, cu)) / (2 * eps)
+        assert abs(fd - ds[j]) < 1e-7 * max(1.0, abs(fd)), (j, fd, ds[j])
+    for h in range(hq):
+        gp, gm = gain.copy(), gain.copy()
+        gp[h] += eps
+        gm[h] -= eps
+        fd = (_loss(q, k, v, do, pos, s, gp, tau, cu) - _loss(q, k, v, do, pos, s, gm, tau, cu)) / (2 * eps)
+        assert abs(fd - dg[h]) < 1e-7 * max(1.0, abs(fd)), (h, fd, dg[h])
+    fd = (_loss(q, k, v, do, pos, s, gain, tau + eps, cu) - _loss(q, k, v, do, pos, s, gain, tau - eps, cu)) / (2 * eps)
+    assert abs(fd - dtau) < 1e-7 * max(1.0, abs(fd))
+
+
+def test_attention_bwd_matches_sdpa_autograd():
+    """torch autograd through float64 scaled_dot_product_attention with the
+    bias g_h s_j and the causal mask as an additive mask, and 1/tau folded
+    into the queries."""
+    q, k, v, do, pos, s, gain, tau, cu = _bwd_case(7, t=33, hq=6, hkv=2, d=16)
+    ds, dg, dtau = oracle.gated_attention_bwd(q, k, v, pos, s, gain, tau, cu, do, q_is_f64=True)
+    qr = torch.from_numpy(_rope_complex(q, pos, 1e6)).permute(1, 0, 2)
+    kr = torch.from_numpy(_rope_complex(k, pos, 1e6)).permute(1, 0, 2).repeat_interleave(3, dim=0)
+    vv = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(3, dim=0)
+    st = torch.tensor(s, requires_grad=True)
+    gt = torch.tensor(gain, requires_grad=True)
+    tt = torch.tensor(tau, dtype=torch.float64, requires_grad=True)
+    pt = torch.from_numpy(pos)
+    causal = torch.where(pt[None, :] <= pt[:, None], 0.0, -math.inf).to(torch.float64)
+    mask = gt[:, None, None] * st[None, None, :] + causal[None]
+    o = torch.nn.functional.scaled_dot_product_attention(qr / tt, kr, vv, attn_mask=mask,
+                                                         scale=1.0 / math.sqrt(q.shape[-1]))
+    loss = (o.permute(1, 0, 2) * torch.from_numpy(do)).sum()
+    loss.backward()
+    np.testing.assert_allclose(ds, st.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dg, gt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    assert abs(dtau - float(tt.grad)) < 1e-10 * max(1.0, abs(dtau))
+
+
+def test_attention_bwd_two_key_closed_form():
+    """One head, two tokens: row 0 sees only itself (p = 1, nothing to
+    differentiate); row 1 sees both with p = sigmoid(l1 - l0), so
+    dL/dl1 = p0 p1 (a1 - a0), a_j = dO_1 . v_j, dL/dl0 = -dL/dl1."""
+    rng = np.random.default_rng(11)
+    d = 4
+    q, k, v, do = (rng.standard_normal((2, 1, d)) for _ in range(4))
+    pos = np.array([0, 1])
+    s = np.array([-0.7, -1.9])
+    g, tau = 1.3, 0.8
+    ds, dg, dtau = oracle.gated_attention_bwd(q, k, v, pos, s, np.array([g]), tau, [0, 2], do, q_is_f64=True)
+    qr = oracle.rope(q, pos)
+    kr = oracle.rope(k, pos)
+    qk = np.array([qr[1, 0] @ kr[0, 0], qr[1, 0] @ kr[1, 0]])
+    l = qk / (math.sqrt(d) * tau) + g * s
+    p1 = 1.0 / (1.0 + math.exp(l[0] - l[1]))
+    p0 = 1.0 - p1
+    a = np.array([do[1, 0] @ v[0, 0], do[1, 0] @ v[1, 0]])
+    dl1 = p0 * p1 * (a[1] - a[0])
+    np.testing.assert_allclose(ds, [-g * dl1, g * dl1], rtol=1e-12)
+    np.testing.assert_allclose(dg, [s[1] * dl1 - s[0] * dl1], rtol=1e-12)
+    np.testing.assert_allclose(dtau, -(qk[1] * dl1 - qk[0] * dl1) / (math.sqrt(d) * tau * tau), rtol=1e-12)
+
+
+def test_attention_bwd_invariants():
+    q, k, v, do, pos, s, gain, tau, cu = _bwd_case(5, t=40, cu=[0, 17, 17, 40])
+    ds, dg, dtau = oracle.gated_attention_bwd(q, k, v, pos, s, gain, tau, cu, do, q_is_f64=True)
+    # softmax is shift-invariant: the ds of a sequence sum to zero
+    for b in range(len(cu) - 1):
+        assert abs(ds[cu[b]:cu[b + 1]].sum()) < 1e-12 * max(1.0, np.abs(ds).max())
+    # a score that is constant over every sequence leaves the gains without gradient
+    _, dg_c, _ = oracle.gated_attention_bwd(q, k, v, pos, np.full(40, -1.3), gain, tau, cu, do, q_is_f64=True)
+    np.testing.assert_allclose(dg_c, 0.0, atol=1e-12)
+    # q = 0: the logits do not depend on tau
+    _, _, dtau0 = oracle.gated_attention_bwd(np.zeros_like(q), k, v, pos, s, gain, tau, cu, do, q_is_f64=True)
+    assert dtau0 == 0.0
+    # varlen equals separate calls
+    for b in range(len(cu) - 1):
+        lo, hi = cu[b], cu[b + 1]
+        if hi == lo:
+            continue
+        dsb, _, _ = oracle.gated_attention_bwd(q[lo:hi], k[lo:hi], v[lo:hi], pos[lo:hi], s[lo:hi], gain, tau,
+                                               [0, hi - lo], do[lo:hi], q_is_f64=True)
+        np.testing.assert_allclose(ds[lo:hi], dsb, rtol=1e-12, atol=1e-14)
+    # the loss is linear in dO
+    ds2, dg2, dtau2 = oracle.gated_attention_bwd(q, k, v, pos, s, gain, tau, cu, 2.5 * do, q_is_f64=True)
+    np.testing.assert_allclose(ds2, 2.5 * ds, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dg2, 2.5 * dg, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_bwd_infinite_score_removes_the_key():
+    """A key with score -inf is invisible for positive gains: its ds is 0 and
+    every other gradient equals the one with that key deleted."""
+    q, k, v, do, pos, s, gain, tau, cu = _bwd_case(9, t=20)
+    do[7] = 0.0                  # row 7 itself adds no loss term, so it can be deleted
+    s2 = s.copy()
+    s2[7] = -np.inf
+    ds, dg, dtau = oracle.gated_attention_bwd(q, k, v, pos, s2, gain, tau, cu, do, q_is_f64=True)
+    keep = np.array([j for j in range(20) if j != 7])
+    dsr, dgr, dtaur = oracle.gated_attention_bwd(q[keep], k[keep], v[keep], pos[keep], s[keep], gain, tau,
+                                                 [0, 19], do[keep], q_is_f64=True)
+    assert ds[7] == 0.0
+    np.testing.assert_allclose(ds[keep], dsr, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dg, dgr, rtol=1e-10, atol=1e-12)
+    assert abs(dtau - dtaur) < 1e-10 * max(1.0, abs(dtau))
