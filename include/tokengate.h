@@ -242,6 +242,51 @@ TG_API size_t tg_attention_workspace_size(int64_t n_kept, int32_t hq, int32_t hk
                                    int32_t head_dim, int32_t has_k_cache);
 
 /*
+ * Backward of token-gated attention with respect to the score-side parameters
+ * (the gradient path from the attention loss back to the gate: section "What
+ * is token-gated attention?" makes the kept score a bias g_h s_j on the
+ * logits, with a learnable gain per head and a learnable temperature).  For
+ * the loss L = sum_{i,h} dO[i,h,:] . o[i,h,:] it writes
+ *   d_s[j]    = dL/ds_j  = sum_h gain_h sum_i dl_ij
+ *   d_gain[h] = dL/dg_h  = sum_{i,j} s_j dl_ij
+ *   d_tau[0]  = dL/dtau  = -sum_{h,i,j} dl_ij (q'_i . k'_j) / (sqrt(D) tau^2)
+ * with P = softmax of the forward's logits, dP_ij = dO_i . v_j, D_i = dO_i . o_i
+ * and dl_ij = P_ij (dP_ij - D_i).  dq, dk and dv are not computed.  A key
+ * whose score is -inf has P = 0 and adds nothing to d_gain.
+ *
+ *   q_rot [n_kept, hq, head_dim], k_rot [n_kept, hkv, head_dim] bf16: the
+ *            rotated q' and k' the forward used (tg_rope_qk's outputs; k_rot
+ *            is the kept-only K cache)
+ *   v [n_kept, hkv, head_dim] bf16;  o [n_kept, hq, head_dim] bf16 and
+ *   lse [hq, n_kept] fp32: the forward's outputs (tg_gated_attention_rotated)
+ *   d_o [n_kept, hq, head_dim] bf16: the upstream gradient dL/do
+ *   pos_kept, s_kept, gain, tau, cu_kept, batch, n_kept, max_kept, hq, hkv,
+ *            head_dim: as for the forward; hq / hkv <= 8; positions strictly
+ *            increasing within each sequence (the forward checks it)
+ *   d_s [n_kept], d_gain [hq], d_tau [1]: fp32 device outputs (d_s is 0 for
+ *            rows outside every sequence)
+ *   workspace of at least tg_attention_bwd_workspace_size(n_kept, hq) bytes,
+ *            256-byte aligned
+ * All pointers are caller-owned device memory; q_rot, k_rot, v, o and d_o
+ * 16-byte aligned.  A sequence longer than max_kept sets TG_ERR_DEVICE_INDEX.
+ * The result is deterministic (fixed reduction order).  Precision: P is
+ * recomputed in fp32 from the bf16 q', k' (as in the forward); D_i uses the
+ * bf16 o; all sums are fp32.
+ */
+TG_API tg_status tg_gated_attention_bwd(const void* q_rot, const void* k_rot, const void* v,
+                                 const void* o, const float* lse, const void* d_o,
+                                 const int32_t* pos_kept, const float* s_kept,
+                                 const float* gain, float tau, const int32_t* cu_kept,
+                                 int32_t batch, int64_t n_kept, int32_t max_kept,
+                                 int32_t hq, int32_t hkv, int32_t head_dim,
+                                 float* d_s, float* d_gain, float* d_tau,
+                                 void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/* Bytes of workspace tg_gated_attention_bwd needs.  Host-only, no CUDA call. */
+TG_API size_t tg_attention_bwd_workspace_size(int64_t n_kept, int32_t hq);
+
+/*
  * Dense projection for the layers above the gate (long-context workload: a
  * stack of token-gated attention layers, each with its own Q/K/V/O
  * projections):  out[m, n] = sum_k a[m, k] * w[n, k]  (+ residual[m, n])

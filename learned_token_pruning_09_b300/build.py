@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libtokengate.so")
-SOURCES = ["tg_api.cu", "tg_gemm.cu", "tg_topk.cu", "tg_gather.cu", "tg_rope.cu", "tg_attention.cu"]
+SOURCES = ["tg_api.cu", "tg_gemm.cu", "tg_topk.cu", "tg_gather.cu", "tg_rope.cu", "tg_attention.cu",
+           "tg_attention_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

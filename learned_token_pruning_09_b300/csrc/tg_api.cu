@@ -424,6 +424,80 @@ tg_status tg_gated_attention_fwd(const void* q, const void* k, const void* v, co
                                     hq, hkv, head_dim, o, lse, stream);
 }
 
+size_t tg_attention_bwd_workspace_size(int64_t n_kept, int32_t hq) {
+  if (n_kept <= 0 || hq <= 0) return 0;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t plane = static_cast<size_t>(n_kept) * hq * 4;
+  return up(plane) + 2 * up(2 * plane) + up(static_cast<size_t>(hq) * 4);
+}
+
+tg_status tg_gated_attention_bwd(const void* q_rot, const void* k_rot, const void* v, const void* o,
+                                 const float* lse, const void* d_o, const int32_t* pos_kept, const float* s_kept,
+                                 const float* gain, float tau, const int32_t* cu_kept, int32_t batch,
+                                 int64_t n_kept, int32_t max_kept, int32_t hq, int32_t hkv, int32_t head_dim,
+                                 float* d_s, float* d_gain, float* d_tau, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+  tg_status st = check_attention_shape(batch, n_kept, hq, hkv, head_dim, cu_kept);
+  if (st != TG_OK) return st;
+  if (hq / hkv > kBwdMaxGroup) return fail(TG_ERR_UNSUPPORTED, "hq / hkv must be at most %d", kBwdMaxGroup);
+  if (max_kept < 0) return fail(TG_ERR_INVALID_ARG, "max_kept must be >= 0");
+  if (!(tau > 0.0f) || !std::isfinite(tau)) return fail(TG_ERR_INVALID_ARG, "tau must be positive and finite");
+  if (!d_gain || !d_tau || (n_kept > 0 && !d_s)) return fail(TG_ERR_INVALID_ARG, "null output pointer");
+  if (n_kept == 0 || max_kept == 0) {
+    // no sequence holds a row: every gradient is zero
+    cudaError_t e = cudaMemsetAsync(d_gain, 0, static_cast<size_t>(hq) * 4, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_tau, 0, 4, stream);
+    if (e == cudaSuccess && n_kept > 0) e = cudaMemsetAsync(d_s, 0, static_cast<size_t>(n_kept) * 4, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    return ok();
+  }
+  if (!q_rot || !k_rot || !v || !o || !lse || !d_o || !pos_kept || !s_kept || !gain)
+    return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q_rot) || !aligned16(k_rot) || !aligned16(v) || !aligned16(o) || !aligned16(d_o))
+    return fail(TG_ERR_INVALID_ARG, "q_rot, k_rot, v, o and d_o must be 16-byte aligned");
+  const size_t need = tg_attention_bwd_workspace_size(n_kept, hq);
+  if (!workspace || workspace_bytes < need)
+    return fail(TG_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(TG_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  DeviceInfo* di = nullptr;
+  st = device_info(&di);
+  if (st != TG_OK) return st;
+  // 2D views [n_kept rows, heads * head_dim columns]; a box is 64 columns of
+  // one head by 128 keys (K, V) or 64 query rows (q', dO)
+  CUtensorMap mq, mk, mv, mdo;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(hq) * head_dim, static_cast<uint64_t>(n_kept)};
+    const uint64_t str[1] = {static_cast<uint64_t>(hq) * head_dim * 2};
+    const uint32_t box[2] = {64, 64};
+    if ((st = make_map(&mq, q_rot, 2, dims, str, box, "q'")) != TG_OK) return st;
+    if ((st = make_map(&mdo, d_o, 2, dims, str, box, "dO")) != TG_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(hkv) * head_dim, static_cast<uint64_t>(n_kept)};
+    const uint64_t str[1] = {static_cast<uint64_t>(hkv) * head_dim * 2};
+    const uint32_t box[2] = {64, 128};
+    if ((st = make_map(&mk, k_rot, 2, dims, str, box, "k'")) != TG_OK) return st;
+    if ((st = make_map(&mv, v, 2, dims, str, box, "v")) != TG_OK) return st;
+  }
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t plane = static_cast<size_t>(n_kept) * hq * 4;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  AttnBwdArgs a{};
+  a.o = o; a.d_o = d_o; a.lse = lse; a.pos = pos_kept; a.s_kept = s_kept; a.gain = gain; a.cu_kept = cu_kept;
+  a.batch = batch; a.n_kept = n_kept; a.max_kept = max_kept; a.hq = hq; a.hkv = hkv; a.head_dim = head_dim;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / (std::sqrt(static_cast<double>(head_dim)) * tau));
+  a.dtau_scale = static_cast<float>(-1.0 / (std::sqrt(static_cast<double>(head_dim)) * static_cast<double>(tau) * tau));
+  a.delta = reinterpret_cast<float*>(ws);
+  a.r_part = reinterpret_cast<float*>(ws + up(plane));
+  a.t_part = reinterpret_cast<float*>(ws + up(plane) + up(2 * plane));
+  a.tsum = reinterpret_cast<float*>(ws + up(plane) + 2 * up(2 * plane));
+  a.ds = d_s; a.dgain = d_gain; a.dtau = d_tau;
+  a.status = di->status; a.watchdog = g_watchdog_cycles; a.num_sms = di->num_sms;
+  const cudaError_t e = launch_attention_bwd(mq, mk, mv, mdo, a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "attention backward launch");
+  return ok();
+}
+
 tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual, void* out, int64_t m, int32_t n,
                          int32_t kdim, cudaStream_t stream) {
   if (m < 0 || m > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "m out of range");

@@ -119,6 +119,36 @@ struct AttnArgs {
 cudaError_t launch_attention(const CUtensorMap& map_q, const CUtensorMap& map_k,
                              const CUtensorMap& map_v, const AttnArgs& a, cudaStream_t st);
 
+// ---- attention backward: gradients of the score, gain and temperature ------
+constexpr int kBwdMaxGroup = 8;   // query heads per KV head
+struct AttnBwdArgs {
+  const void* o;          // [T, hq, D] bf16, the forward output
+  const void* d_o;        // [T, hq, D] bf16
+  const float* lse;       // [hq, T] natural log, from the forward
+  const int32_t* pos;
+  const float* s_kept;
+  const float* gain;
+  const int32_t* cu_kept;
+  int32_t batch;
+  int64_t n_kept;
+  int32_t max_kept;
+  int32_t hq, hkv, head_dim;
+  float scale_log2;       // log2(e) / (sqrt(D) tau)
+  float dtau_scale;       // -1 / (sqrt(D) tau^2)
+  float* delta;           // [hq, T] workspace: dO_i . o_i
+  float* r_part;          // [2, hq, T] workspace: sum_i dl_ij, per softmax warpgroup
+  float* t_part;          // [2, hq, T] workspace: sum_i dl_ij (q'_i . k'_j), per warpgroup
+  float* tsum;            // [hq] workspace
+  float* ds;              // [T]
+  float* dgain;           // [hq]
+  float* dtau;            // [1]
+  unsigned int* status;
+  long long watchdog;
+  int num_sms;
+};
+cudaError_t launch_attention_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
+                                 const CUtensorMap& map_do, const AttnBwdArgs& a, cudaStream_t st);
+
 // ---- linear ----------------------------------------------------------------
 struct LinearArgs {
   const void* residual;

@@ -59,6 +59,9 @@ _SIGS = {
     "tg_gated_attention_rotated": [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
                                    _vp, _vp, _vp],
     "tg_attention_workspace_size": [_i64, _i32, _i32, _i32, _i32],
+    "tg_gated_attention_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _i64, _i32, _i32,
+                               _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp],
+    "tg_attention_bwd_workspace_size": [_i64, _i32],
     "tg_linear_bf16": [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp],
     "tg_check_device_status": [_vp],
     "tg_set_watchdog_cycles": [_ll],
@@ -70,6 +73,7 @@ for _name, _args in _SIGS.items():
     _f.argtypes = _args
     _f.restype = ctypes.c_int
 lib.tg_attention_workspace_size.restype = ctypes.c_size_t
+lib.tg_attention_bwd_workspace_size.restype = ctypes.c_size_t
 lib.tg_last_error_string.restype = ctypes.c_char_p
 lib.tg_version.restype = ctypes.c_char_p
 lib.tg_set_watchdog_cycles.restype = None
@@ -287,6 +291,49 @@ def tg_gated_attention_rotated(q_rot: torch.Tensor, k_rot: torch.Tensor, v: torc
                                           int(max_kept), hq, hkv, dh, _ptr(o), _ptr(lse), _stream(stream)),
            "tg_gated_attention_rotated")
     return (o, lse) if lse is not None else o
+
+
+def tg_gated_attention_bwd(q_rot: torch.Tensor, k_rot: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                           lse: torch.Tensor, d_o: torch.Tensor, pos_kept: torch.Tensor, s_kept: torch.Tensor,
+                           gain: torch.Tensor, tau: float, cu_kept: torch.Tensor, max_kept: int,
+                           d_s: Optional[torch.Tensor] = None, d_gain: Optional[torch.Tensor] = None,
+                           d_tau: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                           stream=None):
+    """(d_s [T], d_gain [hq], d_tau [1]) fp32: gradients of sum(d_o * o) with
+    respect to the kept scores, the gains and the temperature, from the
+    forward's q', k', v, o and lse."""
+    _need(q_rot, torch.bfloat16, "q_rot", 3)
+    _need(k_rot, torch.bfloat16, "k_rot", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    _need(o, torch.bfloat16, "o", 3)
+    _need(d_o, torch.bfloat16, "d_o", 3)
+    _need(lse, torch.float32, "lse", 2)
+    _need(pos_kept, torch.int32, "pos_kept", 1)
+    _need(s_kept, torch.float32, "s_kept", 1)
+    _need(gain, torch.float32, "gain", 1)
+    _need(cu_kept, torch.int32, "cu_kept", 1)
+    t, hq, dh = q_rot.shape
+    hkv = k_rot.shape[1]
+    if k_rot.shape != (t, hkv, dh) or v.shape != (t, hkv, dh):
+        raise ValueError("k_rot and v must be [T, hkv, D] matching q_rot")
+    if o.shape != q_rot.shape or d_o.shape != q_rot.shape or lse.shape != (hq, t):
+        raise ValueError("o and d_o must be [T, hq, D] and lse [hq, T]")
+    dev = q_rot.device
+    if d_s is None:
+        d_s = torch.empty(t, dtype=torch.float32, device=dev)
+    if d_gain is None:
+        d_gain = torch.empty(hq, dtype=torch.float32, device=dev)
+    if d_tau is None:
+        d_tau = torch.empty(1, dtype=torch.float32, device=dev)
+    need = lib.tg_attention_bwd_workspace_size(t, hq)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(lib.tg_gated_attention_bwd(_ptr(q_rot), _ptr(k_rot), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                                      _ptr(pos_kept), _ptr(s_kept), _ptr(gain), float(tau), _ptr(cu_kept),
+                                      cu_kept.shape[0] - 1, t, int(max_kept), hq, hkv, dh, _ptr(d_s), _ptr(d_gain),
+                                      _ptr(d_tau), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "tg_gated_attention_bwd")
+    return d_s, d_gain, d_tau
 
 
 def tg_gated_attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pos_kept: torch.Tensor,

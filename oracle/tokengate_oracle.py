@@ -319,7 +319,7 @@ def gated_attention(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
 def gated_attention_bwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
                         pos: np.ndarray, s_kept: np.ndarray, gain: np.ndarray, tau: float,
                         cu_kept: Sequence[int], do_bits: np.ndarray, theta: float = 1.0e6,
-                        q_is_f64: bool = False, block: int = 512):
+                        q_is_f64: bool = False, block: int = 512, scales: bool = False):
     """Gradient of L = sum_{i,h} dO_i,h . o_i,h with respect to the score-side
     parameters of token-gated attention: the kept scores s, the per-head
     gains and the temperature (the path from the attention loss back to the
@@ -336,7 +336,12 @@ def gated_attention_bwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarr
       dtau   += sum_ij dl_ij * (-(q'_i . k'_j) / (sqrt(D) tau^2))
     A key whose score is infinite has P = 0 in every row, and its s_j dl_ij
     terms are taken as 0.  Query rows are taken ``block`` at a time (each row
-    is independent).  Returns (ds float64 [T], dgain float64 [hq], dtau)."""
+    is independent).  Returns (ds float64 [T], dgain float64 [hq], dtau).
+
+    With ``scales`` it also returns the magnitudes of the summed terms, the
+    natural size of a rounding error in each sum (used by tests for their
+    bounds; they change nothing above): sum_h |gain_h| sum_i |dl_ij| per key,
+    sum_ij |s_j dl_ij| per head, and sum |dl_ij q'_i . k'_j| / (sqrt(D) tau^2)."""
     dec = (lambda a: np.asarray(a, np.float64)) if q_is_f64 else bf16_decode
     q, k, v, do = dec(q_bits), dec(k_bits), dec(v_bits), dec(do_bits)
     t, hq, d = q.shape
@@ -351,6 +356,9 @@ def gated_attention_bwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarr
     ds = np.zeros(t)
     dgain = np.zeros(hq)
     dtau = 0.0
+    ds_mag = np.zeros(t)
+    dg_mag = np.zeros(hq)
+    dtau_mag = 0.0
     for b in range(len(cu_kept) - 1):
         lo, hi = int(cu_kept[b]), int(cu_kept[b + 1])
         if hi <= lo:
@@ -361,6 +369,7 @@ def gated_attention_bwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarr
             g = h // group
             kh, vh = kr[lo:hi, g, :], v[lo:hi, g, :]
             col = np.zeros(hi - lo)          # sum_i dl_ij for this head
+            col_mag = np.zeros(hi - lo)
             for r0 in range(lo, hi, block):
                 r1 = min(hi, r0 + block)
                 qk = qr[r0:r1, h, :] @ kh.T                          # [rows, keys]
@@ -377,9 +386,17 @@ def gated_attention_bwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarr
                 dl = p * (dp - delta)
                 col += dl.sum(axis=0)
                 dtau += float((dl * (-qk / (math.sqrt(d) * tau * tau))).sum())
+                if scales:
+                    col_mag += np.abs(dl).sum(axis=0)
+                    dtau_mag += float(np.abs(dl * qk).sum()) / (math.sqrt(d) * tau * tau)
             ds[lo:hi] += gain[h] * col
             use = np.isfinite(s_b) & (col != 0.0)
             dgain[h] += float((s_b[use] * col[use]).sum())
+            if scales:
+                ds_mag[lo:hi] += abs(gain[h]) * col_mag
+                dg_mag[h] += float(np.abs(s_b[use] * col_mag[use]).sum())
+    if scales:
+        return ds, dgain, dtau, ds_mag, dg_mag, dtau_mag
     return ds, dgain, dtau
 
 
