@@ -132,6 +132,55 @@ def measure_masked(P, shape, flush, steps):
             "gate_us": float(per[0]) * 1e3, "topk_us": float(per[1]) * 1e3, "gather_us": float(per[2]) * 1e3}
 
 
+def measure_attn_bwd(P, shape, flush, steps):
+    """The attention backward with respect to s, gain and tau (one layer:
+    the step's last, with its own q', K cache, v and a forward o, lse), on a
+    seeded upstream gradient dO ~ N(0, 1); one CUDA graph around the call, L2
+    flushed before each replay.  Flops are the forward's (S and dP products
+    over the causal triangle)."""
+    import torch
+    tg = P.tg
+    L = P.layers[-1]
+    T, hq, D = P.T, shape.hq, shape.head_dim
+    o = torch.empty((T, hq, D), dtype=torch.bfloat16, device=P.dev)
+    lse = torch.empty((hq, T), dtype=torch.float32, device=P.dev)
+    tg.tg_gated_attention_rotated(P.q_rot, L["k_cache"], L["v"], P.pos, P.sk, L["gain"], L["tau"], P.cu_kept,
+                                  P.max_kept, o=o, lse=lse)
+    gen = torch.Generator(device=P.dev)
+    gen.manual_seed(20261203)
+    d_o = torch.randn((T, hq, D), generator=gen, device=P.dev).to(torch.bfloat16)
+    d_s = torch.empty(T, dtype=torch.float32, device=P.dev)
+    d_g = torch.empty(hq, dtype=torch.float32, device=P.dev)
+    d_t = torch.empty(1, dtype=torch.float32, device=P.dev)
+    ws = torch.empty(tg.lib.tg_attention_bwd_workspace_size(T, hq), dtype=torch.uint8, device=P.dev)
+
+    def call():
+        tg.tg_gated_attention_bwd(P.q_rot, L["k_cache"], L["v"], o, lse, d_o, P.pos, P.sk, L["gain"], L["tau"],
+                                  P.cu_kept, P.max_kept, d_s=d_s, d_gain=d_g, d_tau=d_t, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ev[0].record()
+        call()
+        ev[1].record()
+    per = []
+    for i in range(3 + steps):
+        flush.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        if i >= 3:
+            per.append(ev[0].elapsed_time(ev[1]))
+    if tg.tg_check_device_status() != tg.TG_OK:
+        raise RuntimeError("device status after the backward: " + tg.lib.tg_last_error_string().decode())
+    ms = float(np.mean(per))
+    fl = attention_flops(shape.kept_lens, hq, D)
+    return {"ms_per_layer": ms, "tflops": fl / (ms * 1e-3) / 1e12, "gflop_per_layer": fl / 1e9,
+            "launches_per_call": 4}
+
+
 def max_over_ranks(values, device):
     """Each value's maximum over the ranks of the default process group (the
     values unchanged when there is one rank): the slowest rank's time."""
@@ -503,6 +552,9 @@ def run_gpu(args, shape):
     # ---- general prunable spans (the next row after the path) ----
     masked = measure_masked(P, shape, flush, args.steps)
     masked["frac_of_measured_hbm"] = masked["gbs"] / peaks["hbm_gbs"]
+    # ---- attention backward w.r.t. s, gain and tau (the next row after that) ----
+    bwd = measure_attn_bwd(P, shape, flush, args.steps)
+    bwd["frac_of_burst"] = bwd["tflops"] / peaks["bf16_tflops"]
 
     # ---- end to end through the public API, host buffers ----
     import torch as _t
@@ -571,6 +623,7 @@ def run_gpu(args, shape):
                           "kernel_ms_per_layer": kern_ms / nl, "kernel_tflops": kern_tflops,
                           "rope_us_per_layer": rope_ms / nl * 1e3},
             "masked_gate_topk_gather": masked,
+            "attention_bwd_s_gain_tau": bwd,
             "gate_topk_gather": {"us": gtg_ms * 1e3, "gbs": byts / (gtg_ms * 1e-3) / 1e9, "bytes": byts,
                                  "frac_of_measured_hbm": byts / (gtg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                  "gate_us": seg_ms["gate"] * 1e3, "topk_us": seg_ms["topk"] * 1e3,

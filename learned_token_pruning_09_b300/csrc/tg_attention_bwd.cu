@@ -32,7 +32,14 @@
 
 namespace tg {
 
-constexpr int kBwdThreads = 320;   // warps 0-3 / 4-7: the two warpgroups; 8: producer; 9: MMA
+constexpr int kBwdThreads = 384;   // warps 0-7: the two warpgroups; 8: copies; 9: MMA; 10: metadata
+// Register split by setmaxnreg: launched with kBwdLaunchRegs per thread
+// (384 x 168 = 64512), the two warpgroups grow to kBwdSoftRegs and warps
+// 8-11 shrink to kBwdCtrlRegs: 2*128*192 + 128*112 = 63488.
+constexpr int kBwdLaunchRegs = 168;
+constexpr int kBwdSoftRegs = 192;
+constexpr int kBwdCtrlRegs = 112;
+static_assert(2 * 128 * kBwdSoftRegs + 128 * kBwdCtrlRegs <= kBwdThreads * kBwdLaunchRegs, "register split");
 constexpr int kBwdStages = 4;      // Q/dO ring
 constexpr int kBwdMeta = 6;        // per-step query metadata slots
 constexpr float kLog2e = 1.4426950408889634f;
@@ -169,10 +176,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
   const uint32_t tmem = sm.tmem_base;
 
   uint32_t issued = 0;   // warp 8 lane 0: ring stages this CTA issued
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBwdCtrlRegs));
   if (warp == 8) {
-    // ======================= producer =======================
-    const uint32_t full0 = mapa_shared(smem_u32(&sm.full[0]), 0);
+    // ======================= copy producer: K/V once, then Q and dO halves =======================
     if (lane == 0) {
+      const uint32_t full0 = mapa_shared(smem_u32(&sm.full[0]), 0);
       prefetch_tmap(&map_q); prefetch_tmap(&map_k); prefetch_tmap(&map_v); prefetch_tmap(&map_do);
       const uint32_t kv_bar = mapa_shared(smem_u32(&sm.kv_full), 0);
       if (leader) mbar_arrive_expect_tx(&sm.kv_full, 4 * kKv);
@@ -181,71 +190,87 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         tma_load_2d_pair(sm.k + bx * kKBox, &map_k, kv_bar, kvh * kD + bx * 64, krow);
         tma_load_2d_pair(sm.v + bx * kKBox, &map_v, kv_bar, kvh * kD + bx * 64, krow);
       }
+      bool ok = true;
+      for (int m = 0; m < n_steps; ++m) {
+        const int st = m % kBwdStages;
+        if (m >= kBwdStages)
+          ok = mbar_wait(&sm.ring_free[st], ((m / kBwdStages) & 1u) ^ 1u, wd, a.status, kStatusTimeout);
+        if (!ok || sm.abort) break;
+        const int h = kvh * group + m % group;
+        const int qrow = seq_start + (qt0 + m / group) * 128 + static_cast<int>(rank) * 64;
+        if (leader) mbar_arrive_expect_tx(&sm.full[st], 4 * kHalf);
+        for (int bx = 0; bx < kBoxes; ++bx) {
+          tma_load_2d_pair(sm.q[st] + bx * kQBox, &map_q, full0 + st * 8u, h * kD + bx * 64, qrow);
+          tma_load_2d_pair(sm.dout[st] + bx * kQBox, &map_do, full0 + st * 8u, h * kD + bx * 64, qrow);
+        }
+        ++issued;
+      }
+      if (!ok) sm.abort = 1;
+      if (!leader) st_cluster_u32(mapa_shared(smem_u32(&sm.peer_issued), 0), issued);
     }
-    // Query metadata of a step, one step ahead in registers: -lse log2 e
-    // (-inf where the row saw no key, so that its P is 0), -D and the
-    // position (-1 past the sequence end: masked for every key).
-    float nl[4], nd[4];
-    int qp[4];
-    auto load_meta = [&](int m) {
-      const int qt = qt0 + m / group;
-      const int h = kvh * group + m % group;
+  } else if (warp == 10) {
+    // ======================= metadata producer =======================
+    // Per step and query column: -lse log2 e (-inf where the row saw no key,
+    // so that its P is 0), -D and the position (-1 past the sequence end:
+    // masked for every key).  The raw values are loaded kAhead steps ahead
+    // into a ring of registers, unconditionally (rows past the sequence read
+    // row 0 of it) and with no use until the step is written, so that the L2
+    // latency of these loads stays off the step-to-step path.
+    constexpr int kAhead = 4;
+    float nl[kAhead][4], nd[kAhead][4];
+    int qp[kAhead][4];
+    auto load_meta = [&](int m, float (&l4)[4], float (&d4)[4], int (&p4)[4]) {
+      const int mm = m < n_steps ? m : n_steps - 1;
+      const int qt = qt0 + mm / group;
+      const int h = kvh * group + mm % group;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int row = qt * 128 + u * 32 + lane;
-        nl[u] = 0.0f;
-        nd[u] = 0.0f;
-        qp[u] = -1;
-        if (m < n_steps && row < seq_len) {
-          const long long gi = static_cast<long long>(h) * a.n_kept + seq_start + row;
-          const float l = __ldg(a.lse + gi);
-          nl[u] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-          nd[u] = -__ldg(a.delta + gi);
-          qp[u] = __ldg(a.pos + seq_start + row);
-        }
+        int row = qt * 128 + u * 32 + lane;
+        row = row < seq_len ? row : 0;
+        const long long gi = static_cast<long long>(h) * a.n_kept + seq_start + row;
+        l4[u] = __ldg(a.lse + gi);
+        d4[u] = __ldg(a.delta + gi);
+        p4[u] = __ldg(a.pos + seq_start + row);
       }
     };
-    load_meta(0);
-    bool ok = true;
-    for (int m = 0; m < n_steps; ++m) {
+    auto produce = [&](int m, const float (&l4)[4], const float (&d4)[4], const int (&p4)[4]) -> bool {
       const int ms = m % kBwdMeta;
-      const int st = m % kBwdStages;
+      bool ok = true;
       if (m >= kBwdMeta) {
         if (lane == 0)
           ok = mbar_wait(&sm.meta_free[ms], ((m / kBwdMeta) & 1u) ^ 1u, wd, a.status, kStatusTimeout);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok || sm.abort) { sm.abort = 1; break; }
+        if (!ok || sm.abort) return false;
       }
       float* ldf = reinterpret_cast<float*>(sm.ld[ms]);
+      const int qt = qt0 + m / group;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = u * 32 + lane;
-        ldf[(c >> 1) * 4 + (c & 1)] = nl[u];
-        ldf[(c >> 1) * 4 + 2 + (c & 1)] = nd[u];
-        sm.qpos[ms][c] = qp[u];
+        const bool in = qt * 128 + c < seq_len;
+        const float l = l4[u];
+        ldf[(c >> 1) * 4 + (c & 1)] = !in ? 0.0f : (l == -INFINITY ? -INFINITY : -l * kLog2e);
+        ldf[(c >> 1) * 4 + 2 + (c & 1)] = in ? -d4[u] : 0.0f;
+        sm.qpos[ms][c] = in ? p4[u] : -1;
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sm.meta_full[ms]);
-        if (m >= kBwdStages)
-          ok = mbar_wait(&sm.ring_free[st], ((m / kBwdStages) & 1u) ^ 1u, wd, a.status, kStatusTimeout);
-        if (ok && !sm.abort) {
-          const int qt = qt0 + m / group;
-          const int h = kvh * group + m % group;
-          const int qrow = seq_start + qt * 128 + static_cast<int>(rank) * 64;
-          if (leader) mbar_arrive_expect_tx(&sm.full[st], 4 * kHalf);
-          for (int bx = 0; bx < kBoxes; ++bx) {
-            tma_load_2d_pair(sm.q[st] + bx * kQBox, &map_q, full0 + st * 8u, h * kD + bx * 64, qrow);
-            tma_load_2d_pair(sm.dout[st] + bx * kQBox, &map_do, full0 + st * 8u, h * kD + bx * 64, qrow);
-          }
-          ++issued;
+      if (lane == 0) mbar_arrive(&sm.meta_full[ms]);
+      return true;
+    };
+#pragma unroll
+    for (int r = 0; r < kAhead; ++r) load_meta(r, nl[r], nd[r], qp[r]);
+    bool ok = true;
+    for (int m0 = 0; m0 < n_steps && ok; m0 += kAhead) {
+#pragma unroll
+      for (int r = 0; r < kAhead; ++r) {
+        const int m = m0 + r;
+        if (ok && m < n_steps) {
+          ok = produce(m, nl[r], nd[r], qp[r]);
+          if (ok) load_meta(m + kAhead, nl[r], nd[r], qp[r]);
         }
       }
-      ok = __shfl_sync(0xffffffffu, (ok && !sm.abort) ? 1 : 0, 0) != 0;
-      if (!ok) { sm.abort = 1; break; }
-      load_meta(m + 1);
     }
-    if (!leader && lane == 0) st_cluster_u32(mapa_shared(smem_u32(&sm.peer_issued), 0), issued);
+    if (!ok) sm.abort = 1;
   } else if (warp == 9) {
     // ======================= pair MMA issuer (leader) =======================
     if (leader && lane == 0) {
@@ -284,7 +309,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       mma_commit_pair_mc(&sm.mma_done, 0x1);
       mbar_wait(&sm.mma_done, 0, kDrainCycles, a.status, kStatusTimeout);
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBwdSoftRegs));
     // ======================= the two warpgroups: one thread per key =======================
     const int t = warp >> 2;                      // TMEM buffer / step parity
     const int sub = warp & 3;                     // TMEM lane quarter
@@ -318,40 +345,45 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
       const float4* ld = sm.ld[ms];
       const int* qp = sm.qpos[ms];
       const uint32_t tS = tmem + static_cast<uint32_t>(t) * 256u + lane_off;
-      float2 r0 = make_float2(0.0f, 0.0f), r1 = r0, q0 = r0, q1 = r0;
+      // two 64-column halves: one TMEM wait each, 32 independent column pairs
+      float2 r[4], q[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rs[32], rp[32];
-        tmem_ld32(tS + c * 32, rs);
-        tmem_ld32(tS + 128u + c * 32, rp);
+      for (int u = 0; u < 4; ++u) { r[u] = make_float2(0.0f, 0.0f); q[u] = r[u]; }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t rs[64], rp[64];
+        tmem_ld32(tS + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
+        tmem_ld32(tS + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
+        tmem_ld32(tS + 128u + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&rp[0]));
+        tmem_ld32(tS + 128u + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rp[32]));
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float4 m4 = ld[c * 16 + i];          // {-L_i, -L_i+1, -D_i, -D_i+1}
+        for (int i = 0; i < 32; ++i) {
+          const float4 m4 = ld[c * 32 + i];          // {-L_i, -L_i+1, -D_i, -D_i+1}
           const float2 sv = make_float2(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1]));
           const float2 x = __fadd2_rn(__ffma2_rn(sv, c2, b2), make_float2(m4.x, m4.y));
           float p0 = ex2_approx(x.x);
           float p1 = ex2_approx(x.y);
           if (masked) {
-            if (kpos > qp[c * 32 + 2 * i]) p0 = 0.0f;
-            if (kpos > qp[c * 32 + 2 * i + 1]) p1 = 0.0f;
+            if (kpos > qp[c * 64 + 2 * i]) p0 = 0.0f;
+            if (kpos > qp[c * 64 + 2 * i + 1]) p1 = 0.0f;
           }
           const float2 dp = __fadd2_rn(make_float2(__uint_as_float(rp[2 * i]), __uint_as_float(rp[2 * i + 1])),
                                        make_float2(m4.z, m4.w));
           const float2 dl = __fmul2_rn(make_float2(p0, p1), dp);
-          if (i & 1) { r1 = __fadd2_rn(r1, dl); q1 = __ffma2_rn(dl, sv, q1); }
-          else { r0 = __fadd2_rn(r0, dl); q0 = __ffma2_rn(dl, sv, q0); }
+          r[i & 3] = __fadd2_rn(r[i & 3], dl);
+          q[i & 3] = __ffma2_rn(dl, sv, q[i & 3]);
         }
       }
       // this warp is done with the TMEM buffer and the metadata slot
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_cluster(tfree0 + static_cast<uint32_t>(t) * 8u);
+        mbar_arrive_cluster_relaxed(tfree0 + static_cast<uint32_t>(t) * 8u);
         mbar_arrive(&sm.meta_free[ms]);
       }
-      const float step_r = (r0.x + r0.y) + (r1.x + r1.y);
-      const float step_t = (q0.x + q0.y) + (q1.x + q1.y);
+      const float step_r = ((r[0].x + r[0].y) + (r[1].x + r[1].y)) + ((r[2].x + r[2].y) + (r[3].x + r[3].y));
+      const float step_t = ((q[0].x + q[0].y) + (q[1].x + q[1].y)) + ((q[2].x + q[2].y) + (q[3].x + q[3].y));
 #pragma unroll
       for (int u = 0; u < kBwdMaxGroup; ++u)
         if (u == hh) { acc_r[u] += step_r; acc_t[u] += step_t; }
@@ -462,6 +494,12 @@ static cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, co
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<kD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  // the setmaxnreg split is only valid for the launch register count it was
+  // sized for; refuse to launch otherwise (setmaxnreg.inc would never return)
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, attn_bwd_kernel<kD>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kBwdLaunchRegs) return cudaErrorInvalidConfiguration;
   const long long n_kp = (static_cast<long long>(a.max_kept) + 255) / 256;
   const long long units = n_kp * a.batch * a.hkv;
   if (units == 0) return cudaSuccess;

@@ -174,6 +174,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Arrive without release semantics, for a signal that announces only the
+// completion of work that is already complete in the arriving thread (TMEM
+// reads finished by tcgen05.wait::ld): a release arrive at cluster scope
+// costs the arriving warp about a microsecond.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 // TMA 2D tile load into this CTA's shared memory whose completion is counted
 // on an mbarrier of either CTA of the pair (`bar_cluster`: shared::cluster)
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster,
