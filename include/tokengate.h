@@ -261,7 +261,7 @@ TG_API size_t tg_attention_workspace_size(int64_t n_kept, int32_t hq, int32_t hk
  *   lse [hq, n_kept] fp32: the forward's outputs (tg_gated_attention_rotated)
  *   d_o [n_kept, hq, head_dim] bf16: the upstream gradient dL/do
  *   pos_kept, s_kept, gain, tau, cu_kept, batch, n_kept, max_kept, hq, hkv,
- *            head_dim: as for the forward; hq / hkv <= 8; positions strictly
+ *            head_dim: as for the forward; hq / hkv <= 8, hq <= 256; positions strictly
  *            increasing within each sequence (the forward checks it)
  *   d_s [n_kept], d_gain [hq], d_tau [1]: fp32 device outputs (d_s is 0 for
  *            rows outside every sequence)

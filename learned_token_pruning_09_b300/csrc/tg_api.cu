@@ -428,7 +428,7 @@ size_t tg_attention_bwd_workspace_size(int64_t n_kept, int32_t hq) {
   if (n_kept <= 0 || hq <= 0) return 0;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t plane = static_cast<size_t>(n_kept) * hq * 4;
-  return up(plane) + 2 * up(2 * plane) + up(static_cast<size_t>(hq) * 4);
+  return up(plane) + 2 * up(2 * plane) + up(static_cast<size_t>(hq) * kBwdChunks * 2 * 4);
 }
 
 tg_status tg_gated_attention_bwd(const void* q_rot, const void* k_rot, const void* v, const void* o,
@@ -440,6 +440,7 @@ tg_status tg_gated_attention_bwd(const void* q_rot, const void* k_rot, const voi
   tg_status st = check_attention_shape(batch, n_kept, hq, hkv, head_dim, cu_kept);
   if (st != TG_OK) return st;
   if (hq / hkv > kBwdMaxGroup) return fail(TG_ERR_UNSUPPORTED, "hq / hkv must be at most %d", kBwdMaxGroup);
+  if (hq > kBwdMaxHeads) return fail(TG_ERR_UNSUPPORTED, "hq must be at most %d", kBwdMaxHeads);
   if (max_kept < 0) return fail(TG_ERR_INVALID_ARG, "max_kept must be >= 0");
   if (!(tau > 0.0f) || !std::isfinite(tau)) return fail(TG_ERR_INVALID_ARG, "tau must be positive and finite");
   if (!d_gain || !d_tau || (n_kept > 0 && !d_s)) return fail(TG_ERR_INVALID_ARG, "null output pointer");
@@ -490,7 +491,7 @@ tg_status tg_gated_attention_bwd(const void* q_rot, const void* k_rot, const voi
   a.delta = reinterpret_cast<float*>(ws);
   a.r_part = reinterpret_cast<float*>(ws + up(plane));
   a.t_part = reinterpret_cast<float*>(ws + up(plane) + up(2 * plane));
-  a.tsum = reinterpret_cast<float*>(ws + up(plane) + 2 * up(2 * plane));
+  a.part = reinterpret_cast<float*>(ws + up(plane) + 2 * up(2 * plane));
   a.ds = d_s; a.dgain = d_gain; a.dtau = d_tau;
   a.status = di->status; a.watchdog = g_watchdog_cycles; a.num_sms = di->num_sms;
   const cudaError_t e = launch_attention_bwd(mq, mk, mv, mdo, a, stream);

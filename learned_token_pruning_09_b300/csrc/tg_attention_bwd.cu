@@ -425,9 +425,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 }
 
 // ---------------------------------------------------------------------------
-// reductions: dgain_h = sum_j s_j R_hj, tsum_h = sum_j T_hj (one block per
-// head), then ds_j = sum_h gain_h R_hj and dtau = dtau_scale sum_h tsum_h.
-// R = the two warpgroups' partial sums; keys past cu_kept[batch] hold none.
+// reductions, in a fixed order (bit-reproducible results):
+//   bwd_head_kernel, block (c, h): partial sums over key chunk c of
+//     sum_j s_j R_hj and sum_j T_hj into part[h][c] (R, T: the two
+//     warpgroups' partial sums added; keys past cu_kept[batch] hold none);
+//   bwd_ds_kernel: ds_j = sum_h gain_h R_hj per key; block 0 also forms
+//     dgain_h = sum_c part_g[h][c] and dtau = dtau_scale sum_h sum_c part_t[h][c].
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float block_sum_256(float v, float* red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -442,15 +445,19 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
 
 __global__ void __launch_bounds__(256) bwd_head_kernel(AttnBwdArgs a) {
   __shared__ float red[8];
-  const int h = blockIdx.x;
+  const int c = blockIdx.x;
+  const int h = blockIdx.y;
   const long long n = a.n_kept;
   const long long n_rows = min(max(static_cast<long long>(__ldg(a.cu_kept + a.batch)), 0LL), n);
+  const long long chunk = (n_rows + kBwdChunks - 1) / kBwdChunks;
+  const long long j0 = c * chunk;
+  const long long j1 = min(n_rows, j0 + chunk);
   const float* r0 = a.r_part + static_cast<long long>(h) * n;
   const float* r1 = a.r_part + static_cast<long long>(a.hq + h) * n;
   const float* t0 = a.t_part + static_cast<long long>(h) * n;
   const float* t1 = a.t_part + static_cast<long long>(a.hq + h) * n;
   float g = 0.0f, tt = 0.0f;
-  for (long long j = threadIdx.x; j < n_rows; j += 256) {
+  for (long long j = j0 + threadIdx.x; j < j1; j += 256) {
     const float r = r0[j] + r1[j];
     const float s = __ldg(a.s_kept + j);
     if (r != 0.0f && isfinite(s)) g = fmaf(s, r, g);
@@ -459,12 +466,13 @@ __global__ void __launch_bounds__(256) bwd_head_kernel(AttnBwdArgs a) {
   g = block_sum_256(g, red);
   tt = block_sum_256(tt, red);
   if (threadIdx.x == 0) {
-    a.dgain[h] = g;
-    a.tsum[h] = tt;
+    a.part[(static_cast<long long>(h) * kBwdChunks + c) * 2] = g;
+    a.part[(static_cast<long long>(h) * kBwdChunks + c) * 2 + 1] = tt;
   }
 }
 
 __global__ void __launch_bounds__(256) bwd_ds_kernel(AttnBwdArgs a) {
+  __shared__ float tsum[256];
   const long long j = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   const long long n = a.n_kept;
   const long long n_rows = min(max(static_cast<long long>(__ldg(a.cu_kept + a.batch)), 0LL), n);
@@ -476,10 +484,23 @@ __global__ void __launch_bounds__(256) bwd_ds_kernel(AttnBwdArgs a) {
                                           a.r_part[static_cast<long long>(a.hq + h) * n + j], acc);
     a.ds[j] = acc;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    float tt = 0.0f;
-    for (int h = 0; h < a.hq; ++h) tt += a.tsum[h];
-    *a.dtau = tt * a.dtau_scale;
+  if (blockIdx.x == 0) {
+    // one thread per head (the host checks hq <= kBwdMaxHeads = 256), then thread 0 over heads
+    for (int h = threadIdx.x; h < a.hq; h += 256) {
+      float g = 0.0f, tt = 0.0f;
+      for (int c = 0; c < kBwdChunks; ++c) {
+        g += a.part[(static_cast<long long>(h) * kBwdChunks + c) * 2];
+        tt += a.part[(static_cast<long long>(h) * kBwdChunks + c) * 2 + 1];
+      }
+      a.dgain[h] = g;
+      if (h < 256) tsum[h] = tt;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float tt = 0.0f;
+      for (int h = 0; h < a.hq && h < 256; ++h) tt += tsum[h];
+      *a.dtau = tt * a.dtau_scale;
+    }
   }
 }
 
@@ -536,7 +557,7 @@ cudaError_t launch_attention_bwd(const CUtensorMap& mq, const CUtensorMap& mk, c
   cudaError_t e = (a.head_dim == 128) ? launch_bwd_d<128>(mq, mk, mv, mdo, a, st)
                                       : launch_bwd_d<64>(mq, mk, mv, mdo, a, st);
   if (e != cudaSuccess) return e;
-  bwd_head_kernel<<<a.hq, 256, 0, st>>>(a);
+  bwd_head_kernel<<<dim3(kBwdChunks, a.hq), 256, 0, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   bwd_ds_kernel<<<static_cast<unsigned>((a.n_kept + 255) / 256), 256, 0, st>>>(a);

@@ -121,6 +121,8 @@ cudaError_t launch_attention(const CUtensorMap& map_q, const CUtensorMap& map_k,
 
 // ---- attention backward: gradients of the score, gain and temperature ------
 constexpr int kBwdMaxGroup = 8;   // query heads per KV head
+constexpr int kBwdChunks = 32;    // key chunks per head in the dgain / dtau reduction
+constexpr int kBwdMaxHeads = 256; // query heads (the final reduction holds one per thread)
 struct AttnBwdArgs {
   const void* o;          // [T, hq, D] bf16, the forward output
   const void* d_o;        // [T, hq, D] bf16
@@ -138,7 +140,7 @@ struct AttnBwdArgs {
   float* delta;           // [hq, T] workspace: dO_i . o_i
   float* r_part;          // [2, hq, T] workspace: sum_i dl_ij, per softmax warpgroup
   float* t_part;          // [2, hq, T] workspace: sum_i dl_ij (q'_i . k'_j), per warpgroup
-  float* tsum;            // [hq] workspace
+  float* part;            // [hq, kBwdChunks, 2] workspace: per-chunk sums for dgain and dtau
   float* ds;              // [T]
   float* dgain;           // [hq]
   float* dtau;            // [1]
