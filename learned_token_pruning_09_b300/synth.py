@@ -309,3 +309,36 @@ ALL_SHAPES = {
     "long-128k": long_128k,
     "ragged-8": ragged_batch,
 }
+
+
+# ---------------------------------------------------------------------------
+# pruned Gated DeltaNet scan inputs
+# ---------------------------------------------------------------------------
+_S_DELTA = 10
+
+# Kept-token streams of the hybrid model's linear-attention layers: a 32k
+# needle-in-a-haystack context (32,704 document + 64 question tokens) cut to
+# K = 4,096 kept document tokens, so T = 4,160, batch 1; and a ragged batch.
+DELTA_SHAPES = {
+    "deltanet-tiny": {"lens": [160], "hk": 2, "hv": 4, "dk": 64, "dv": 64},
+    "deltanet-32k-k4096": {"lens": [4160], "hk": 16, "hv": 32, "dk": 128, "dv": 128},
+    "deltanet-ragged": {"lens": [1500, 37, 0, 900, 2049], "hk": 4, "hv": 8, "dk": 128, "dv": 128},
+}
+
+
+def deltanet_inputs(name: str) -> Dict[str, object]:
+    """Seeded inputs of one gated-delta scan: q, k [T, hk, dk] and v
+    [T, hv, dv] bf16 bits ~ N(0, 1); g [T, hv] fp32 log-decays, -g
+    log-uniform in [0.005, 0.5] (decays exp(g) in [0.61, 0.995]); beta
+    [T, hv] fp32 ~ U(0.05, 0.95); cu_kept [B+1] int32."""
+    cfg = DELTA_SHAPES[name]
+    lens = cfg["lens"]
+    t = int(sum(lens))
+    r = np.random.default_rng(np.random.SeedSequence([BASE_SEED, _S_DELTA, t, cfg["hv"], cfg["dk"]]))
+    q = _normal_bf16(r, (t, cfg["hk"], cfg["dk"]))
+    k = _normal_bf16(r, (t, cfg["hk"], cfg["dk"]))
+    v = _normal_bf16(r, (t, cfg["hv"], cfg["dv"]))
+    g = (-np.exp(r.uniform(np.log(0.005), np.log(0.5), size=(t, cfg["hv"])))).astype(np.float32)
+    beta = r.uniform(0.05, 0.95, size=(t, cfg["hv"])).astype(np.float32)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "cu_kept": cu}

@@ -30,6 +30,12 @@ the exact algebra that they leave open is taken as follows:
 * attention backward (the gradient path from the attention loss to the gate):
           for L = sum dO . o, the derivatives with respect to s_j, g_h and tau,
           from dl_ij = p_ij (dO_i . v_j - sum_j' p_ij' dO_i . v_j').
+* pruned Gated DeltaNet (the hybrid model's linear-attention layers, which
+          TokenGate also prunes): per value head a state S (d_v x d_k) runs
+          the gated delta rule over the KEPT tokens of a sequence, in order,
+          S_t = S_{t-1} alpha_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+          o_t = S_t q_t, with alpha_t = exp(g_t), q and k L2-normalised and q
+          scaled by 1/sqrt(d_k); a pruned token never updates the state.
 * stacked layer (long-context workload): qkv = x W_qkv^T, attention as above,
           x_out = x + o W_o^T.  No norm and no MLP.
 * general prunable spans (the prompt template marks the prunable document
@@ -59,7 +65,7 @@ __all__ = [
     "bf16_decode", "gelu", "logsigmoid", "gate_score", "score_from_logit",
     "topk_select", "gather_kept", "rope", "gated_attention",
     "stacked_layer", "project_qkv", "gate_score_masked", "topk_select_masked",
-    "gated_attention_bwd",
+    "gated_attention_bwd", "gated_delta_scan",
 ]
 
 
@@ -398,6 +404,54 @@ def gated_attention_bwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarr
     if scales:
         return ds, dgain, dtau, ds_mag, dg_mag, dtau_mag
     return ds, dgain, dtau
+
+
+# ---------------------------------------------------------------------------
+# pruned Gated DeltaNet (TokenGate prunes the Gated DeltaNet layers of the
+# hybrid Qwen3.5 model as well as its attention layers; the layer itself is
+# the gated delta rule of Gated DeltaNet, Yang, Kautz and Hatamizadeh, 2024)
+# ---------------------------------------------------------------------------
+
+
+def gated_delta_scan(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, g: np.ndarray,
+                     beta: np.ndarray, cu_kept: Sequence[int], scale: Optional[float] = None,
+                     initial_state: Optional[np.ndarray] = None, q_is_f64: bool = False,
+                     l2_eps: float = 1e-6):
+    """The gated delta rule over the kept tokens of each sequence.
+
+    q, k [T, hk, d_k] and v [T, hv, d_v] (bf16 bits, or float64 with
+    ``q_is_f64``); g [T, hv] log-decays (alpha = exp(g), g <= 0); beta [T, hv]
+    write strengths in [0, 1]; cu_kept [B+1].  Value head h reads q/k head
+    h // (hv / hk).  Per sequence and value head, from S = initial_state
+    (zero when None), token by token in order:
+      k^ = k / sqrt(|k|^2 + eps), q^ = scale q / sqrt(|q|^2 + eps)
+      S  = exp(g) (S - beta (S k^) k^T) + beta v k^T
+      o  = S q^
+    scale defaults to 1 / sqrt(d_k).  Returns (o float64 [T, hv, d_v],
+    final states float64 [B, hv, d_v, d_k])."""
+    dec = (lambda a: np.asarray(a, np.float64)) if q_is_f64 else bf16_decode
+    q, k, v = dec(q_bits), dec(k_bits), dec(v_bits)
+    t, hk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    rep = hv // hk
+    g = np.asarray(g, np.float64)
+    beta = np.asarray(beta, np.float64)
+    scale = 1.0 / math.sqrt(dk) if scale is None else float(scale)
+    nb = len(cu_kept) - 1
+    o = np.zeros((t, hv, dv))
+    states = np.zeros((nb, hv, dv, dk))
+    for b in range(nb):
+        lo, hi = int(cu_kept[b]), int(cu_kept[b + 1])
+        for h in range(hv):
+            S = np.zeros((dv, dk)) if initial_state is None else np.array(initial_state[b, h], np.float64)
+            kh = h // rep
+            for i in range(lo, hi):
+                kk = k[i, kh] / math.sqrt(float(k[i, kh] @ k[i, kh]) + l2_eps)
+                qq = scale * q[i, kh] / math.sqrt(float(q[i, kh] @ q[i, kh]) + l2_eps)
+                S = math.exp(g[i, h]) * (S - beta[i, h] * np.outer(S @ kk, kk)) + beta[i, h] * np.outer(v[i, h], kk)
+                o[i, h] = S @ qq
+            states[b, h] = S
+    return o, states
 
 
 # ---------------------------------------------------------------------------

@@ -699,3 +699,136 @@ def test_attention_bwd_infinite_score_removes_the_key():
     np.testing.assert_allclose(ds[keep], dsr, rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dg, dgr, rtol=1e-10, atol=1e-12)
     assert abs(dtau - dtaur) < 1e-10 * max(1.0, abs(dtau))
+
+
+# ---------------------------------------------------------------------------
+# pruned Gated DeltaNet (gated delta rule over kept tokens)
+# ---------------------------------------------------------------------------
+
+
+def _unit(a):
+    return a / np.linalg.norm(a, axis=-1, keepdims=True)
+
+
+def test_delta_scan_orthogonal_keys_is_decayed_linear_attention():
+    """Mutually orthogonal keys: the erase term never touches earlier content,
+    so o_t = sum_{i<=t} exp(G_t - G_i) beta_i (k^_i . q^_t) v_i, G = cumsum(g):
+    decayed linear attention, written here as one masked matrix product."""
+    rng = np.random.default_rng(1)
+    t, dk, dv = 12, 16, 5
+    basis = np.linalg.qr(rng.standard_normal((dk, dk)))[0][:t]          # orthonormal rows
+    k = (basis * rng.uniform(0.5, 3.0, (t, 1)))[:, None, :]              # any length: k is normalised
+    q = rng.standard_normal((t, 1, dk))
+    v = rng.standard_normal((t, 1, dv))
+    g = -rng.uniform(0.0, 0.7, (t, 1))
+    beta = rng.uniform(0.1, 1.0, (t, 1))
+    o, _ = oracle.gated_delta_scan(q, k, v, g, beta, [0, t], scale=1.0, q_is_f64=True, l2_eps=0.0)
+    G = np.cumsum(g[:, 0])
+    mask = np.tril(np.exp(G[:, None] - G[None, :]))
+    ref = (mask * (_unit(q[:, 0]) @ _unit(k[:, 0]).T)) @ (beta * v[:, 0])
+    np.testing.assert_allclose(o[:, 0], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_delta_scan_overwrites_a_repeated_key():
+    """alpha = 1, beta = 1: writing v2 under the key that holds v1 replaces it
+    (the delta rule's overwrite), so the read returns v2 (k^ . q^)."""
+    rng = np.random.default_rng(2)
+    dk, dv = 8, 4
+    key = rng.standard_normal(dk)
+    k = np.stack([key, 2.5 * key])[:, None, :]
+    q = rng.standard_normal((2, 1, dk))
+    v = rng.standard_normal((2, 1, dv))
+    o, S = oracle.gated_delta_scan(q, k, v, np.zeros((2, 1)), np.ones((2, 1)), [0, 2], scale=1.0,
+                                   q_is_f64=True, l2_eps=0.0)
+    kh = _unit(key)
+    np.testing.assert_allclose(o[1, 0], v[1, 0] * (kh @ _unit(q[1, 0])), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(S[0, 0], np.outer(v[1, 0], kh), rtol=1e-12, atol=1e-14)
+
+
+def test_delta_scan_matches_unrolled_products():
+    """Brute force on a tiny case: S_t = sum_{i<=t} beta_i v_i k^_i^T
+    prod_{j=i+1..t} alpha_j (I - beta_j k^_j k^_j^T), the recurrence unrolled
+    and multiplied in the other association."""
+    rng = np.random.default_rng(3)
+    t, dk, dv = 7, 5, 3
+    q, k = rng.standard_normal((t, 1, dk)), rng.standard_normal((t, 1, dk))
+    v = rng.standard_normal((t, 1, dv))
+    g, beta = -rng.uniform(0, 0.5, (t, 1)), rng.uniform(0, 1, (t, 1))
+    o, _ = oracle.gated_delta_scan(q, k, v, g, beta, [0, t], scale=0.7, q_is_f64=True, l2_eps=0.0)
+    kh, qh = _unit(k[:, 0]), 0.7 * _unit(q[:, 0])
+    for tt in range(t):
+        S = np.zeros((dv, dk))
+        for i in range(tt + 1):
+            P = np.eye(dk)
+            for j in range(i + 1, tt + 1):
+                P = P @ (math.exp(g[j, 0]) * (np.eye(dk) - beta[j, 0] * np.outer(kh[j], kh[j])))
+            S += beta[i, 0] * np.outer(v[i, 0], kh[i]) @ P
+        # token i's own write carries no alpha_i (S_i = alpha_i (...) + beta_i v_i k_i^T)
+        np.testing.assert_allclose(o[tt, 0], S @ qh[tt], rtol=1e-11, atol=1e-13)
+
+
+def test_delta_scan_pruned_tokens_are_skipped():
+    """Running every token with beta = 0 and g = 0 on the pruned ones equals
+    running the kept tokens alone: a pruned token never touches the state."""
+    rng = np.random.default_rng(4)
+    n, hk, hv, dk, dv = 40, 2, 4, 8, 6
+    q, k = rng.standard_normal((n, hk, dk)), rng.standard_normal((n, hk, dk))
+    v = rng.standard_normal((n, hv, dv))
+    g, beta = -rng.uniform(0, 0.5, (n, hv)), rng.uniform(0, 1, (n, hv))
+    kept = np.sort(rng.choice(n, 17, replace=False))
+    gz, bz = np.zeros_like(g), np.zeros_like(beta)
+    gz[kept], bz[kept] = g[kept], beta[kept]
+    o_all, s_all = oracle.gated_delta_scan(q, k, v, gz, bz, [0, n], q_is_f64=True)
+    o_k, s_k = oracle.gated_delta_scan(q[kept], k[kept], v[kept], g[kept], beta[kept], [0, len(kept)],
+                                       q_is_f64=True)
+    np.testing.assert_allclose(o_all[kept], o_k, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(s_all, s_k, rtol=1e-12, atol=1e-13)
+
+
+def test_delta_scan_invariants():
+    rng = np.random.default_rng(5)
+    t, hk, hv, dk, dv = 30, 2, 4, 8, 6
+    q, k = rng.standard_normal((t, hk, dk)), rng.standard_normal((t, hk, dk))
+    v = rng.standard_normal((t, hv, dv))
+    g, beta = -rng.uniform(0, 0.5, (t, hv)), rng.uniform(0, 1, (t, hv))
+    cu = [0, 11, 11, 30]
+    o, S = oracle.gated_delta_scan(q, k, v, g, beta, cu, q_is_f64=True, l2_eps=0.0)
+    # q and k enter only through their directions
+    o2, _ = oracle.gated_delta_scan(3.0 * q, 0.25 * k, v, g, beta, cu, q_is_f64=True, l2_eps=0.0)
+    np.testing.assert_allclose(o2, o, rtol=1e-11, atol=1e-13)
+    # linear in v from a zero state
+    o3, S3 = oracle.gated_delta_scan(q, k, -2.0 * v, g, beta, cu, q_is_f64=True, l2_eps=0.0)
+    np.testing.assert_allclose(o3, -2.0 * o, rtol=1e-12, atol=1e-13)
+    # the default scale is 1/sqrt(d_k), and the output is linear in it
+    o4, _ = oracle.gated_delta_scan(q, k, v, g, beta, cu, scale=1.0, q_is_f64=True, l2_eps=0.0)
+    np.testing.assert_allclose(o4 / math.sqrt(dk), o, rtol=1e-12, atol=1e-13)
+    # value head h reads q/k head h // (hv / hk): heads 2, 3 alone with q/k head 1
+    o5, _ = oracle.gated_delta_scan(q[:, 1:], k[:, 1:], v[:, 2:], g[:, 2:], beta[:, 2:], cu, q_is_f64=True,
+                                    l2_eps=0.0)
+    np.testing.assert_allclose(o5, o[:, 2:], rtol=1e-12, atol=1e-13)
+    # an empty sequence keeps its initial (zero) state; varlen equals separate calls
+    assert np.all(S[1] == 0.0)
+    for b in range(3):
+        lo, hi = cu[b], cu[b + 1]
+        if hi == lo:
+            continue
+        ob, sb = oracle.gated_delta_scan(q[lo:hi], k[lo:hi], v[lo:hi], g[lo:hi], beta[lo:hi], [0, hi - lo],
+                                         q_is_f64=True, l2_eps=0.0)
+        np.testing.assert_allclose(ob, o[lo:hi], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(sb[0], S[b], rtol=1e-12, atol=1e-13)
+
+
+def test_delta_scan_state_continues_across_calls():
+    """Two calls, the second started from the first's final state, equal one
+    call over the whole sequence (the chunk-to-chunk carry)."""
+    rng = np.random.default_rng(6)
+    t, dk, dv = 25, 8, 8
+    q, k = rng.standard_normal((t, 1, dk)), rng.standard_normal((t, 1, dk))
+    v = rng.standard_normal((t, 2, dv))
+    g, beta = -rng.uniform(0, 0.5, (t, 2)), rng.uniform(0, 1, (t, 2))
+    o, S = oracle.gated_delta_scan(q, k, v, g, beta, [0, t], q_is_f64=True)
+    oa, Sa = oracle.gated_delta_scan(q[:9], k[:9], v[:9], g[:9], beta[:9], [0, 9], q_is_f64=True)
+    ob, Sb = oracle.gated_delta_scan(q[9:], k[9:], v[9:], g[9:], beta[9:], [0, t - 9], initial_state=Sa,
+                                     q_is_f64=True)
+    np.testing.assert_allclose(np.concatenate([oa, ob]), o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(Sb, S, rtol=1e-12, atol=1e-13)
