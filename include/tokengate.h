@@ -287,6 +287,39 @@ TG_API tg_status tg_gated_attention_bwd(const void* q_rot, const void* k_rot, co
 TG_API size_t tg_attention_bwd_workspace_size(int64_t n_kept, int32_t hq);
 
 /*
+ * Pruned Gated DeltaNet scan.  TokenGate prunes the Gated DeltaNet layers of
+ * the hybrid Qwen3.5 model as well as its attention layers (MarkTechPost
+ * article, section "Does it work on hybrid attention models?", and the
+ * DeltaNet row of its table "TokenGate vs FastKV, SlimInfer, GemFilter and
+ * DASH"); above the gate such a layer runs its recurrence
+ * over the kept tokens only, and a pruned token never updates the state.  The
+ * layer's recurrence is the gated delta rule (Gated DeltaNet).  Per sequence b
+ * and value head h, from S = initial_state[b, h] (zero when initial_state is
+ * NULL), over the kept tokens of b in order:
+ *     k^ = k / sqrt(|k|^2 + 1e-6),   q^ = scale q / sqrt(|q|^2 + 1e-6)
+ *     S  = exp(g) (S - beta (S k^) k^T) + beta v k^T,    o = S q^
+ * with S of shape [dv, dk]; value head h reads q/k head h / (hv / hk).
+ *
+ *   q, k   [n_kept, hk, dk] bf16 (16-byte aligned), dk in {64, 128}
+ *   v      [n_kept, hv, dv] bf16, hv a multiple of hk, 1 <= dv <= 1024
+ *   g      [n_kept, hv] fp32 log-decays (exp(g) in (0, 1] for g <= 0)
+ *   beta   [n_kept, hv] fp32 write strengths
+ *   cu_kept [batch+1] int32 (device), sequences of kept tokens
+ *   scale  positive (1/sqrt(dk) in the layer)
+ *   initial_state [batch, hv, dv, dk] fp32 or NULL
+ *   o      [n_kept, hv, dv] bf16 output
+ *   final_state   [batch, hv, dv, dk] fp32 output, or NULL
+ * fp32 state and arithmetic; o rounded once to bf16.  No workspace.
+ * Device-side errors: cu_kept out of range -> TG_ERR_DEVICE_INDEX.
+ */
+TG_API tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v,
+                              const float* g, const float* beta, const int32_t* cu_kept,
+                              int32_t batch, int64_t n_kept, int32_t hk, int32_t hv,
+                              int32_t dk, int32_t dv, float scale,
+                              const float* initial_state, void* o, float* final_state,
+                              cudaStream_t stream);
+
+/*
  * Dense projection for the layers above the gate (long-context workload: a
  * stack of token-gated attention layers, each with its own Q/K/V/O
  * projections):  out[m, n] = sum_k a[m, k] * w[n, k]  (+ residual[m, n])

@@ -499,6 +499,32 @@ tg_status tg_gated_attention_bwd(const void* q_rot, const void* k_rot, const voi
   return ok();
 }
 
+tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              const int32_t* cu_kept, int32_t batch, int64_t n_kept, int32_t hk, int32_t hv,
+                              int32_t dk, int32_t dv, float scale, const float* initial_state, void* o,
+                              float* final_state, cudaStream_t stream) {
+  if (batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
+  if (n_kept < 0 || n_kept > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_kept out of range");
+  if (hk < 1 || hv < 1 || hv % hk != 0) return fail(TG_ERR_INVALID_ARG, "hv must be a positive multiple of hk");
+  if (dk != 64 && dk != 128) return fail(TG_ERR_UNSUPPORTED, "dk must be 64 or 128");
+  if (dv < 1 || dv > 1024) return fail(TG_ERR_INVALID_ARG, "dv must be in [1, 1024]");
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return fail(TG_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (!cu_kept) return fail(TG_ERR_INVALID_ARG, "null cu_kept");
+  if (n_kept > 0 && (!q || !k || !v || !g || !beta || !o)) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (n_kept > 0 && (!aligned16(q) || !aligned16(k)))
+    return fail(TG_ERR_INVALID_ARG, "q and k must be 16-byte aligned");
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+  ScanArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_kept = cu_kept; a.batch = batch; a.n_kept = n_kept;
+  a.hk = hk; a.hv = hv; a.dk = dk; a.dv = dv; a.scale = scale; a.initial_state = initial_state; a.o = o;
+  a.final_state = final_state; a.status = di->status;
+  const cudaError_t e = launch_delta_scan(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gated delta scan launch");
+  return ok();
+}
+
 tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual, void* out, int64_t m, int32_t n,
                          int32_t kdim, cudaStream_t stream) {
   if (m < 0 || m > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "m out of range");

@@ -151,6 +151,25 @@ struct AttnBwdArgs {
 cudaError_t launch_attention_bwd(const CUtensorMap& map_q, const CUtensorMap& map_k, const CUtensorMap& map_v,
                                  const CUtensorMap& map_do, const AttnBwdArgs& a, cudaStream_t st);
 
+// ---- pruned Gated DeltaNet scan --------------------------------------------
+struct ScanArgs {
+  const void* q;              // [T, hk, dk] bf16
+  const void* k;              // [T, hk, dk] bf16
+  const void* v;              // [T, hv, dv] bf16
+  const float* g;             // [T, hv] log-decays
+  const float* beta;          // [T, hv]
+  const int32_t* cu_kept;
+  int32_t batch;
+  int64_t n_kept;
+  int32_t hk, hv, dk, dv;
+  float scale;
+  const float* initial_state; // [batch, hv, dv, dk] or null (zero)
+  void* o;                    // [T, hv, dv] bf16
+  float* final_state;         // [batch, hv, dv, dk] or null
+  unsigned int* status;
+};
+cudaError_t launch_delta_scan(const ScanArgs& a, cudaStream_t st);
+
 // ---- linear ----------------------------------------------------------------
 struct LinearArgs {
   const void* residual;

@@ -62,6 +62,8 @@ _SIGS = {
     "tg_gated_attention_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _i64, _i32, _i32,
                                _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp],
     "tg_attention_bwd_workspace_size": [_i64, _i32],
+    "tg_gated_delta_scan": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
+                            _vp],
     "tg_linear_bf16": [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp],
     "tg_check_device_status": [_vp],
     "tg_set_watchdog_cycles": [_ll],
@@ -369,6 +371,38 @@ def tg_gated_attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, po
                                       _ptr(workspace), workspace.numel(), _stream(stream)),
            "tg_gated_attention_fwd")
     return (o, lse) if lse is not None else o
+
+
+def tg_gated_delta_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                        cu_kept: torch.Tensor, scale: Optional[float] = None,
+                        initial_state: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
+                        final_state: Optional[torch.Tensor] = None, want_state: bool = False, stream=None):
+    """o [T, hv, dv] bf16 (and the final states [B, hv, dv, dk] fp32 when
+    requested or given): the gated delta rule over the kept tokens."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k, torch.bfloat16, "k", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    _need(g, torch.float32, "g", 2)
+    _need(beta, torch.float32, "beta", 2)
+    _need(cu_kept, torch.int32, "cu_kept", 1)
+    t, hk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    batch = cu_kept.shape[0] - 1
+    if k.shape != q.shape or v.shape[0] != t or g.shape != (t, hv) or beta.shape != (t, hv):
+        raise ValueError("k must match q; v [T, hv, dv]; g and beta [T, hv]")
+    if initial_state is not None:
+        _need(initial_state, torch.float32, "initial_state", 4)
+        if initial_state.shape != (batch, hv, dv, dk):
+            raise ValueError("initial_state must be [B, hv, dv, dk]")
+    if o is None:
+        o = torch.empty((t, hv, dv), dtype=torch.bfloat16, device=q.device)
+    if final_state is None and want_state:
+        final_state = torch.empty((batch, hv, dv, dk), dtype=torch.float32, device=q.device)
+    sc = (1.0 / dk ** 0.5) if scale is None else float(scale)
+    _check(lib.tg_gated_delta_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_kept), batch, t, hk, hv,
+                                   dk, dv, sc, _ptr(initial_state), _ptr(o), _ptr(final_state), _stream(stream)),
+           "tg_gated_delta_scan")
+    return (o, final_state) if final_state is not None else o
 
 
 def tg_linear_bf16(a: torch.Tensor, w: torch.Tensor, residual: Optional[torch.Tensor] = None,

@@ -123,6 +123,47 @@ def test_host_validation_rejects_before_launch(tg):
     assert rot(v=None) == tg.TG_ERR_INVALID_ARG
     assert rot(k=_c(264)) == tg.TG_ERR_INVALID_ARG
     assert rot(mk=0) == tg.TG_OK
+    # attention backward w.r.t. s, gain and tau
+    bw = dict(q=p, k=p, v=p, o=p, lse=p, do=p, pos=p, s=p, g=p, tau=1.0, cu=p, b=1, t=100, mk=100, hq=16, hkv=8,
+              d=128, ds=p, dg=p, dt=p, ws=p, wsb=1 << 30)
+
+    def bwd(**kw):
+        a = dict(bw, **kw)
+        return L.tg_gated_attention_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["pos"], a["s"], a["g"],
+                                        a["tau"], a["cu"], a["b"], a["t"], a["mk"], a["hq"], a["hkv"], a["d"],
+                                        a["ds"], a["dg"], a["dt"], a["ws"], a["wsb"], None)
+    assert bwd(hq=12, hkv=8) == tg.TG_ERR_INVALID_ARG
+    assert bwd(hq=18, hkv=2) == tg.TG_ERR_UNSUPPORTED        # more than 8 query heads per KV head
+    assert bwd(hq=512, hkv=64) == tg.TG_ERR_UNSUPPORTED      # more than 256 query heads
+    assert bwd(d=96) == tg.TG_ERR_UNSUPPORTED
+    assert bwd(tau=0.0) == tg.TG_ERR_INVALID_ARG
+    assert bwd(mk=-1) == tg.TG_ERR_INVALID_ARG
+    assert bwd(dg=None) == tg.TG_ERR_INVALID_ARG
+    assert bwd(ds=None) == tg.TG_ERR_INVALID_ARG
+    assert bwd(lse=None) == tg.TG_ERR_INVALID_ARG
+    assert bwd(do=_c(264)) == tg.TG_ERR_INVALID_ARG         # not 16-byte aligned
+    assert bwd(wsb=10) == tg.TG_ERR_WORKSPACE
+    assert bwd(ws=_c(272)) == tg.TG_ERR_INVALID_ARG          # not 256-byte aligned
+    assert L.tg_attention_bwd_workspace_size(100, 16) >= 5 * 100 * 16 * 4 + 16 * 64 * 4
+    assert L.tg_attention_bwd_workspace_size(0, 16) == 0
+    # pruned Gated DeltaNet scan
+    sc = dict(q=p, k=p, v=p, g=p, beta=p, cu=p, b=1, t=100, hk=16, hv=32, dk=128, dv=128, scale=0.088,
+              s0=None, o=p, s1=None)
+
+    def scan(**kw):
+        a = dict(sc, **kw)
+        return L.tg_gated_delta_scan(a["q"], a["k"], a["v"], a["g"], a["beta"], a["cu"], a["b"], a["t"], a["hk"],
+                                     a["hv"], a["dk"], a["dv"], a["scale"], a["s0"], a["o"], a["s1"], None)
+    assert scan(hv=24) == tg.TG_ERR_INVALID_ARG               # hv not a multiple of hk
+    assert scan(dk=96) == tg.TG_ERR_UNSUPPORTED
+    assert scan(dv=0) == tg.TG_ERR_INVALID_ARG
+    assert scan(scale=0.0) == tg.TG_ERR_INVALID_ARG
+    assert scan(scale=float("nan")) == tg.TG_ERR_INVALID_ARG
+    assert scan(b=0) == tg.TG_ERR_INVALID_ARG
+    assert scan(cu=None) == tg.TG_ERR_INVALID_ARG
+    assert scan(beta=None) == tg.TG_ERR_INVALID_ARG
+    assert scan(o=None) == tg.TG_ERR_INVALID_ARG
+    assert scan(k=_c(264)) == tg.TG_ERR_INVALID_ARG           # not 16-byte aligned
     # linear
     assert L.tg_linear_bf16(p, p, None, p, 10, 24, 64, None) == tg.TG_ERR_INVALID_ARG
     assert L.tg_linear_bf16(p, p, None, p, 10, 32, 96, None) == tg.TG_ERR_INVALID_ARG
