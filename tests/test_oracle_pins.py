@@ -832,3 +832,51 @@ def test_delta_scan_state_continues_across_calls():
                                      q_is_f64=True)
     np.testing.assert_allclose(np.concatenate([oa, ob]), o, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(Sb, S, rtol=1e-12, atol=1e-13)
+
+
+def _chunked_delta_scan(q, k, v, g, beta, cu, chunk, scale):
+    """The gated delta rule in its chunked (WY) form, derived from the
+    recurrence: within a chunk with decays gamma_i = exp(sum_{j<=i} g_j) and
+    entering state S0, the pseudo-values u_i = beta_i (v_i - alpha_i S_{i-1}
+    k_i) solve (I + A) U = beta V - (beta gamma K) S0^T with
+    A_ij = beta_i (gamma_i / gamma_j) k_i . k_j for j < i; then
+    O = (gamma Q) S0^T + (M o Q K^T) U (M_ij = gamma_i / gamma_j, j <= i) and
+    S <- gamma_C S0 + U^T ((gamma_C / gamma) K)."""
+    t, hk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    o = np.zeros((t, hv, dv))
+    kh_all = _unit(k)
+    qh_all = scale * _unit(q)
+    for b in range(len(cu) - 1):
+        for h in range(hv):
+            S = np.zeros((dv, dk))
+            kh = h // (hv // hk)
+            for c0 in range(cu[b], cu[b + 1], chunk):
+                c1 = min(cu[b + 1], c0 + chunk)
+                K, Q, V = kh_all[c0:c1, kh], qh_all[c0:c1, kh], v[c0:c1, h]
+                bt = beta[c0:c1, h]
+                G = np.cumsum(g[c0:c1, h])
+                ratio = np.exp(G[:, None] - G[None, :])
+                n = c1 - c0
+                A = np.tril(bt[:, None] * ratio * (K @ K.T), -1)
+                Tm = np.linalg.solve(np.eye(n) + A, np.eye(n))
+                U = Tm @ (bt[:, None] * V) - Tm @ ((bt * np.exp(G))[:, None] * K) @ S.T
+                o[c0:c1, h] = (np.exp(G)[:, None] * Q) @ S.T + (np.tril(ratio) * (Q @ K.T)) @ U
+                S = np.exp(G[-1]) * S + U.T @ (np.exp(G[-1] - G)[:, None] * K)
+    return o
+
+
+@pytest.mark.parametrize("chunk", [1, 4, 16, 64])
+def test_delta_scan_equals_chunked_wy_form(chunk):
+    """The recurrence equals its chunked form for any chunk size, on
+    sequences that are not multiples of the chunk."""
+    rng = np.random.default_rng(7)
+    lens = [70, 1, 0, 45]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    t, hk, hv, dk, dv = int(cu[-1]), 2, 4, 16, 8
+    q, k = rng.standard_normal((t, hk, dk)), rng.standard_normal((t, hk, dk))
+    v = rng.standard_normal((t, hv, dv))
+    g, beta = -rng.uniform(0, 0.5, (t, hv)), rng.uniform(0, 1, (t, hv))
+    o, _ = oracle.gated_delta_scan(q, k, v, g, beta, cu, scale=0.3, q_is_f64=True, l2_eps=0.0)
+    oc = _chunked_delta_scan(q, k, v, g, beta, cu, chunk, 0.3)
+    np.testing.assert_allclose(oc, o, rtol=1e-10, atol=1e-12)
