@@ -342,3 +342,46 @@ def deltanet_inputs(name: str) -> Dict[str, object]:
     beta = r.uniform(0.05, 0.95, size=(t, cfg["hv"])).astype(np.float32)
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "cu_kept": cu}
+
+
+# ---------------------------------------------------------------------------
+# synthetic Qwen3-style model for the pruned prefill and its decode step
+# ---------------------------------------------------------------------------
+_S_MODEL = 11
+
+MODEL_CONFIGS = {
+    # small enough for the float64 oracle; the layout of the full model
+    "model-tiny": {"n_layers": 4, "gate_layer": 1, "d": 128, "ffn": 256, "hq": 4, "hkv": 2, "head_dim": 64,
+                   "vocab": 500, "gate_h": 32},
+}
+
+
+def model_params(name: str) -> Dict[str, object]:
+    """Seeded weights (bf16 bits) of a synthetic model: per layer ln1, ln2,
+    q_norm, k_norm ~ 1 + N(0, 0.1^2); w_q, w_k, w_v, w_o, w_gate, w_up,
+    w_down ~ N(0, 1/fan_in); layers above the gate get gain ~ U(0.5, 2) and
+    tau ~ U(0.9, 1.3); the gate MLP as gate_weights; final norm and an LM
+    head ~ N(0, 1/d)."""
+    c = MODEL_CONFIGS[name]
+    r = np.random.default_rng(np.random.SeedSequence([BASE_SEED, _S_MODEL, c["d"], c["n_layers"]]))
+    d, f, hq, hkv, dh = c["d"], c["ffn"], c["hq"], c["hkv"], c["head_dim"]
+    norm = lambda n: f32_to_bf16_bits((1.0 + 0.1 * r.standard_normal(n)).astype(np.float32))
+    layers = []
+    for li in range(c["n_layers"]):
+        layers.append({
+            "ln1": norm(d), "ln2": norm(d), "q_norm": norm(dh), "k_norm": norm(dh),
+            "w_q": _normal_bf16(r, (hq * dh, d), 1.0 / np.sqrt(d)),
+            "w_k": _normal_bf16(r, (hkv * dh, d), 1.0 / np.sqrt(d)),
+            "w_v": _normal_bf16(r, (hkv * dh, d), 1.0 / np.sqrt(d)),
+            "w_o": _normal_bf16(r, (d, hq * dh), 1.0 / np.sqrt(hq * dh)),
+            "w_gate": _normal_bf16(r, (f, d), 1.0 / np.sqrt(d)),
+            "w_up": _normal_bf16(r, (f, d), 1.0 / np.sqrt(d)),
+            "w_down": _normal_bf16(r, (d, f), 1.0 / np.sqrt(f)),
+            "gain": r.uniform(0.5, 2.0, size=hq).astype(np.float32),
+            "tau": float(np.float32(r.uniform(0.9, 1.3))),
+        })
+    gate = {"w1": _normal_bf16(r, (c["gate_h"], d), 1.0 / np.sqrt(d)),
+            "w2": _normal_bf16(r, (c["gate_h"],), 1.0 / np.sqrt(c["gate_h"])),
+            "b1": np.zeros(c["gate_h"], np.float32), "b2": 0.0}
+    return {"config": c, "layers": layers, "gate": gate, "final_norm": norm(d),
+            "w_lm": _normal_bf16(r, (c["vocab"], d), 1.0 / np.sqrt(d))}
