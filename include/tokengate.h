@@ -320,6 +320,46 @@ TG_API tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v
                               cudaStream_t stream);
 
 /*
+ * The layer around the pruned path, for the whole pruned prefill and its
+ * first decode step (the three phases of "How does TokenGate's learned token
+ * pruning work?"; the model is Qwen3, "How does TokenGate perform on the
+ * benchmarks?").  Not part of the pruned path itself.
+ *
+ * tg_rms_norm: y = x / sqrt(mean(x^2) + eps) * w for each of `rows` rows of
+ *   length d (x, y [rows, d] bf16, w [d] bf16; 16-byte aligned; d a multiple
+ *   of 8).  With rows = T * heads and d = head_dim it is the per-head
+ *   QK-norm.  fp32 arithmetic, one rounding to bf16.
+ *
+ * tg_swiglu: y = SiLU(a) * b with a = gate_up[:, :f], b = gate_up[:, f:]
+ *   (gate_up [rows, 2f] bf16, the fused gate/up projection; y [rows, f]
+ *   bf16; f a multiple of 8; 16-byte aligned).
+ *
+ * tg_decode_attention: one new query per sequence (the first decode step).
+ *   Sequence b's new token attends the rows [cache_cu[b], cache_cu[b+1]) of
+ *   the cache and its own key, with logits (q' . k'_j) / (sqrt(D) tau) +
+ *   gain_h s_j (the new token's own score is 0; s_cache and gain NULL: no
+ *   bias, as in the layers at or below the gate).  q_rot [B, hq, D],
+ *   k_new_rot and v_new [B, hkv, D], k_cache (rotated) and v_cache
+ *   [cache_rows, hkv, D], all bf16; s_cache [cache_rows] fp32; gain [hq]
+ *   fp32; o [B, hq, D] bf16 output.  max_cache_len: host bound on every
+ *   sequence's cache length (sizes the split of the cache over CTAs).
+ *   hq / hkv <= 8, head_dim 64 or 128.  Workspace of
+ *   tg_decode_workspace_size(...) bytes, 16-byte aligned.  fp32 arithmetic.
+ */
+TG_API tg_status tg_rms_norm(const void* x, const void* w, int64_t rows, int32_t d, float eps,
+                      void* y, cudaStream_t stream);
+TG_API tg_status tg_swiglu(const void* gate_up, int64_t rows, int32_t f, void* y,
+                    cudaStream_t stream);
+TG_API size_t tg_decode_workspace_size(int32_t batch, int32_t hq, int32_t head_dim,
+                                int32_t max_cache_len);
+TG_API tg_status tg_decode_attention(const void* q_rot, const void* k_new_rot, const void* v_new,
+                              const void* k_cache, const void* v_cache,
+                              const int32_t* cache_cu, int32_t batch, int64_t cache_rows,
+                              int32_t max_cache_len, const float* s_cache, const float* gain,
+                              float tau, int32_t hq, int32_t hkv, int32_t head_dim, void* o,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Dense projection for the layers above the gate (long-context workload: a
  * stack of token-gated attention layers, each with its own Q/K/V/O
  * projections):  out[m, n] = sum_k a[m, k] * w[n, k]  (+ residual[m, n])

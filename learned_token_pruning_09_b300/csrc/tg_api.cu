@@ -525,6 +525,77 @@ tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v, const
   return ok();
 }
 
+tg_status tg_rms_norm(const void* x, const void* w, int64_t rows, int32_t d, float eps, void* y,
+                      cudaStream_t stream) {
+  if (rows < 0) return fail(TG_ERR_INVALID_ARG, "rows must be >= 0");
+  if (d < 8 || d % 8 != 0 || d > (1 << 16)) return fail(TG_ERR_INVALID_ARG, "d must be a multiple of 8 in [8, 65536]");
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(TG_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (rows == 0) return ok();
+  if (!x || !w || !y) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return fail(TG_ERR_INVALID_ARG, "x, w and y must be 16-byte aligned");
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+  const cudaError_t e = launch_rms_norm(x, w, rows, d, eps, y, di->num_sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "RMSNorm launch");
+  return ok();
+}
+
+tg_status tg_swiglu(const void* gate_up, int64_t rows, int32_t f, void* y, cudaStream_t stream) {
+  if (rows < 0) return fail(TG_ERR_INVALID_ARG, "rows must be >= 0");
+  if (f < 8 || f % 8 != 0) return fail(TG_ERR_INVALID_ARG, "f must be a positive multiple of 8");
+  if (rows == 0) return ok();
+  if (!gate_up || !y) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(gate_up) || !aligned16(y)) return fail(TG_ERR_INVALID_ARG, "gate_up and y must be 16-byte aligned");
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+  const cudaError_t e = launch_swiglu(gate_up, rows, f, y, di->num_sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "SwiGLU launch");
+  return ok();
+}
+
+size_t tg_decode_workspace_size(int32_t batch, int32_t hq, int32_t head_dim, int32_t max_cache_len) {
+  if (batch <= 0 || hq <= 0 || head_dim <= 0 || max_cache_len < 0) return 0;
+  const long long n_split = max_cache_len > 0 ? (static_cast<long long>(max_cache_len) + kDecodeSplit - 1) / kDecodeSplit : 1;
+  return static_cast<size_t>(batch) * hq * n_split * (head_dim + 2) * 4;
+}
+
+tg_status tg_decode_attention(const void* q_rot, const void* k_new_rot, const void* v_new, const void* k_cache,
+                              const void* v_cache, const int32_t* cache_cu, int32_t batch, int64_t cache_rows,
+                              int32_t max_cache_len, const float* s_cache, const float* gain, float tau, int32_t hq,
+                              int32_t hkv, int32_t head_dim, void* o, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+  if (batch < 0) return fail(TG_ERR_INVALID_ARG, "batch must be >= 0");
+  if (cache_rows < 0 || cache_rows > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "cache_rows out of range");
+  if (max_cache_len < 0) return fail(TG_ERR_INVALID_ARG, "max_cache_len must be >= 0");
+  if (hq < 1 || hkv < 1 || hq % hkv != 0) return fail(TG_ERR_INVALID_ARG, "hq must be a positive multiple of hkv");
+  if (hq / hkv > kDecodeMaxGroup) return fail(TG_ERR_UNSUPPORTED, "hq / hkv must be at most %d", kDecodeMaxGroup);
+  if (head_dim != 64 && head_dim != 128) return fail(TG_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (!(tau > 0.0f) || !std::isfinite(tau)) return fail(TG_ERR_INVALID_ARG, "tau must be positive and finite");
+  if (batch == 0) return ok();
+  if (!q_rot || !k_new_rot || !v_new || !cache_cu || !o) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (cache_rows > 0 && (!k_cache || !v_cache)) return fail(TG_ERR_INVALID_ARG, "null cache");
+  if ((s_cache == nullptr) != (gain == nullptr)) return fail(TG_ERR_INVALID_ARG, "s_cache and gain go together");
+  const size_t need = tg_decode_workspace_size(batch, hq, head_dim, max_cache_len);
+  if (!workspace || workspace_bytes < need)
+    return fail(TG_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (!aligned16(workspace)) return fail(TG_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+  DecodeArgs a{};
+  a.q = q_rot; a.k_new = k_new_rot; a.v_new = v_new; a.k_cache = k_cache; a.v_cache = v_cache; a.cache_cu = cache_cu;
+  a.s_cache = s_cache; a.gain = gain; a.batch = batch; a.cache_rows = cache_rows; a.hq = hq; a.hkv = hkv;
+  a.head_dim = head_dim; a.split_len = kDecodeSplit;
+  a.n_split = max_cache_len > 0 ? (max_cache_len + kDecodeSplit - 1) / kDecodeSplit : 1;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / (std::sqrt(static_cast<double>(head_dim)) * tau));
+  a.part = static_cast<float*>(workspace); a.o = o; a.status = di->status;
+  const cudaError_t e = launch_decode_attention(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+  return ok();
+}
+
 tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual, void* out, int64_t m, int32_t n,
                          int32_t kdim, cudaStream_t stream) {
   if (m < 0 || m > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "m out of range");

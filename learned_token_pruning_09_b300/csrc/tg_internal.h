@@ -170,6 +170,32 @@ struct ScanArgs {
 };
 cudaError_t launch_delta_scan(const ScanArgs& a, cudaStream_t st);
 
+// ---- the layer around the pruned path: norms, SwiGLU, decode attention -----
+cudaError_t launch_rms_norm(const void* x, const void* w, long long rows, int d, float eps, void* y, int num_sms,
+                            cudaStream_t st);
+cudaError_t launch_swiglu(const void* gate_up, long long rows, int f, void* y, int num_sms, cudaStream_t st);
+constexpr int kDecodeMaxGroup = 8;   // query heads per KV head
+constexpr int kDecodeSplit = 256;    // cache rows per CTA
+struct DecodeArgs {
+  const void* q;          // [B, hq, D] bf16, rotated
+  const void* k_new;      // [B, hkv, D] bf16, rotated
+  const void* v_new;      // [B, hkv, D] bf16
+  const void* k_cache;    // [cache_rows, hkv, D] bf16, rotated
+  const void* v_cache;    // [cache_rows, hkv, D] bf16
+  const int32_t* cache_cu;
+  const float* s_cache;   // [cache_rows] or null (no score bias)
+  const float* gain;      // [hq] or null
+  int32_t batch;
+  int64_t cache_rows;
+  int32_t hq, hkv, head_dim;
+  int32_t split_len, n_split;
+  float scale_log2;       // log2(e) / (sqrt(D) tau)
+  float* part;            // [B, hq, n_split, D + 2] workspace
+  void* o;                // [B, hq, D] bf16
+  unsigned int* status;
+};
+cudaError_t launch_decode_attention(const DecodeArgs& a, cudaStream_t st);
+
 // ---- linear ----------------------------------------------------------------
 struct LinearArgs {
   const void* residual;

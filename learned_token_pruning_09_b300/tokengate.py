@@ -62,6 +62,11 @@ _SIGS = {
     "tg_gated_attention_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _i64, _i32, _i32,
                                _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp],
     "tg_attention_bwd_workspace_size": [_i64, _i32],
+    "tg_rms_norm": [_vp, _vp, _i64, _i32, _f32, _vp, _vp],
+    "tg_swiglu": [_vp, _i64, _i32, _vp, _vp],
+    "tg_decode_workspace_size": [_i32, _i32, _i32, _i32],
+    "tg_decode_attention": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _vp, _vp, _f32, _i32, _i32, _i32, _vp,
+                            _vp, _sz, _vp],
     "tg_gated_delta_scan": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
                             _vp],
     "tg_linear_bf16": [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp],
@@ -76,6 +81,7 @@ for _name, _args in _SIGS.items():
     _f.restype = ctypes.c_int
 lib.tg_attention_workspace_size.restype = ctypes.c_size_t
 lib.tg_attention_bwd_workspace_size.restype = ctypes.c_size_t
+lib.tg_decode_workspace_size.restype = ctypes.c_size_t
 lib.tg_last_error_string.restype = ctypes.c_char_p
 lib.tg_version.restype = ctypes.c_char_p
 lib.tg_set_watchdog_cycles.restype = None
@@ -403,6 +409,62 @@ def tg_gated_delta_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: to
                                    dk, dv, sc, _ptr(initial_state), _ptr(o), _ptr(final_state), _stream(stream)),
            "tg_gated_delta_scan")
     return (o, final_state) if final_state is not None else o
+
+
+def tg_rms_norm(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, y: Optional[torch.Tensor] = None,
+                stream=None):
+    """y = RMSNorm(x) * w over the last dimension (bf16); x of any shape
+    whose last dimension is w's length."""
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w", 1)
+    d = w.shape[0]
+    if x.shape[-1] != d:
+        raise ValueError("the last dimension of x must be len(w)")
+    y = torch.empty_like(x) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    _check(lib.tg_rms_norm(_ptr(x), _ptr(w), x.numel() // d, d, float(eps), _ptr(y), _stream(stream)), "tg_rms_norm")
+    return y
+
+
+def tg_swiglu(gate_up: torch.Tensor, y: Optional[torch.Tensor] = None, stream=None):
+    """SiLU(gate_up[:, :f]) * gate_up[:, f:] (bf16 [rows, 2f] -> [rows, f])."""
+    _need(gate_up, torch.bfloat16, "gate_up", 2)
+    rows, f2 = gate_up.shape
+    if f2 % 2:
+        raise ValueError("gate_up must have an even number of columns")
+    f = f2 // 2
+    y = torch.empty((rows, f), dtype=torch.bfloat16, device=gate_up.device) if y is None else y
+    _need(y, torch.bfloat16, "y", 2)
+    _check(lib.tg_swiglu(_ptr(gate_up), rows, f, _ptr(y), _stream(stream)), "tg_swiglu")
+    return y
+
+
+def tg_decode_attention(q_rot: torch.Tensor, k_new_rot: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                        v_cache: torch.Tensor, cache_cu: torch.Tensor, max_cache_len: int,
+                        s_cache: Optional[torch.Tensor] = None, gain: Optional[torch.Tensor] = None,
+                        tau: float = 1.0, o: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None):
+    """o [B, hq, D] bf16: each sequence's new query over its cache rows and
+    its own key (score bias when s_cache and gain are given)."""
+    for t_, n_ in ((q_rot, "q_rot"), (k_new_rot, "k_new_rot"), (v_new, "v_new"), (k_cache, "k_cache"),
+                   (v_cache, "v_cache")):
+        _need(t_, torch.bfloat16, n_, 3)
+    _need(cache_cu, torch.int32, "cache_cu", 1)
+    if s_cache is not None:
+        _need(s_cache, torch.float32, "s_cache", 1)
+    if gain is not None:
+        _need(gain, torch.float32, "gain", 1)
+    b, hq, dh = q_rot.shape
+    hkv = k_new_rot.shape[1]
+    o = torch.empty_like(q_rot) if o is None else o
+    need = lib.tg_decode_workspace_size(b, hq, dh, int(max_cache_len))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_rot.device)
+    _check(lib.tg_decode_attention(_ptr(q_rot), _ptr(k_new_rot), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(cache_cu), b, k_cache.shape[0], int(max_cache_len), _ptr(s_cache), _ptr(gain),
+                                   float(tau), hq, hkv, dh, _ptr(o), _ptr(workspace), workspace.numel(),
+                                   _stream(stream)), "tg_decode_attention")
+    return o
 
 
 def tg_linear_bf16(a: torch.Tensor, w: torch.Tensor, residual: Optional[torch.Tensor] = None,

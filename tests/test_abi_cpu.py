@@ -164,6 +164,33 @@ def test_host_validation_rejects_before_launch(tg):
     assert scan(beta=None) == tg.TG_ERR_INVALID_ARG
     assert scan(o=None) == tg.TG_ERR_INVALID_ARG
     assert scan(k=_c(264)) == tg.TG_ERR_INVALID_ARG           # not 16-byte aligned
+    # the layer around the path: norms, SwiGLU, decode attention
+    assert L.tg_rms_norm(p, p, 10, 12, 1e-6, p, None) == tg.TG_ERR_INVALID_ARG       # d not a multiple of 8
+    assert L.tg_rms_norm(p, p, 10, 64, -1.0, p, None) == tg.TG_ERR_INVALID_ARG       # negative eps
+    assert L.tg_rms_norm(p, None, 10, 64, 1e-6, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_rms_norm(_c(264), p, 10, 64, 1e-6, p, None) == tg.TG_ERR_INVALID_ARG  # not 16-byte aligned
+    assert L.tg_rms_norm(p, p, 0, 64, 1e-6, p, None) == tg.TG_OK
+    assert L.tg_swiglu(p, 10, 12, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_swiglu(p, 10, 64, None, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_swiglu(p, 0, 64, p, None) == tg.TG_OK
+    dargs = dict(q=p, kn=p, vn=p, kc=p, vc=p, cu=p, b=2, rows=100, ml=60, s=None, g=None, tau=1.0, hq=16, hkv=8,
+                 d=128, o=p, ws=p, wsb=1 << 30)
+
+    def dec(**kw):
+        a = dict(dargs, **kw)
+        return L.tg_decode_attention(a["q"], a["kn"], a["vn"], a["kc"], a["vc"], a["cu"], a["b"], a["rows"],
+                                     a["ml"], a["s"], a["g"], a["tau"], a["hq"], a["hkv"], a["d"], a["o"], a["ws"],
+                                     a["wsb"], None)
+    assert dec(hq=12) == tg.TG_ERR_INVALID_ARG
+    assert dec(hq=18, hkv=2) == tg.TG_ERR_UNSUPPORTED
+    assert dec(d=96) == tg.TG_ERR_UNSUPPORTED
+    assert dec(tau=0.0) == tg.TG_ERR_INVALID_ARG
+    assert dec(s=p) == tg.TG_ERR_INVALID_ARG                 # s_cache without gain
+    assert dec(kc=None) == tg.TG_ERR_INVALID_ARG
+    assert dec(wsb=8) == tg.TG_ERR_WORKSPACE
+    assert dec(b=0) == tg.TG_OK
+    assert L.tg_decode_workspace_size(2, 16, 128, 600) == 2 * 16 * 3 * 130 * 4
+    assert L.tg_decode_workspace_size(2, 16, 128, 0) == 2 * 16 * 1 * 130 * 4
     # linear
     assert L.tg_linear_bf16(p, p, None, p, 10, 24, 64, None) == tg.TG_ERR_INVALID_ARG
     assert L.tg_linear_bf16(p, p, None, p, 10, 32, 96, None) == tg.TG_ERR_INVALID_ARG
