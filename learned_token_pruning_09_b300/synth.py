@@ -352,7 +352,7 @@ _S_MODEL = 11
 MODEL_CONFIGS = {
     # small enough for the float64 oracle; the layout of the full model
     "model-tiny": {"n_layers": 4, "gate_layer": 1, "d": 128, "ffn": 256, "hq": 4, "hkv": 2, "head_dim": 64,
-                   "vocab": 500, "gate_h": 32},
+                   "vocab": 512, "gate_h": 32},
 }
 
 
