@@ -98,8 +98,10 @@ def test_scan_pruned_tokens_are_skipped(tg):
     sub = {key: d[key][kept] for key in ("q", "k", "v", "g", "beta")}
     sub["cu_kept"] = np.array([0, len(kept)], np.int32)
     o_k, s_k = run_scan(tg, sub)
-    np.testing.assert_allclose(o_all[kept], o_k, rtol=0, atol=1e-6)
-    np.testing.assert_allclose(s_all, s_k, rtol=0, atol=1e-6)
+    # a pruned token that touched the state would move o by ~0.1; the bound
+    # leaves room for exp(0) evaluated one ulp away from 1 on every pruned token
+    np.testing.assert_allclose(o_all[kept], o_k, rtol=0, atol=O_ATOL)
+    np.testing.assert_allclose(s_all, s_k, rtol=0, atol=S_REL * max(np.abs(s_k).max(), 1e-6))
 
 
 def test_scan_rejects_bad_sequences(tg):
