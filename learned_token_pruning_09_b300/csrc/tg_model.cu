@@ -136,7 +136,9 @@ decode_partial_kernel(DecodeArgs a) {
   const int warp = warp_id(), lane = lane_id();
   const int group = a.hq / a.hkv;
   const int lo = __ldg(a.cache_cu + b), hi = __ldg(a.cache_cu + b + 1);
-  if (lo < 0 || hi < lo || hi > a.cache_rows) {
+  // a sequence longer than the slices cover (max_cache_len too small) is flagged, not cut short
+  if (lo < 0 || hi < lo || hi > a.cache_rows ||
+      static_cast<long long>(hi - lo) > static_cast<long long>(a.n_split) * a.split_len) {
     if (threadIdx.x == 0) record_error(a.status, kStatusIndex);
     return;
   }
