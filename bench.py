@@ -264,9 +264,18 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 
-def make_inputs(shape):
+_RESIDUALS = {}
+
+
+def make_inputs(shape, with_scores=True):
     from learned_token_pruning_09_b300 import synth
-    inp = {"x": synth.residuals(shape), "p": synth.gate_weights(shape), "s_draw": synth.score_draws(shape)}
+    key = (shape.seed, shape.n_rows, shape.d)     # the budget sweep's three workloads share theirs
+    if key not in _RESIDUALS:
+        _RESIDUALS.clear()
+        _RESIDUALS[key] = synth.residuals(shape)
+    inp = {"x": _RESIDUALS[key], "p": synth.gate_weights(shape)}
+    if with_scores:
+        inp["s_draw"] = synth.score_draws(shape)
     if shape.with_proj:
         inp["layers"] = [synth.layer_params(shape, i) for i in range(shape.n_layers)]
     else:
@@ -316,12 +325,55 @@ def oracle_step_sample(shape, inputs, rng, n_gate_rows=256, n_attn_rows=16):
     return dt, flops
 
 
+def _openblas():
+    """numpy's OpenBLAS, loaded in this process, and its thread-count calls
+    (the exported names carry a prefix and suffix in numpy's own build)."""
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            paths = sorted({ln.split()[-1] for ln in f if "openblas" in ln and ln.rstrip().endswith(".so")})
+    except OSError:
+        return None
+    for path in paths:
+        lib = ctypes.CDLL(path)
+        for pre, suf in (("scipy_", "64_"), ("", "64_"), ("", "")):
+            get, put = f"{pre}openblas_get_num_threads{suf}", f"{pre}openblas_set_num_threads{suf}"
+            if hasattr(lib, get) and hasattr(lib, put):
+                return getattr(lib, get), getattr(lib, put)
+    return None
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
         return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        return os.cpu_count() or 1
+    except ImportError:
+        ob = _openblas()
+        return int(ob[0]()) if ob else (os.cpu_count() or 1)
+
+
+class single_thread:
+    """The oracle timed as a single-threaded program: numpy's BLAS pool held
+    at one thread while inside (the oracle itself is plain serial code)."""
+
+    def __enter__(self):
+        self.lim, self.ob, self.old = None, None, None
+        try:
+            from threadpoolctl import threadpool_limits
+            self.lim = threadpool_limits(limits=1)
+        except ImportError:
+            self.ob = _openblas()
+            if self.ob:
+                self.old = int(self.ob[0]())
+                self.ob[1](1)
+        return self
+
+    def __exit__(self, *exc):
+        if self.lim is not None:
+            self.lim.restore_original_limits()
+        elif self.ob:
+            self.ob[1](self.old)
+        return False
 
 
 def cpu_model():
@@ -345,13 +397,15 @@ def run_reference(args, shape):
         return 0
     inputs = make_inputs(shape)
     rng = np.random.default_rng(0)
-    for _ in range(args.warmup):
-        oracle_step_sample(shape, inputs, rng, 16, 1)
-    tot_t, tot_f = 0.0, 0.0
-    for _ in range(args.steps):
-        dt, fl = oracle_step_sample(shape, inputs, rng)
-        tot_t += dt
-        tot_f += fl
+    with single_thread():
+        for _ in range(args.warmup):
+            oracle_step_sample(shape, inputs, rng, 16, 1)
+        tot_t, tot_f = 0.0, 0.0
+        for _ in range(args.steps):
+            dt, fl = oracle_step_sample(shape, inputs, rng)
+            tot_t += dt
+            tot_f += fl
+        cores = blas_threads()
     val = tot_f / tot_t / 1e12
     sample = "per step: " + SAMPLE_TEXT.format(proj=" (with its K/V projections of every kept row)"
                                                if shape.with_proj else "")
@@ -359,7 +413,7 @@ def run_reference(args, shape):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(shape),
-            "cpu_baseline": {"value": val, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample, "cpu": cpu_model()},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -470,6 +524,153 @@ class Path:
         return n
 
 
+def capture_step(segs):
+    """The calls of one step captured as one CUDA graph, with a timing event
+    recorded before each call and after the last, so that no launch gap sits
+    between two kernels and each call's device time can be read back."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(segs) + 1)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for k, (_, f) in enumerate(segs):
+            evs[k].record()
+            f()
+        evs[-1].record()
+    torch.cuda.synchronize()
+    return graph, evs
+
+
+def replay_timed(graph, evs, flush, steps):
+    """Replays the step ``steps`` times, L2 flushed before each, and returns
+    the per-call device times [steps, calls] in ms."""
+    import torch
+    per = []
+    for _ in range(steps):
+        flush.zero_()
+        graph.replay()
+        torch.cuda.synchronize()     # the events are re-recorded by the next replay
+        per.append([evs[k].elapsed_time(evs[k + 1]) for k in range(len(evs) - 1)])
+    return np.array(per)
+
+
+# the other workloads of the metric, each measured as one single-layer step
+SIDE_WORKLOADS = ("qwen3-1.7b-16k", "budget-32k-k1024", "budget-32k-k4096", "budget-32k-k8192", "ragged-8")
+
+
+def measure_workload(name, dev, flush, steps, peaks):
+    """One workload's step (gate, top-K, gather, RoPE, token-gated attention
+    on seeded q/k/v), captured and timed like the headline step."""
+    import torch
+    from learned_token_pruning_09_b300 import synth
+    shape = synth.ALL_SHAPES[name]()
+    P = Path(shape, make_inputs(shape, with_scores=False), dev)
+    tg = P.tg
+    segs = P.segments()
+    for _, f in segs:
+        f()
+    torch.cuda.synchronize()
+    if tg.tg_check_device_status() != tg.TG_OK:
+        raise RuntimeError(f"device status ({name}): " + tg.lib.tg_last_error_string().decode())
+    graph, evs = capture_step(segs)
+    replay_timed(graph, evs, flush, 3)
+    seg = dict(zip([n for n, _ in segs], replay_timed(graph, evs, flush, steps).mean(axis=0)))
+    if tg.tg_check_device_status() != tg.TG_OK:
+        raise RuntimeError(f"device status ({name}): " + tg.lib.tg_last_error_string().decode())
+    fl = attention_flops(shape.kept_lens, shape.hq, shape.head_dim)
+    attn_ms = seg["rope0"] + seg["attn0"]
+    gtg_ms = seg["gate"] + seg["topk"] + seg["gather"]
+    byts = path_bytes(shape)
+    out = {"batch": shape.batch, "n_rows": shape.n_rows, "kept_tokens": shape.n_kept,
+           "attention": {"ms_per_layer": attn_ms, "tflops": fl / (attn_ms * 1e-3) / 1e12,
+                         "kernel_ms": seg["attn0"], "kernel_tflops": fl / (seg["attn0"] * 1e-3) / 1e12,
+                         "kernel_frac_of_burst": fl / (seg["attn0"] * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                         "rope_us": seg["rope0"] * 1e3, "gflop": fl / 1e9},
+           "gate_topk_gather": {"us": gtg_ms * 1e3, "gbs": byts / (gtg_ms * 1e-3) / 1e9, "bytes": byts,
+                                "frac_of_measured_hbm": byts / (gtg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                "gate_us": seg["gate"] * 1e3, "topk_us": seg["topk"] * 1e3,
+                                "gather_us": seg["gather"] * 1e3}}
+    del P, graph
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_model_ttft(dev, flush, steps):
+    """Synthetic time to first token and peak prefill memory of a model with
+    Qwen3-1.7B's layout and random weights: TokenGate's pruned prefill
+    (gate at layer 1, 27 layers on the kept tokens) against the full prefill
+    (every layer on every token), each followed by the first decode step.
+    Everything runs eagerly through the public Python API, as a user calls
+    it: TTFT is the device time from the first call of the prefill to the
+    logits of the first token (host launch gaps included)."""
+    import torch
+    from learned_token_pruning_09_b300 import synth
+    from learned_token_pruning_09_b300.model import SyntheticModel
+    model = SyntheticModel(synth.model_params_device("qwen3-1.7b", dev), device=dev)
+    c = model.cfg
+    torch.cuda.synchronize()
+    weights = torch.cuda.memory_allocated()
+    out = {"model": "Qwen3-1.7B layout, random weights", "layers": c["n_layers"], "gate_layer": c["gate_layer"] + 1,
+           "weights_gb": weights / 1e9, "contexts": {}}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(synth.BASE_SEED + 51)
+    for ctx, (n_doc, n_q, k) in synth.MODEL_CONTEXTS.items():
+        n = n_doc + n_q
+        x = torch.randn((n, c["d"]), generator=gen, device=dev).to(torch.bfloat16)
+        x_new = torch.randn((1, c["d"]), generator=gen, device=dev).to(torch.bfloat16)
+        res = {"n_doc": n_doc, "n_q": n_q, "k": k}
+        for mode in ("pruned", "full"):
+            run = ((lambda: model.prefill(x, [n], [n_doc], [k])) if mode == "pruned"
+                   else (lambda: model.prefill_full(x, [n])))
+            st = run()
+            model.decode(x_new, st)
+            del st
+            torch.cuda.synchronize()
+            ttft, dec, peak = [], [], []
+            for _ in range(steps):
+                flush.zero_()
+                torch.cuda.synchronize()
+                base = torch.cuda.memory_allocated()
+                torch.cuda.reset_peak_memory_stats()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                e[0].record()
+                st = run()
+                e[1].record()
+                torch.cuda.synchronize()
+                peak.append(torch.cuda.max_memory_allocated() - base)
+                e[2].record()
+                model.decode(x_new, st)
+                e[3].record()
+                torch.cuda.synchronize()
+                ttft.append(e[0].elapsed_time(e[1]))
+                dec.append(e[2].elapsed_time(e[3]))
+                del st
+            res[mode] = {"ttft_ms": float(np.mean(ttft)), "decode_ms": float(np.mean(dec)),
+                         "peak_prefill_gb": float(np.max(peak)) / 1e9,
+                         "peak_prefill_gb_with_weights": (float(np.max(peak)) + weights) / 1e9}
+            torch.cuda.empty_cache()
+        if model_status_bad(model):
+            raise RuntimeError("device status after the model runs: " + tg_error())
+        res["ttft_speedup"] = res["full"]["ttft_ms"] / res["pruned"]["ttft_ms"]
+        res["peak_memory_ratio"] = res["full"]["peak_prefill_gb"] / res["pruned"]["peak_prefill_gb"]
+        res["peak_memory_ratio_with_weights"] = (res["full"]["peak_prefill_gb_with_weights"] /
+                                                 res["pruned"]["peak_prefill_gb_with_weights"])
+        out["contexts"][ctx] = res
+        del x, x_new
+    del model
+    torch.cuda.empty_cache()
+    return out
+
+
+def model_status_bad(model):
+    from learned_token_pruning_09_b300 import tokengate as tg
+    return tg.tg_check_device_status() != tg.TG_OK
+
+
+def tg_error():
+    from learned_token_pruning_09_b300 import tokengate as tg
+    return tg.lib.tg_last_error_string().decode()
+
+
 def run_gpu(args, shape):
     import torch
     import torch.distributed as dist
@@ -496,22 +697,10 @@ def run_gpu(args, shape):
         raise RuntimeError("device status after warm-up: " + tg.lib.tg_last_error_string().decode())
     # The whole step is one CUDA graph, with timing events recorded inside it
     # between the segments, so that no launch gap sits between two kernels.
-    nseg = len(segs)
     names = [n for n, _ in segs]
-    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nseg + 1)]
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for k, (_, f) in enumerate(segs):
-            evs[k].record()
-            f()
-        evs[-1].record()
-    torch.cuda.synchronize()
+    graph, evs = capture_step(segs)
     stream = torch.cuda.current_stream()
-
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        graph.replay()
-    torch.cuda.synchronize()
+    replay_timed(graph, evs, flush, max(args.warmup, 3))
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -519,19 +708,13 @@ def run_gpu(args, shape):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    per = []
-    for i in range(args.steps):
-        flush.zero_()
-        graph.replay()
-        torch.cuda.synchronize()     # the events are re-recorded by the next replay
-        per.append([evs[k].elapsed_time(evs[k + 1]) for k in range(nseg)])
+    per = replay_timed(graph, evs, flush, args.steps)
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
     if tg.tg_check_device_status() != tg.TG_OK:
         raise RuntimeError("device status after timed steps: " + tg.lib.tg_last_error_string().decode())
 
-    per = np.array(per)
     seg_ms = dict(zip(names, per.mean(axis=0)))
     step_ms = float(per.sum(axis=1).mean())
     # the token-gated attention layer: its RoPE prologue and the attention kernel
@@ -555,6 +738,14 @@ def run_gpu(args, shape):
     # ---- attention backward w.r.t. s, gain and tau (the next row after that) ----
     bwd = measure_attn_bwd(P, shape, flush, args.steps)
     bwd["frac_of_burst"] = bwd["tflops"] / peaks["bf16_tflops"]
+
+    # ---- the metric's other workloads, and the synthetic model's TTFT ----
+    workloads, model_ttft = None, None
+    if not args.headline_only:
+        del graph
+        torch.cuda.empty_cache()
+        workloads = {n: measure_workload(n, dev, flush, args.steps, peaks) for n in SIDE_WORKLOADS}
+        model_ttft = measure_model_ttft(dev, flush, 2)
 
     # ---- end to end through the public API, host buffers ----
     import torch as _t
@@ -596,10 +787,12 @@ def run_gpu(args, shape):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rng = np.random.default_rng(0)
         tt, ff, ns = 0.0, 0.0, 0
-        while tt < args.cpu_seconds:
-            dt, fl = oracle_step_sample(shape, inputs, rng)
-            tt, ff, ns = tt + dt, ff + fl, ns + 1
-        cpu = {"value": ff / tt / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+        with single_thread():
+            while tt < args.cpu_seconds:
+                dt, fl = oracle_step_sample(shape, inputs, rng)
+                tt, ff, ns = tt + dt, ff + fl, ns + 1
+            cores = blas_threads()
+        cpu = {"value": ff / tt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{ns} samples, each: " + SAMPLE_TEXT.format(
                    proj=" (with its K/V projections of every kept row)" if shape.with_proj else ""),
                "seconds": tt, "cpu": cpu_model()}
@@ -622,6 +815,8 @@ def run_gpu(args, shape):
                           "gflop_per_layer": flops_layer / 1e9,
                           "kernel_ms_per_layer": kern_ms / nl, "kernel_tflops": kern_tflops,
                           "rope_us_per_layer": rope_ms / nl * 1e3},
+            "workloads": workloads,
+            "model_ttft": model_ttft,
             "masked_gate_topk_gather": masked,
             "attention_bwd_s_gain_tau": bwd,
             "gate_topk_gather": {"us": gtg_ms * 1e3, "gbs": byts / (gtg_ms * 1e-3) / 1e9, "bytes": byts,
@@ -658,6 +853,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="override the stacked workload's layer count")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other workloads and the synthetic model's TTFT")
     args = ap.parse_args()
     from learned_token_pruning_09_b300 import synth
     if args.workload not in synth.ALL_SHAPES:

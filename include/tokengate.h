@@ -391,7 +391,10 @@ TG_API tg_status tg_linear_bf16(const void* a, const void* w, const void* residu
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current): make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
+ * capture.  The address is cached per device ordinal and belongs to the
+ * device's primary context (the one the CUDA runtime uses); a caller that
+ * drives the library from another driver context, or resets the device and
+ * starts a new context, must not use this call afterwards in that process.  All calls share the one array and it keeps the last call's
  * contents; nothing in it needs to start at zero, since each call overwrites
  * what it reads.  Calls whose kernels overlap on the GPU (different streams
  * or host threads) race on the array: serialise them.

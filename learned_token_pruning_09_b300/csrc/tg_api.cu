@@ -685,8 +685,9 @@ extern "C" tg_status tg_gated_attention_fwd_noalloc(const void* q, const void* k
                                                    int32_t max_kept, int32_t hq, int32_t hkv,
                                                    int32_t head_dim, void* o, float* lse, void* k_cache,
                                                    cudaStream_t stream) {
-  if (n_kept < 0 || hq < 1 || hkv < 1 || head_dim < 1)
-    return fail(TG_ERR_INVALID_ARG, "n_kept, hq, hkv and head_dim must be positive");
+  // the same shape checks and messages as tg_gated_attention_fwd, before the scratch is sized
+  const tg_status shape_ok = check_attention_shape(batch, n_kept, hq, hkv, head_dim, cu_kept);
+  if (shape_ok != TG_OK) return shape_ok;
   const size_t need = tg_attention_workspace_size(n_kept, hq, hkv, head_dim, k_cache ? 1 : 0);
   if (need > kStaticScratchBytes)
     return fail(TG_ERR_WORKSPACE,

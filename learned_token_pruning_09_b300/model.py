@@ -31,7 +31,14 @@ class SyntheticModel:
         self.hq, self.hkv, self.dh, self.L = c["hq"], c["hkv"], c["head_dim"], c["gate_layer"]
 
         def bf(a):
+            if isinstance(a, torch.Tensor):            # already bf16 on the device
+                return a.to(self.dev).contiguous()
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(self.dev).view(torch.bfloat16)
+
+        def f32(a):
+            if isinstance(a, torch.Tensor):
+                return a.to(device=self.dev, dtype=torch.float32).contiguous()
+            return torch.as_tensor(np.asarray(a, np.float32)).to(self.dev)
 
         self.layers = []
         for lp in params["layers"]:
@@ -40,10 +47,9 @@ class SyntheticModel:
                 "w_q": bf(lp["w_q"]), "w_k": bf(lp["w_k"]), "w_v": bf(lp["w_v"]), "w_o": bf(lp["w_o"]),
                 "w_gate_up": torch.cat([bf(lp["w_gate"]), bf(lp["w_up"])], dim=0).contiguous(),
                 "w_down": bf(lp["w_down"]),
-                "gain": torch.as_tensor(np.asarray(lp["gain"], np.float32)).to(self.dev), "tau": float(lp["tau"])})
+                "gain": f32(lp["gain"]), "tau": float(lp["tau"])})
         g = params["gate"]
-        self.gate = {"w1": bf(g["w1"]), "w2": bf(g["w2"]),
-                     "b1": torch.as_tensor(np.asarray(g["b1"], np.float32)).to(self.dev), "b2": float(g["b2"])}
+        self.gate = {"w1": bf(g["w1"]), "w2": bf(g["w2"]), "b1": f32(g["b1"]), "b2": float(g["b2"])}
         self.final_norm = bf(params["final_norm"])
         self.w_lm = bf(params["w_lm"])
         self.zero_gain = torch.zeros(self.hq, dtype=torch.float32, device=self.dev)
@@ -109,12 +115,35 @@ class SyntheticModel:
         cu_kept_full = torch.as_tensor(np.concatenate([[0], np.cumsum(kept_len)]).astype(np.int32)).to(dev)
         x_last, _, _ = tg.tg_gather_kept(xk, None, cu_kept_full, last, cu_rows, len(seqlens), want=("x",))
         return {"logits": self._logits(x_last), "caches": caches, "cu": cu, "seqlens": seqlens, "cu_kept": cu_kept,
-                "kept_len": kept_len, "s_kept": s_k, "kept": kept}
+                "kept_len": kept_len, "s_kept": s_k, "kept": kept, "pruned": True}
+
+    # ---- the full (unpruned) prefill, the baseline TokenGate is measured against ----
+    def prefill_full(self, x: torch.Tensor, seqlens: Sequence[int]):
+        """Every layer on every row with plain causal attention (no gate, no
+        score bias): the full prefill.  Returns the logits [B, vocab] of each
+        sequence's last row and the full-length caches of every layer."""
+        dev = self.dev
+        seqlens = [int(v) for v in seqlens]
+        cu_h = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+        cu = torch.as_tensor(cu_h).to(dev)
+        pos = torch.as_tensor(np.concatenate([np.arange(n) for n in seqlens]).astype(np.int32)).to(dev)
+        zeros_s = torch.zeros(int(cu_h[-1]), dtype=torch.float32, device=dev)
+        caches: List[tuple] = []
+        for li in range(len(self.layers)):
+            h, cache = self._attn_block(x, li, pos, cu, max(seqlens), zeros_s, self.zero_gain, 1.0)
+            caches.append(cache)
+            x = self._mlp_block(h, li)
+        last = torch.as_tensor((cu_h[1:] - 1).astype(np.int32)).to(dev)
+        cu_rows = torch.as_tensor(np.arange(len(seqlens) + 1, dtype=np.int32)).to(dev)
+        x_last, _, _ = tg.tg_gather_kept(x, None, cu, last, cu_rows, len(seqlens), want=("x",))
+        return {"logits": self._logits(x_last), "caches": caches, "cu": cu, "seqlens": seqlens, "pruned": False}
 
     # ---- the first decode step ----
     def decode(self, x_new: torch.Tensor, state: Dict[str, object]):
         """x_new [B, d] bf16: the input row of each sequence's generated token
-        (at position N_b).  Returns the next logits [B, vocab] (bf16)."""
+        (at position N_b), over the caches of ``prefill`` (kept-only above the
+        gate layer) or ``prefill_full`` (full length everywhere).  Returns the
+        next logits [B, vocab] (bf16)."""
         dev, b = self.dev, x_new.shape[0]
         cu_b = torch.as_tensor(np.arange(b + 1, dtype=np.int32)).to(dev)
         pos_new = torch.as_tensor(np.asarray(state["seqlens"], np.int32)).to(dev)
@@ -126,7 +155,7 @@ class SyntheticModel:
             v = tg.tg_linear_bf16(a, p["w_v"]).view(b, self.hkv, self.dh)
             q_rot, k_rot = tg.tg_rope_qk(q, k, pos_new, self.theta, cu_b)
             k_c, v_c = state["caches"][li]
-            if li > self.L:
+            if state["pruned"] and li > self.L:
                 o = tg.tg_decode_attention(q_rot, k_rot, v, k_c, v_c, state["cu_kept"], max(state["kept_len"]),
                                            s_cache=state["s_kept"], gain=p["gain"], tau=p["tau"])
             else:

@@ -33,9 +33,11 @@ BASE_SEED = 20261202
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round float32 values to bfloat16 (round-to-nearest-even); return bits."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    rounding = np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))
-    return ((u + rounding) >> np.uint64(16)).astype(np.uint16)
+    u = a.view(np.uint32)
+    # the sum wraps only for NaN patterns; the low 16 bits of the shifted sum
+    # are the same as those of the unwrapped sum
+    rounding = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + rounding) >> np.uint32(16)).astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -353,7 +355,16 @@ MODEL_CONFIGS = {
     # small enough for the float64 oracle; the layout of the full model
     "model-tiny": {"n_layers": 4, "gate_layer": 1, "d": 128, "ffn": 256, "hq": 4, "hkv": 2, "head_dim": 64,
                    "vocab": 512, "gate_h": 32},
+    # Qwen3-1.7B's layout (28 layers, hidden 2048, MLP 6144, 16/8 heads of 128,
+    # vocabulary 151,936); TokenGate prunes it at layer 1 counted from one,
+    # i.e. index 0 here, so 27 layers run on the kept tokens only
+    "qwen3-1.7b": {"n_layers": 28, "gate_layer": 0, "d": 2048, "ffn": 6144, "hq": 16, "hkv": 8, "head_dim": 128,
+                   "vocab": 151936, "gate_h": 256},
 }
+
+# context lengths of the synthetic time-to-first-token measurement: document
+# rows, question rows and the document budget K (the 16k and 128k workloads)
+MODEL_CONTEXTS = {"16k": (16320, 64, 2048), "128k": (131008, 64, 8192)}
 
 
 def model_params(name: str) -> Dict[str, object]:
@@ -385,3 +396,38 @@ def model_params(name: str) -> Dict[str, object]:
             "b1": np.zeros(c["gate_h"], np.float32), "b2": 0.0}
     return {"config": c, "layers": layers, "gate": gate, "final_norm": norm(d),
             "w_lm": _normal_bf16(r, (c["vocab"], d), 1.0 / np.sqrt(d))}
+
+
+def model_params_device(name: str, device, seed: int = BASE_SEED + 50) -> Dict[str, object]:
+    """The same layout and distributions as ``model_params``, drawn on the
+    device by torch's seeded generator (the full-size model has 1.4 billion
+    weights, too many to draw on the host in a benchmark).  bf16 tensors and
+    float32 gains; for timing and memory only, never compared bit for bit."""
+    import torch
+    c = MODEL_CONFIGS[name]
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    d, f, hq, hkv, dh = c["d"], c["ffn"], c["hq"], c["hkv"], c["head_dim"]
+
+    def normal(shape, std):
+        return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
+
+    def norm(n):
+        return (1.0 + 0.1 * torch.randn(n, generator=g, device=device, dtype=torch.float32)).to(torch.bfloat16)
+
+    def uniform(n, lo, hi):
+        return lo + (hi - lo) * torch.rand(n, generator=g, device=device, dtype=torch.float32)
+
+    layers = []
+    for _ in range(c["n_layers"]):
+        layers.append({
+            "ln1": norm(d), "ln2": norm(d), "q_norm": norm(dh), "k_norm": norm(dh),
+            "w_q": normal((hq * dh, d), d ** -0.5), "w_k": normal((hkv * dh, d), d ** -0.5),
+            "w_v": normal((hkv * dh, d), d ** -0.5), "w_o": normal((d, hq * dh), (hq * dh) ** -0.5),
+            "w_gate": normal((f, d), d ** -0.5), "w_up": normal((f, d), d ** -0.5),
+            "w_down": normal((d, f), f ** -0.5),
+            "gain": uniform(hq, 0.5, 2.0), "tau": float(uniform(1, 0.9, 1.3).item())})
+    gate = {"w1": normal((c["gate_h"], d), d ** -0.5), "w2": normal((c["gate_h"],), c["gate_h"] ** -0.5),
+            "b1": torch.zeros(c["gate_h"], device=device), "b2": 0.0}
+    return {"config": c, "layers": layers, "gate": gate, "final_norm": norm(d),
+            "w_lm": normal((c["vocab"], d), d ** -0.5)}

@@ -139,7 +139,7 @@ def test_attention_full(tg, name):
     check_attention(o, lse, ref_o, ref_lse, rows, name)
 
 
-@pytest.mark.parametrize("name", ["budget-32k-k8192", "ragged-8"])
+@pytest.mark.parametrize("name", ["budget-32k-k1024", "budget-32k-k4096", "budget-32k-k8192", "ragged-8"])
 def test_attention_sampled_full_size(tg, name):
     shape = synth.ALL_SHAPES[name]()
     ai, pos, s_kept, cu_kept = attention_case(shape)

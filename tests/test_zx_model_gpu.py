@@ -107,3 +107,34 @@ def test_runner_prefill_and_decode(tg):
     ref_nxt, _ = oracle.model.decode_step(dec(x_new), ref, layers, c["gate_layer"], cu, dec(m["final_norm"]),
                                           dec(m["w_lm"]), c["hq"], c["hkv"], c["head_dim"])
     assert np.abs(nxt - ref_nxt).max() <= 0.03 * np.abs(ref_nxt).max()
+
+
+def test_runner_full_prefill_and_decode(tg):
+    """The full prefill (every layer on every row, no gate) and its decode
+    step over full-length caches.  The oracle's pruned prefill with the gate
+    at the last layer and the whole document kept is that dense stack: every
+    layer runs on every row, none with a score bias."""
+    from learned_token_pruning_09_b300.model import SyntheticModel
+    m = synth.model_params("model-tiny")
+    c = m["config"]
+    dec = oracle.bf16_decode
+    layers = [{k: (dec(v) if isinstance(v, np.ndarray) and v.dtype == np.uint16 else v) for k, v in lp.items()}
+              for lp in m["layers"]]
+    gate = {"w1": dec(m["gate"]["w1"]), "w2": dec(m["gate"]["w2"]), "b1": np.zeros(c["gate_h"]), "b2": 0.0}
+    rng = np.random.default_rng(1)
+    lens = [70, 33, 1]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    x = bf(rng.standard_normal((int(cu[-1]), c["d"])))
+    x_new = bf(rng.standard_normal((len(lens), c["d"])))
+    model = SyntheticModel(m)
+    st = model.prefill_full(dev_bf16(x), lens)
+    logits = host_f64(st["logits"])
+    nxt = host_f64(model.decode(dev_bf16(x_new), st))
+    assert tg.tg_check_device_status() == tg.TG_OK
+    last = c["n_layers"] - 1
+    ref = oracle.model.pruned_prefill(dec(x), layers, gate, last, cu, lens, lens, dec(m["final_norm"]),
+                                      dec(m["w_lm"]), c["hq"], c["hkv"], c["head_dim"])
+    assert np.abs(logits - ref["logits"]).max() <= 0.03 * np.abs(ref["logits"]).max()
+    ref_nxt, _ = oracle.model.decode_step(dec(x_new), ref, layers, last, cu, dec(m["final_norm"]), dec(m["w_lm"]),
+                                          c["hq"], c["hkv"], c["head_dim"])
+    assert np.abs(nxt - ref_nxt).max() <= 0.03 * np.abs(ref_nxt).max()
