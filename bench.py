@@ -14,13 +14,15 @@ q/k/v.
 
 Prints ONE JSON line (rank 0).  ``value`` is gated-attention TFLOP/s:
 causal-triangle flops 2*hq*D*T(T+1) per layer over the measured attention
-time (RoPE prologue + attention kernel), summed over ranks.
-``gate_topk_gather`` gives the GB/s of the first three steps on algorithmic
-bytes.  Every call is captured once in a CUDA graph and replayed, so the
-device time excludes host launch cost; ``e2e`` instead runs the public
-Python API with host buffers (copies in the timed region).  L2 is flushed
-(256 MB written) before every timed step.  N > 1 runs independent replicas:
-the workload is one sequence and the path has no exchange step.
+time, summed over ranks.  In the long-context stack RoPE is fused into the
+Q/K/V projection, so that time is the attention kernel's; single-layer
+workloads add their RoPE call.  ``gate_topk_gather`` gives the GB/s of the
+first three steps on algorithmic bytes.  Every call is captured once in a
+CUDA graph and replayed, so the device time excludes host launch cost;
+``e2e`` instead runs the public Python API with host buffers (copies in the
+timed region).  L2 is flushed before every timed step (256 MB written, then
+256 MB read).  N > 1 runs independent replicas: the workload is one
+sequence and the path has no exchange step.
 """
 from __future__ import annotations
 
@@ -95,6 +97,12 @@ def measure_masked(P, shape, flush, steps):
     s = torch.empty(shape.n_rows, dtype=torch.float32, device=P.dev)
     ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
 
+    def calls_plain(n_kept):
+        tg.tg_gate_score_masked(P.X, mask, P.W1, None, P.W2, P.b2, s_out=s)
+        tg.tg_topk_select_masked(s, P.cu, mask, P.kk, max_len, kept_idx=kept, cu_kept=cu_kept, n_prunable=n_prun)
+        tg.tg_gather_kept(P.X, s, P.cu, kept[:n_kept], cu_kept, n_kept, x_kept=P.xk_masked[:n_kept],
+                          pos_kept=P.pos_masked[:n_kept], s_kept=P.s_masked[:n_kept])
+
     def calls(n_kept):
         ev[0].record()
         tg.tg_gate_score_masked(P.X, mask, P.W1, None, P.W2, P.b2, s_out=s)
@@ -117,7 +125,7 @@ def measure_masked(P, shape, flush, steps):
         calls(n_kept)
     per = []
     for i in range(3 + steps):
-        flush.zero_()
+        flush()
         g.replay()
         torch.cuda.synchronize()
         if i >= 3:
@@ -125,7 +133,7 @@ def measure_masked(P, shape, flush, steps):
     if tg.tg_check_device_status() != tg.TG_OK:
         raise RuntimeError("device status after the masked path: " + tg.lib.tg_last_error_string().decode())
     per = np.array(per).mean(axis=0)
-    us = float(per.sum()) * 1e3
+    us = time_calls([lambda: calls_plain(n_kept)], flush, steps)
     byts = masked_path_bytes(shape, n_kept)
     return {"us": us, "gbs": byts / (us * 1e-6) / 1e9, "bytes": byts, "n_kept": n_kept,
             "spans_per_seq": 4, "prunable_rows": int(mask_h.sum()),
@@ -168,7 +176,7 @@ def measure_attn_bwd(P, shape, flush, steps):
         ev[1].record()
     per = []
     for i in range(3 + steps):
-        flush.zero_()
+        flush()
         g.replay()
         torch.cuda.synchronize()
         if i >= 3:
@@ -179,6 +187,44 @@ def measure_attn_bwd(P, shape, flush, steps):
     fl = attention_flops(shape.kept_lens, hq, D)
     return {"ms_per_layer": ms, "tflops": fl / (ms * 1e-3) / 1e12, "gflop_per_layer": fl / 1e9,
             "launches_per_call": 4}
+
+
+def deltanet_bytes(t, hk, hv, dk, dv):
+    """Algorithmic HBM bytes of one gated-delta scan: q and k read (bf16),
+    v read and o written (bf16), g and beta read (fp32)."""
+    return float(t * (2 * hk * dk * 2 + 2 * hv * dv * 2 + 2 * hv * 4))
+
+
+def measure_deltanet(dev, flush, steps, peaks, name="deltanet-32k-k4096"):
+    """The pruned Gated DeltaNet scan over the kept tokens of a 32k NIAH-like
+    context cut to K = 4096 (plus 64 question tokens), one CUDA graph around
+    the call, L2 flushed before each replay."""
+    import torch
+    from learned_token_pruning_09_b300 import synth
+    from learned_token_pruning_09_b300 import tokengate as tg
+    inp = synth.deltanet_inputs(name)
+    cfg = synth.DELTA_SHAPES[name]
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = bf(inp["q"]), bf(inp["k"]), bf(inp["v"])
+    g = torch.as_tensor(inp["g"]).to(dev)
+    beta = torch.as_tensor(inp["beta"]).to(dev)
+    cu = torch.as_tensor(inp["cu_kept"]).to(dev)
+    o = torch.empty_like(v)
+    tg.tg_gated_delta_scan(q, k, v, g, beta, cu, o=o)
+    torch.cuda.synchronize()
+    graph, evs = capture_step([("scan", lambda: tg.tg_gated_delta_scan(q, k, v, g, beta, cu, o=o))])
+    replay_timed(graph, evs, flush, 3)
+    us = float(replay_timed(graph, evs, flush, steps).mean()) * 1e3
+    if tg.tg_check_device_status() != tg.TG_OK:
+        raise RuntimeError("device status after the scan: " + tg.lib.tg_last_error_string().decode())
+    t = int(inp["cu_kept"][-1])
+    byts = deltanet_bytes(t, cfg["hk"], cfg["hv"], cfg["dk"], cfg["dv"])
+    return {"workload": name, "tokens": t, "hk": cfg["hk"], "hv": cfg["hv"], "dk": cfg["dk"], "dv": cfg["dv"],
+            "us": us, "gbs": byts / (us * 1e-6) / 1e9, "bytes": byts,
+            "frac_of_measured_hbm": byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
 
 
 def max_over_ranks(values, device):
@@ -288,7 +334,8 @@ def workload_config(shape):
             "k": shape.k, "kept_tokens": shape.n_kept, "d": shape.d, "gate_h": shape.h, "hq": shape.hq,
             "hkv": shape.hkv, "head_dim": shape.head_dim, "layers_above_gate": shape.n_layers,
             "projections": shape.with_proj, "rope_theta": 1e6,
-            "l2": "flushed (256 MB write) before every timed step", "parallelism": "replicas"}
+            "rope": "fused into the Q/K/V projection" if shape.with_proj else "tg_rope_qk before the attention",
+            "l2": "flushed before every timed step: 256 MB written, then 256 MB read (no dirty line left)", "parallelism": "replicas"}
 
 
 # ---------------------------------------------------------------------------
@@ -458,13 +505,9 @@ class Path:
         self.layers = []
         if shape.with_proj:
             for lp in inputs["layers"]:
-                w = bf(lp["w_qkv"])
-                nq, nk = hq * D, hkv * D
                 self.layers.append({
-                    "wq": w[:nq].contiguous(), "wk": w[nq:nq + nk].contiguous(), "wv": w[nq + nk:].contiguous(),
-                    "wo": bf(lp["w_o"]), "gain": torch.as_tensor(lp["gain"]).to(dev), "tau": lp["tau"],
-                    "k_cache": e(T, hkv, D), "v": e(T, hkv, D)})
-            self.q, self.k = e(T, hq, D), e(T, hkv, D)
+                    "w_qkv": bf(lp["w_qkv"]), "wo": bf(lp["w_o"]), "gain": torch.as_tensor(lp["gain"]).to(dev),
+                    "tau": lp["tau"], "k_cache": e(T, hkv, D), "v": e(T, hkv, D)})
             self.o = e(T, hq, D)
         else:
             ai = inputs["ai"]
@@ -486,10 +529,11 @@ class Path:
                                pos_kept=self.pos, s_kept=self.sk)
 
     def proj_qkv(self, i):
-        L, tg, T = self.layers[i], self.tg, self.T
-        tg.tg_linear_bf16(self.xk, L["wq"], out=self.q.view(T, -1))
-        tg.tg_linear_bf16(self.xk, L["wk"], out=self.k.view(T, -1))
-        tg.tg_linear_bf16(self.xk, L["wv"], out=L["v"].view(T, -1))
+        # one GEMM for q, k and v with RoPE in its epilogue: q' into its own
+        # buffer, k' into the layer's kept-only K cache
+        L, sh = self.layers[i], self.shape
+        self.tg.tg_qkv_rope_bf16(self.xk, L["w_qkv"], self.pos, sh.hq, sh.hkv, sh.head_dim, 1e6, q_out=self.q_rot,
+                                 k_out=L["k_cache"], v_out=L["v"])
 
     def rope(self, i):
         # q' into a buffer of its own, k' into the layer's kept-only K cache
@@ -511,7 +555,8 @@ class Path:
         for i in range(len(self.layers)):
             if self.shape.with_proj:
                 segs.append((f"proj_qkv{i}", lambda i=i: self.proj_qkv(i)))
-            segs.append((f"rope{i}", lambda i=i: self.rope(i)))
+            else:
+                segs.append((f"rope{i}", lambda i=i: self.rope(i)))
             segs.append((f"attn{i}", lambda i=i: self.attn(i)))
             if self.shape.with_proj:
                 segs.append((f"proj_o{i}", lambda i=i: self.proj_o(i)))
@@ -520,8 +565,26 @@ class Path:
     def launches_per_step(self):
         n = 3
         for _ in self.layers:
-            n += 2 + (4 if self.shape.with_proj else 0)
+            n += 3 if self.shape.with_proj else 2     # qkv (with RoPE), attention, output / RoPE, attention
         return n
+
+
+class L2Flush:
+    """Before every timed step: 256 MB written, then another 256 MB read.
+    L2 (126 MB) is then left holding clean lines of a buffer that the timed
+    kernels never touch, so they neither hit their own data in L2 nor pay for
+    writing back dirty lines of the flush itself."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(64 * 1024 * 1024, dtype=torch.int32, device=dev)
+        self.out = torch.empty((), dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.amax(self.r, dim=0, out=self.out)
 
 
 def capture_step(segs):
@@ -546,11 +609,22 @@ def replay_timed(graph, evs, flush, steps):
     import torch
     per = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         graph.replay()
         torch.cuda.synchronize()     # the events are re-recorded by the next replay
         per.append([evs[k].elapsed_time(evs[k + 1]) for k in range(len(evs) - 1)])
     return np.array(per)
+
+
+def time_calls(calls, flush, steps):
+    """Device time (us) of a sequence of calls captured as one CUDA graph with
+    events only around the whole sequence, so that consecutive kernels keep
+    their programmatic launch edges (a kernel launched early behind its
+    predecessor and waiting for it on the device); L2 flushed before each
+    replay."""
+    graph, evs = capture_step([("calls", lambda: [f() for f in calls])])
+    replay_timed(graph, evs, flush, 3)
+    return float(replay_timed(graph, evs, flush, steps).mean()) * 1e3
 
 
 # the other workloads of the metric, each measured as one single-layer step
@@ -578,7 +652,7 @@ def measure_workload(name, dev, flush, steps, peaks):
         raise RuntimeError(f"device status ({name}): " + tg.lib.tg_last_error_string().decode())
     fl = attention_flops(shape.kept_lens, shape.hq, shape.head_dim)
     attn_ms = seg["rope0"] + seg["attn0"]
-    gtg_ms = seg["gate"] + seg["topk"] + seg["gather"]
+    gtg_ms = time_calls([P.gate, P.topk, P.gather], flush, steps) * 1e-3
     byts = path_bytes(shape)
     out = {"batch": shape.batch, "n_rows": shape.n_rows, "kept_tokens": shape.n_kept,
            "attention": {"ms_per_layer": attn_ms, "tflops": fl / (attn_ms * 1e-3) / 1e12,
@@ -588,7 +662,9 @@ def measure_workload(name, dev, flush, steps, peaks):
            "gate_topk_gather": {"us": gtg_ms * 1e3, "gbs": byts / (gtg_ms * 1e-3) / 1e9, "bytes": byts,
                                 "frac_of_measured_hbm": byts / (gtg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                 "gate_us": seg["gate"] * 1e3, "topk_us": seg["topk"] * 1e3,
-                                "gather_us": seg["gather"] * 1e3}}
+                                "gather_us": seg["gather"] * 1e3,
+                                "split": "us: the three calls in one graph; gate/topk/gather_us: each "
+                                         "between events (no early launch)"}}
     del P, graph
     torch.cuda.empty_cache()
     return out
@@ -601,14 +677,20 @@ def measure_model_ttft(dev, flush, steps):
     (every layer on every token), each followed by the first decode step.
     Everything runs eagerly through the public Python API, as a user calls
     it: TTFT is the device time from the first call of the prefill to the
-    logits of the first token (host launch gaps included)."""
+    logits of the first token (host launch gaps included).  Peak prefill
+    memory is the most device memory the prefill allocated on top of what
+    was allocated before it (the model's weights and inputs, and this
+    benchmark's other buffers); ``..._with_weights`` adds the model's own
+    weight bytes, the figure a single-model process would see."""
     import torch
     from learned_token_pruning_09_b300 import synth
     from learned_token_pruning_09_b300.model import SyntheticModel
     model = SyntheticModel(synth.model_params_device("qwen3-1.7b", dev), device=dev)
     c = model.cfg
     torch.cuda.synchronize()
-    weights = torch.cuda.memory_allocated()
+    tensors = [t for lp in model.layers for t in lp.values() if isinstance(t, torch.Tensor)]
+    tensors += list(model.gate.values()) + [model.final_norm, model.w_lm]
+    weights = float(sum(t.numel() * t.element_size() for t in tensors if isinstance(t, torch.Tensor)))
     out = {"model": "Qwen3-1.7B layout, random weights", "layers": c["n_layers"], "gate_layer": c["gate_layer"] + 1,
            "weights_gb": weights / 1e9, "contexts": {}}
     gen = torch.Generator(device=dev)
@@ -627,7 +709,7 @@ def measure_model_ttft(dev, flush, steps):
             torch.cuda.synchronize()
             ttft, dec, peak = [], [], []
             for _ in range(steps):
-                flush.zero_()
+                flush()
                 torch.cuda.synchronize()
                 base = torch.cuda.memory_allocated()
                 torch.cuda.reset_peak_memory_stats()
@@ -686,7 +768,7 @@ def run_gpu(args, shape):
     P = Path(shape, inputs, dev)
     tg = P.tg
     segs = P.segments()
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     # eager warm-up (initialises the library on this device), then capture
     for _ in range(2):
@@ -722,7 +804,7 @@ def run_gpu(args, shape):
     rope_ms = float(sum(v for n, v in seg_ms.items() if n.startswith("rope")))
     attn_ms = kern_ms + rope_ms
     proj_ms = float(sum(v for n, v in seg_ms.items() if n.startswith("proj")))
-    gtg_ms = seg_ms["gate"] + seg_ms["topk"] + seg_ms["gather"]
+    gtg_ms = time_calls([P.gate, P.topk, P.gather], flush, args.steps) * 1e-3
     nl = len(P.layers)
     step_ms, attn_ms, kern_ms, rope_ms = max_over_ranks([step_ms, attn_ms, kern_ms, rope_ms], dev)
     flops_layer = attention_flops(shape.kept_lens, shape.hq, shape.head_dim)
@@ -740,12 +822,13 @@ def run_gpu(args, shape):
     bwd["frac_of_burst"] = bwd["tflops"] / peaks["bf16_tflops"]
 
     # ---- the metric's other workloads, and the synthetic model's TTFT ----
-    workloads, model_ttft = None, None
+    workloads, model_ttft, deltanet = None, None, None
     if not args.headline_only:
         del graph
         torch.cuda.empty_cache()
         workloads = {n: measure_workload(n, dev, flush, args.steps, peaks) for n in SIDE_WORKLOADS}
         model_ttft = measure_model_ttft(dev, flush, 2)
+    deltanet = measure_deltanet(dev, flush, args.steps, peaks)
 
     # ---- end to end through the public API, host buffers ----
     import torch as _t
@@ -817,12 +900,15 @@ def run_gpu(args, shape):
                           "rope_us_per_layer": rope_ms / nl * 1e3},
             "workloads": workloads,
             "model_ttft": model_ttft,
+            "gated_deltanet_scan": deltanet,
             "masked_gate_topk_gather": masked,
             "attention_bwd_s_gain_tau": bwd,
             "gate_topk_gather": {"us": gtg_ms * 1e3, "gbs": byts / (gtg_ms * 1e-3) / 1e9, "bytes": byts,
                                  "frac_of_measured_hbm": byts / (gtg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                  "gate_us": seg_ms["gate"] * 1e3, "topk_us": seg_ms["topk"] * 1e3,
-                                 "gather_us": seg_ms["gather"] * 1e3},
+                                 "gather_us": seg_ms["gather"] * 1e3,
+                                 "split": "us: the three calls in one graph; gate/topk/gather_us: each "
+                                          "between events (no early launch)"},
             "projections": ({"ms_per_step": proj_ms, "tflops": proj_flops(shape) * nl / (proj_ms * 1e-3) / 1e12}
                             if shape.with_proj else None),
             "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": peaks["bf16_tflops"],

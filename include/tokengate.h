@@ -15,9 +15,11 @@
  *
  * The calls below are the steps of that path, in order:
  *   tg_gate_score -> tg_topk_select -> tg_gather_kept -> (per layer)
- *   [tg_linear_bf16 for Q/K/V] -> tg_gated_attention_fwd (= tg_rope_qk ->
- *   tg_gated_attention_rotated) -> [tg_linear_bf16 for the output projection
+ *   tg_qkv_rope_bf16 (the Q/K/V projection with RoPE fused into it) ->
+ *   tg_gated_attention_rotated -> [tg_linear_bf16 for the output projection
  *   with the residual add].
+ * When q, k and v come from elsewhere, tg_gated_attention_fwd (=
+ * tg_rope_qk -> tg_gated_attention_rotated) rotates them itself.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -156,11 +158,14 @@ TG_API tg_status tg_topk_select_masked(const float* s, int64_t n_rows, const int
  *     s_kept[i] = s[kept_idx[i]]
  *
  *   x_bf16 [n_rows, d] bf16; s [n_rows] fp32; cu_seqlens [batch+1];
+ *   n_rows  rows of x and s (kept ids at or beyond it are flagged, not read)
  *   kept_idx [n_kept], cu_kept [batch+1] as written by tg_topk_select
  *   n_kept  host-side total kept rows (= cu_kept[batch])
  *   x_kept_bf16 [n_kept, d] bf16, pos_kept [n_kept] int32, s_kept [n_kept]
  *   fp32 outputs; any of the three may be NULL to skip it.
  * A kept index outside its sequence -> TG_ERR_DEVICE_INDEX, row skipped.
+ * The kernel is launched early behind the previous kernel in the stream
+ * (programmatic dependent launch) and waits for it before reading anything.
  */
 TG_API tg_status tg_gather_kept(const void* x_bf16, int64_t n_rows, int32_t d, const float* s,
                          const int32_t* cu_seqlens, const int32_t* kept_idx,
@@ -300,8 +305,9 @@ TG_API size_t tg_attention_bwd_workspace_size(int64_t n_kept, int32_t hq);
  *     S  = exp(g) (S - beta (S k^) k^T) + beta v k^T,    o = S q^
  * with S of shape [dv, dk]; value head h reads q/k head h / (hv / hk).
  *
- *   q, k   [n_kept, hk, dk] bf16 (16-byte aligned), dk in {64, 128}
- *   v      [n_kept, hv, dv] bf16, hv a multiple of hk, 1 <= dv <= 1024
+ *   q, k   [n_kept, hk, dk] bf16, dk in {64, 128}
+ *   v      [n_kept, hv, dv] bf16, hv a multiple of hk, dv a multiple of 16
+ *          in [16, 1024]
  *   g      [n_kept, hv] fp32 log-decays (exp(g) in (0, 1] for g <= 0)
  *   beta   [n_kept, hv] fp32 write strengths
  *   cu_kept [batch+1] int32 (device), sequences of kept tokens
@@ -309,7 +315,8 @@ TG_API size_t tg_attention_bwd_workspace_size(int64_t n_kept, int32_t hq);
  *   initial_state [batch, hv, dv, dk] fp32 or NULL
  *   o      [n_kept, hv, dv] bf16 output
  *   final_state   [batch, hv, dv, dk] fp32 output, or NULL
- * fp32 state and arithmetic; o rounded once to bf16.  No workspace.
+ * Every pointer 16-byte aligned.  fp32 state and arithmetic; o rounded once
+ * to bf16.  No workspace.
  * Device-side errors: cu_kept out of range -> TG_ERR_DEVICE_INDEX.
  */
 TG_API tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v,
@@ -370,6 +377,33 @@ TG_API tg_status tg_decode_attention(const void* q_rot, const void* k_new_rot, c
  */
 TG_API tg_status tg_linear_bf16(const void* a, const void* w, const void* residual, void* out,
                          int64_t m, int32_t n, int32_t kdim, cudaStream_t stream);
+
+/*
+ * The Q/K/V projection of a layer above the gate with RoPE fused into it
+ * (the same long-context stack; MarkTechPost article, "What is token-gated
+ * attention?": the kept tokens keep their original positions, and the
+ * rotated keys are the kept-only KV cache, "How does TokenGate's learned
+ * token pruning work?").  One GEMM against the stacked weight
+ *   w_qkv [(hq + 2 hkv) * head_dim, kdim] (rows: W_q, then W_k, then W_v),
+ * whose fp32 result is split into heads of head_dim columns:
+ *   q_out[m, hq, D]  = RoPE(x W_q^T)  at pos[m]    (the queries q')
+ *   k_out[m, hkv, D] = RoPE(x W_k^T)  at pos[m]    (the K cache k')
+ *   v_out[m, hkv, D] = x W_v^T
+ * RoPE as tg_rope_qk (rotate-half, rate rope_theta^(-2i/D) per position),
+ * applied to the fp32 accumulators and rounded once to bf16, so q' and k'
+ * are within one bf16 rounding of the exact rotation of the exact product.
+ * tg_gated_attention_rotated then takes q_out, k_out and v_out directly.
+ *   x [m, kdim] bf16 (kdim a multiple of 64), pos [m] int32 (the rows'
+ *   original positions, not checked here: the attention kernel checks them),
+ *   head_dim 64 or 128; all buffers device memory, 16-byte aligned, owned by
+ *   the caller; outputs must not overlap x or w_qkv.
+ * Errors: invalid sizes or pointers return TG_ERR_INVALID_ARG /
+ * TG_ERR_UNSUPPORTED before any launch.
+ */
+TG_API tg_status tg_qkv_rope_bf16(const void* x, const void* w_qkv, int64_t m, int32_t kdim,
+                           int32_t hq, int32_t hkv, int32_t head_dim, const int32_t* pos,
+                           float rope_theta, void* q_out, void* k_out, void* v_out,
+                           cudaStream_t stream);
 
 /*
  * Token-gated attention with no workspace argument.  The TokenGate articles

@@ -289,6 +289,7 @@ tg_status tg_gather_kept(const void* x_bf16, int64_t n_rows, int32_t d, const fl
   if (st != TG_OK) return st;
   GatherArgs a{};
   a.x = x_bf16;
+  a.n_rows = n_rows;
   a.d = d;
   a.s = s;
   a.cu_seqlens = cu_seqlens;
@@ -316,6 +317,16 @@ size_t tg_attention_workspace_size(int64_t n_kept, int32_t hq, int32_t hkv, int3
 }
 
 // shared argument checks of the attention calls
+// RoPE rates theta^(-2i/D) / (2 pi) in turns per position, i < D/2, each as
+// an fp32 pair hi + lo (formed in fp64).
+static void rope_turns(float rope_theta, int32_t head_dim, RopeFreqs* f) {
+  for (int i = 0; i < head_dim / 2; ++i) {
+    const double t = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim) / (2.0 * 3.141592653589793);
+    f->turns_hi[i] = static_cast<float>(t);
+    f->turns_lo[i] = static_cast<float>(t - static_cast<double>(f->turns_hi[i]));
+  }
+}
+
 static tg_status check_attention_shape(int32_t batch, int64_t n_kept, int32_t hq, int32_t hkv, int32_t head_dim,
                                        const int32_t* cu_kept) {
   if (batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
@@ -341,11 +352,7 @@ tg_status tg_rope_qk(const void* q, const void* k, const int32_t* pos_kept, floa
   st = device_info(&di);
   if (st != TG_OK) return st;
   RopeFreqs f{};
-  for (int i = 0; i < head_dim / 2; ++i) {
-    const double t = std::pow(static_cast<double>(rope_theta), -2.0 * i / head_dim) / (2.0 * 3.141592653589793);
-    f.turns_hi[i] = static_cast<float>(t);
-    f.turns_lo[i] = static_cast<float>(t - static_cast<double>(f.turns_hi[i]));
-  }
+  rope_turns(rope_theta, head_dim, &f);
   RopeArgs ra{};
   ra.q = q; ra.k = k; ra.pos = pos_kept; ra.cu_kept = cu_kept; ra.batch = batch; ra.n_kept = n_kept;
   ra.hq = hq; ra.hkv = hkv; ra.head_dim = head_dim; ra.q_out = q_out; ra.k_out = k_out;
@@ -507,12 +514,14 @@ tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v, const
   if (n_kept < 0 || n_kept > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_kept out of range");
   if (hk < 1 || hv < 1 || hv % hk != 0) return fail(TG_ERR_INVALID_ARG, "hv must be a positive multiple of hk");
   if (dk != 64 && dk != 128) return fail(TG_ERR_UNSUPPORTED, "dk must be 64 or 128");
-  if (dv < 1 || dv > 1024) return fail(TG_ERR_INVALID_ARG, "dv must be in [1, 1024]");
+  if (dv < 16 || dv > 1024 || dv % 16 != 0) return fail(TG_ERR_INVALID_ARG, "dv must be a multiple of 16 in [16, 1024]");
   if (!(scale > 0.0f) || !std::isfinite(scale)) return fail(TG_ERR_INVALID_ARG, "scale must be positive and finite");
   if (!cu_kept) return fail(TG_ERR_INVALID_ARG, "null cu_kept");
   if (n_kept > 0 && (!q || !k || !v || !g || !beta || !o)) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
-  if (n_kept > 0 && (!aligned16(q) || !aligned16(k)))
-    return fail(TG_ERR_INVALID_ARG, "q and k must be 16-byte aligned");
+  if (n_kept > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)))
+    return fail(TG_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
+    return fail(TG_ERR_INVALID_ARG, "initial_state and final_state must be 16-byte aligned");
   DeviceInfo* di = nullptr;
   tg_status st = device_info(&di);
   if (st != TG_OK) return st;
@@ -596,6 +605,27 @@ tg_status tg_decode_attention(const void* q_rot, const void* k_new_rot, const vo
   return ok();
 }
 
+// TMA maps of a linear call: A [m, kdim] in 128-row boxes, W [n, kdim] in
+// boxes of half a tile's rows (each CTA of a pair stages one half).
+static tg_status linear_maps(const void* a_ptr, const void* w, int64_t m, int32_t n, int32_t kdim, CUtensorMap* ma,
+                             CUtensorMap* mw) {
+  tg_status st;
+  const int bn = linear_tile_n(n);
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(kdim), static_cast<uint64_t>(m)};
+    const uint64_t str[1] = {static_cast<uint64_t>(kdim) * 2};
+    const uint32_t box[2] = {64, 128};
+    if ((st = make_map(ma, a_ptr, 2, dims, str, box, "a")) != TG_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(kdim), static_cast<uint64_t>(n)};
+    const uint64_t str[1] = {static_cast<uint64_t>(kdim) * 2};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(bn / 2)};
+    if ((st = make_map(mw, w, 2, dims, str, box, "w")) != TG_OK) return st;
+  }
+  return TG_OK;
+}
+
 tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual, void* out, int64_t m, int32_t n,
                          int32_t kdim, cudaStream_t stream) {
   if (m < 0 || m > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "m out of range");
@@ -608,26 +638,43 @@ tg_status tg_linear_bf16(const void* a_ptr, const void* w, const void* residual,
   DeviceInfo* di = nullptr;
   tg_status st = device_info(&di);
   if (st != TG_OK) return st;
-  const int bn = linear_tile_n(n);
   CUtensorMap ma, mw;
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(kdim), static_cast<uint64_t>(m)};
-    const uint64_t str[1] = {static_cast<uint64_t>(kdim) * 2};
-    const uint32_t box[2] = {64, 128};
-    if ((st = make_map(&ma, a_ptr, 2, dims, str, box, "a")) != TG_OK) return st;
-  }
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(kdim), static_cast<uint64_t>(n)};
-    const uint64_t str[1] = {static_cast<uint64_t>(kdim) * 2};
-    // each CTA of a pair stages one half of a tile's W rows
-    const uint32_t box[2] = {64, static_cast<uint32_t>(bn / 2)};
-    if ((st = make_map(&mw, w, 2, dims, str, box, "w")) != TG_OK) return st;
-  }
+  if ((st = linear_maps(a_ptr, w, m, n, kdim, &ma, &mw)) != TG_OK) return st;
   LinearArgs la{};
   la.residual = residual; la.out = out; la.m = m; la.n = n; la.kdim = kdim;
   la.status = di->status; la.watchdog = g_watchdog_cycles; la.num_sms = di->num_sms;
   cudaError_t e = launch_linear(ma, mw, la, stream);
   if (e != cudaSuccess) return cuda_fail(e, "linear kernel launch");
+  return ok();
+}
+
+tg_status tg_qkv_rope_bf16(const void* x, const void* w_qkv, int64_t m, int32_t kdim, int32_t hq, int32_t hkv,
+                           int32_t head_dim, const int32_t* pos, float rope_theta, void* q_out, void* k_out,
+                           void* v_out, cudaStream_t stream) {
+  if (m < 0 || m > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "m out of range");
+  if (kdim < 64 || kdim % 64 != 0) return fail(TG_ERR_INVALID_ARG, "kdim must be a positive multiple of 64");
+  if (hq < 1 || hkv < 1) return fail(TG_ERR_INVALID_ARG, "hq and hkv must be >= 1");
+  if (head_dim != 64 && head_dim != 128) return fail(TG_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  const int64_t n = static_cast<int64_t>(hq + 2 * hkv) * head_dim;
+  if (n > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "too many heads");
+  if (!(rope_theta > 0.0f) || !std::isfinite(rope_theta)) return fail(TG_ERR_INVALID_ARG, "rope_theta must be positive");
+  if (m == 0) return ok();
+  if (!x || !w_qkv || !pos || !q_out || !k_out || !v_out) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(v_out))
+    return fail(TG_ERR_INVALID_ARG, "x, w_qkv, q_out, k_out and v_out must be 16-byte aligned");
+  DeviceInfo* di = nullptr;
+  tg_status st = device_info(&di);
+  if (st != TG_OK) return st;
+  CUtensorMap ma, mw;
+  if ((st = linear_maps(x, w_qkv, m, static_cast<int32_t>(n), kdim, &ma, &mw)) != TG_OK) return st;
+  LinearArgs la{};
+  la.m = m; la.n = static_cast<int32_t>(n); la.kdim = kdim;
+  la.status = di->status; la.watchdog = g_watchdog_cycles; la.num_sms = di->num_sms;
+  la.q_out = q_out; la.k_out = k_out; la.v_out = v_out; la.pos = pos;
+  la.hq = hq; la.hkv = hkv; la.head_dim = head_dim;
+  rope_turns(rope_theta, head_dim, &la.freqs);
+  cudaError_t e = launch_linear(ma, mw, la, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "QKV projection launch");
   return ok();
 }
 

@@ -198,6 +198,12 @@ __device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) 
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
+// A cluster barrier split in two: arrive now, wait later (every thread of
+// every CTA of the cluster executes both).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -427,6 +433,32 @@ __device__ __forceinline__ float2 gelu_erf2(float2 u) {
   const float2 phi = __ffma2_rn(erf_s, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));
   return __fmul2_rn(u, phi);
 }
+
+// sin and cos of the RoPE angle 2 pi * p * t for a position p >= 0 and a
+// rate t = th + tl turns per position (an unevaluated sum of two fp32 numbers,
+// split on the host in fp64).  p = p1 + p2 with p1 a multiple of 4096 and
+// p2 < 4096, both exact in fp32; each p_k * th is taken as its rounded
+// product plus the FMA-recovered rounding error (Dekker's two-product), the
+// integer turns are dropped exactly, and the small terms are added back.  The
+// fractional turn is good to ~1e-7 of a turn for p < 2^24 (~2e-6 at 2^31).
+// The products use __fmul_rn so that no FMA contraction folds them into the
+// subtractions that follow.
+__device__ __forceinline__ void rope_sincos(int p, float th, float tl, float* s, float* c) {
+  const float p1 = static_cast<float>(p & ~4095);
+  const float p2 = static_cast<float>(p & 4095);
+  const float x1 = __fmul_rn(p1, th), x2 = __fmul_rn(p2, th);
+  const float e = fmaf(p1, th, -x1) + fmaf(p2, th, -x2);     // the products' rounding errors, exactly
+  const float frac = ((x1 - rintf(x1)) + (x2 - rintf(x2))) + fmaf(static_cast<float>(p), tl, e);
+  sincospif(2.0f * frac, s, c);
+}
+
+// Programmatic dependent launch.  pdl_trigger: this CTA allows the next
+// kernel in the stream (launched with programmatic stream serialization) to
+// start launching; pdl_wait: block until the previous kernel in the stream
+// has completed and its memory is visible.  pdl_wait returns at once when
+// the kernel was launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // max of three floats in one instruction (sm_100+)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

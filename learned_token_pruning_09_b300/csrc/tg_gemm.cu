@@ -227,6 +227,9 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   cluster_sync();      // both CTAs' barriers exist before either signals the other
   tc_fence_after();
 
+  // the top-K launched after the gate may start launching now (its CTAs wait
+  // for the scores before they read anything)
+  pdl_trigger();
   uint32_t issued = 0;                 // warp 0 lane 0: stages this CTA issued
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer: this CTA's X rows and W1 half ----------------
@@ -360,6 +363,74 @@ struct LinearTail {
   PairHead head;
 };
 
+// One row's share of the Q/K/V projection epilogue: the accumulator columns
+// [n0, n0 + ncols) of buffer `tbase` (whole heads of head_dim), rotated by
+// RoPE at the row's position when the head is a q or k head, rounded to bf16
+// and written to q_out, k_out or v_out.  Rotate-half pairs column c with
+// c + D/2 of the same head, so each step reads 32 columns of both halves of a
+// head; the 32 angles of a step are shared by every head of the tile.  The
+// warp's last TMEM read releases the buffer (acc_empty, on the leader).
+__device__ __forceinline__ void qkv_rope_epilogue(const LinearArgs& a, uint32_t tbase, long long row, int n0,
+                                                  int ncols, uint32_t acc_empty_addr, int lane) {
+  const int D = a.head_dim, half = D >> 1;
+  const int heads_here = ncols / D;
+  const int head0 = n0 / D;
+  const bool in_rows = row < a.m;
+  const int p = in_rows ? __ldg(a.pos + row) : 0;
+  const bool rot_tile = head0 < a.hq + a.hkv;         // the tile holds a q or k head
+  for (int f0 = 0; f0 < half; f0 += 32) {
+    float cs[32], sn[32];
+    if (rot_tile) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) rope_sincos(p, a.freqs.turns_hi[f0 + j], a.freqs.turns_lo[f0 + j], &sn[j], &cs[j]);
+    }
+    for (int hh = 0; hh < heads_here; ++hh) {
+      uint32_t rl[32], rh[32];
+      tmem_ld32(tbase + static_cast<uint32_t>(hh * D + f0), rl);
+      tmem_ld32(tbase + static_cast<uint32_t>(hh * D + f0 + half), rh);
+      tmem_ld_wait();
+      if (f0 + 32 >= half && hh + 1 == heads_here) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_addr);
+      }
+      if (!in_rows) continue;
+      const int head = head0 + hh;
+      __nv_bfloat16* dst;
+      bool rot = true;
+      if (head < a.hq) {
+        dst = static_cast<__nv_bfloat16*>(a.q_out) + (row * a.hq + head) * static_cast<long long>(D);
+      } else if (head < a.hq + a.hkv) {
+        dst = static_cast<__nv_bfloat16*>(a.k_out) + (row * a.hkv + (head - a.hq)) * static_cast<long long>(D);
+      } else {
+        dst = static_cast<__nv_bfloat16*>(a.v_out) +
+              (row * a.hkv + (head - a.hq - a.hkv)) * static_cast<long long>(D);
+        rot = false;
+      }
+      uint4 olo[4], ohi[4];
+      uint32_t* pl = reinterpret_cast<uint32_t*>(olo);
+      uint32_t* ph = reinterpret_cast<uint32_t*>(ohi);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float l0 = __uint_as_float(rl[2 * j]), l1 = __uint_as_float(rl[2 * j + 1]);
+        const float h0 = __uint_as_float(rh[2 * j]), h1 = __uint_as_float(rh[2 * j + 1]);
+        if (rot) {
+          pl[j] = pack_bf16x2(l0 * cs[2 * j] - h0 * sn[2 * j], l1 * cs[2 * j + 1] - h1 * sn[2 * j + 1]);
+          ph[j] = pack_bf16x2(h0 * cs[2 * j] + l0 * sn[2 * j], h1 * cs[2 * j + 1] + l1 * sn[2 * j + 1]);
+        } else {
+          pl[j] = pack_bf16x2(l0, l1);
+          ph[j] = pack_bf16x2(h0, h1);
+        }
+      }
+      uint4* dl = reinterpret_cast<uint4*>(dst + f0);
+      uint4* dh = reinterpret_cast<uint4*>(dst + f0 + half);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) { dl[v] = olo[v]; dh[v] = ohi[v]; }
+    }
+  }
+}
+
+template <bool kQkv>
 __global__ void __launch_bounds__(kPairThreads, 1)
 linear_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
               LinearArgs a, int bn, int n_st) {
@@ -454,49 +525,53 @@ linear_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__
       const uint32_t tbase = head.tmem_base + static_cast<uint32_t>(b) * half_cols +
                              (static_cast<uint32_t>(sub * 32) << 16);
       const int ncols_here = min(bn, a.n - n0);
-      for (int c0 = 0; c0 < ncols_here; c0 += 32) {
-        uint32_t r[32];
-        const bool full32 = ncols_here - c0 >= 32;
-        if (full32) {
-          tmem_ld32(tbase + c0, r);
-        } else {
-          uint32_t r16[16];
-          tmem_ld16(tbase + c0, r16);
+      if constexpr (kQkv) {
+        qkv_rope_epilogue(a, tbase, row, n0, ncols_here, acc_empty0 + static_cast<uint32_t>(b) * 8u, lane);
+      } else {
+        for (int c0 = 0; c0 < ncols_here; c0 += 32) {
+          uint32_t r[32];
+          const bool full32 = ncols_here - c0 >= 32;
+          if (full32) {
+            tmem_ld32(tbase + c0, r);
+          } else {
+            uint32_t r16[16];
+            tmem_ld16(tbase + c0, r16);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) { r[i] = r16[i]; r[16 + i] = 0u; }
-        }
-        tmem_ld_wait();
-        if (c0 + 32 >= ncols_here) {
-          // the last TMEM read of this buffer: tell the leader's MMA issuer
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(b) * 8u);
-        }
-        if (row < a.m) {
-          const size_t off = static_cast<size_t>(row) * a.n + n0 + c0;
-          const int nv = full32 ? 4 : 2;              // 16-byte vectors (8 bf16)
-          uint4 res[4] = {};
-          if (a.residual) {
-            const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.residual) + off);
-            for (int v = 0; v < nv; ++v) res[v] = rp[v];
+            for (int i = 0; i < 16; ++i) { r[i] = r16[i]; r[16 + i] = 0u; }
           }
-          uint4* op = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + off);
-          for (int v = 0; v < nv; ++v) {
-            const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&res[v]);
-            uint4 o;
-            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float x0 = __uint_as_float(r[v * 8 + 2 * e]);
-              float x1 = __uint_as_float(r[v * 8 + 2 * e + 1]);
-              if (a.residual) {
-                const float2 rr = __bfloat1622float2(rb[e]);
-                x0 += rr.x;
-                x1 += rr.y;
-              }
-              ow[e] = pack_bf16x2(x0, x1);
+          tmem_ld_wait();
+          if (c0 + 32 >= ncols_here) {
+            // the last TMEM read of this buffer: tell the leader's MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(b) * 8u);
+          }
+          if (row < a.m) {
+            const size_t off = static_cast<size_t>(row) * a.n + n0 + c0;
+            const int nv = full32 ? 4 : 2;              // 16-byte vectors (8 bf16)
+            uint4 res[4] = {};
+            if (a.residual) {
+              const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.residual) + off);
+              for (int v = 0; v < nv; ++v) res[v] = rp[v];
             }
-            op[v] = o;
+            uint4* op = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + off);
+            for (int v = 0; v < nv; ++v) {
+              const __nv_bfloat162* rb = reinterpret_cast<const __nv_bfloat162*>(&res[v]);
+              uint4 o;
+              uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float x0 = __uint_as_float(r[v * 8 + 2 * e]);
+                float x1 = __uint_as_float(r[v * 8 + 2 * e + 1]);
+                if (a.residual) {
+                  const float2 rr = __bfloat1622float2(rb[e]);
+                  x0 += rr.x;
+                  x1 += rr.y;
+                }
+                ow[e] = pack_bf16x2(x0, x1);
+              }
+              op[v] = o;
+            }
           }
         }
       }
@@ -521,7 +596,8 @@ cudaError_t launch_linear(const CUtensorMap& map_a, const CUtensorMap& map_w, co
   if (e != cudaSuccess) return e;
   const size_t smem = static_cast<size_t>(n_st) * stage_bytes + sizeof(LinearTail);
   const long long tiles = ((a.m + 2 * kBM - 1) / (2 * kBM)) * ((a.n + bn - 1) / bn);
-  return launch_pairs(linear_kernel, smem, tiles, st, a.num_sms, map_a, map_w, a, bn, n_st);
+  if (a.q_out) return launch_pairs(linear_kernel<true>, smem, tiles, st, a.num_sms, map_a, map_w, a, bn, n_st);
+  return launch_pairs(linear_kernel<false>, smem, tiles, st, a.num_sms, map_a, map_w, a, bn, n_st);
 }
 
 }  // namespace tg

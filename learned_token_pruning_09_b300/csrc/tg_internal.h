@@ -68,6 +68,7 @@ cudaError_t launch_topk_count(const uint8_t* prunable, const int32_t* cu_seqlens
 // ---- gather ----------------------------------------------------------------
 struct GatherArgs {
   const void* x;
+  int64_t n_rows;           // rows of x (and s)
   int32_t d;
   const float* s;
   const int32_t* cu_seqlens;
@@ -206,6 +207,16 @@ struct LinearArgs {
   unsigned int* status;
   long long watchdog;
   int num_sms;
+  // Q/K/V projection with RoPE (out == null): the columns form heads of
+  // head_dim; the first hq heads go to q_out [m, hq, D], the next hkv to
+  // k_out [m, hkv, D], the rest to v_out [m, hkv, D]; q and k heads are
+  // rotated at pos[row]
+  void* q_out;
+  void* k_out;
+  void* v_out;
+  const int32_t* pos;
+  int32_t hq, hkv, head_dim;
+  RopeFreqs freqs;
 };
 // Columns of a linear tile: 256, or n itself when smaller (n is a multiple
 // of 16, so each CTA of a pair stages a multiple of 8 rows of W).

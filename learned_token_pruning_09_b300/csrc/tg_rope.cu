@@ -7,13 +7,8 @@
 // Angles: a = pos * theta^(-2i/D) reaches 1.3e5 rad at 128k context, where a
 // plain fp32 product would be off by ~1e-2 rad.  The angle is formed in turns,
 // pos * t with t = theta^(-2i/D) / (2 pi) held as an unevaluated sum of two
-// fp32 numbers (t_hi + t_lo, split on the host in fp64).  The position is
-// split as p1 + p2 (p1 a multiple of 4096, p2 < 4096), both exact in fp32 for
-// any int32; each p_k * t_hi is taken exactly as a rounded product plus its
-// FMA-recovered error (Dekker's two-product), its integer part is dropped
-// exactly, and the small terms are added back.  The fractional turn is good
-// to ~1e-7 of a turn for positions below 2^24 (~2e-6 at 2^31), and its sine
-// and cosine come from sincospif.  No fp64 arithmetic on the device.
+// fp32 numbers (t_hi + t_lo, split on the host in fp64), and reduced exactly
+// by rope_sincos (tg_common.cuh).  No fp64 arithmetic on the device.
 //
 // One warp per token (grid-stride), no block-wide synchronisation: every lane
 // of the warp handles the same 8-element column v of several heads (the
@@ -66,13 +61,7 @@ rope_kernel(RopeArgs a, RopeFreqs f) {
 #pragma unroll
       for (int q = 0; q < kShare; ++q) {
         const int i = v * 8 + grp * kShare + q;
-        const float th = th_s[i];
-        const float p1 = static_cast<float>(p & ~4095);     // exact: at most 19 significant bits
-        const float p2 = static_cast<float>(p & 4095);
-        const float x1 = p1 * th, x2 = p2 * th;
-        const float e = fmaf(p1, th, -x1) + fmaf(p2, th, -x2);   // the products' rounding errors, exactly
-        const float frac = ((x1 - rintf(x1)) + (x2 - rintf(x2))) + fmaf(static_cast<float>(p), tl_s[i], e);
-        sincospif(2.0f * frac, &ss[q], &cc[q]);
+        rope_sincos(p, th_s[i], tl_s[i], &ss[q], &cc[q]);
       }
       float cs[8], sn[8];
 #pragma unroll

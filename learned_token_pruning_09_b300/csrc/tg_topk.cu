@@ -6,12 +6,16 @@
 // contiguous slice of the sequence's document rows, converts its scores to
 // 32-bit order keys once (kept in shared memory when they fit) and the
 // cluster runs an MSB-first radix select (4 passes x 8 bits): every CTA
-// builds a 256-bin histogram of its slice, the histograms are summed across
-// the cluster through distributed shared memory, and every CTA derives the
-// same next digit.  The result is the exact K-th key and the number of keys
-// equal to it that are taken (lowest row index first).  A final ordered
-// compaction (warp ballots + prefix sums, slice offsets exchanged across the
-// cluster) writes the kept rows in ascending order, then the question rows.
+// builds a 256-bin histogram of its slice and stores it into its own slot of
+// every CTA's shared memory (distributed shared memory stores, which the
+// storing CTA does not wait for); after one cluster barrier each CTA sums the
+// slots locally and every CTA derives the same next digit.  The result is
+// the exact K-th key and the number of keys equal to it that are taken
+// (lowest row index first).  A final ordered compaction (warp ballots +
+// prefix sums; slice counts exchanged the same way) writes the kept rows in
+// ascending order, then the question rows.  No CTA reads another's shared
+// memory, and none writes into another's after the last cluster barrier, so
+// the CTAs may leave as soon as they are done.
 //
 // General prunable spans (a per-row mask instead of a document prefix): the
 // slices cover the whole sequence; a row outside the mask gets the key
@@ -31,7 +35,7 @@ constexpr int kTopkClusterMax = 16;   // non-portable cluster size, when the dev
 constexpr int kTopkClusterPortable = 8;
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkMaxSmemKeys = (200 * 1024) / 4;
+constexpr int kTopkMaxSmemKeys = (180 * 1024) / 4;
 constexpr uint32_t kFixedKey = 0xFFFFFFFFu;   // a row outside the prunable mask
 constexpr uint32_t kNoneKey = 0xFFFFFFFEu;    // "K-th key" when no prunable row is kept
 
@@ -46,12 +50,13 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 struct TopkShared {
-  uint32_t hist[2][256];
+  uint32_t slot[2][kTopkClusterMax][256];   // per pass parity: each CTA's histogram, stored by that CTA
+  uint32_t local[256];                      // this CTA's histogram of the current pass
   uint32_t warp_tot[8];
   uint32_t warp_gt[kTopkWarps];
   uint32_t warp_eq[kTopkWarps];
-  uint32_t cta_gt;          // read by the other CTAs of the cluster
-  uint32_t cta_eq;
+  uint32_t slice_gt[kTopkClusterMax];       // each CTA's kept-above and equal counts, stored by that CTA
+  uint32_t slice_eq[kTopkClusterMax];
   uint32_t digit;
   int32_t remaining;
   int32_t found;
@@ -63,6 +68,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
 topk_kernel(TopkArgs a) {
   extern __shared__ __align__(16) uint32_t keys_smem[];
   __shared__ TopkShared sh;
+  // launched early behind the gate (programmatic dependent launch): wait for
+  // it to finish before any global memory is read or written, and let the
+  // gather behind this kernel start launching
+  pdl_wait();
+  pdl_trigger();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int kTopkCluster = static_cast<int>(cluster.num_blocks());   // 8 or 16
@@ -127,6 +137,9 @@ topk_kernel(TopkArgs a) {
   }
   if (!kMasked && ke == 0) return;   // question only
   const bool none = kMasked && ke == 0;   // only the rows outside the mask
+  // every CTA of the cluster must be running before any stores into its
+  // shared memory: arrive here, wait before the first remote store
+  cluster_arrive_relaxed();
 
   if (kSmemKeys) {
     // eight loads in flight per thread before any is used (the scores were
@@ -158,18 +171,27 @@ topk_kernel(TopkArgs a) {
   int remaining = ke;
   for (int pass = 0; pass < (none ? 0 : 4); ++pass) {
     const int shift = 24 - 8 * pass;
-    uint32_t* h = sh.hist[pass & 1];
-    if (tid < 256) h[tid] = 0;
+    if (tid < 256) sh.local[tid] = 0;
     __syncthreads();
     for (int i = tid; i < n_loc; i += kTopkThreads) {
       const uint32_t key = key_at(i);
-      if ((!kMasked || key != kFixedKey) && (key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
+      if ((!kMasked || key != kFixedKey) && (key & mask) == prefix) atomicAdd(&sh.local[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    // this CTA's histogram into its slot of every CTA (two threads per bin,
+    // each covering half of the ranks)
+    if (pass == 0) cluster_wait();
+    {
+      const uint32_t bin = static_cast<uint32_t>(tid) & 255u;
+      const uint32_t v = sh.local[bin];
+      const uint32_t dst = smem_u32(&sh.slot[pass & 1][rank][bin]);
+      for (int r = tid >> 8; r < kTopkCluster; r += 2) st_cluster_u32(mapa_shared(dst, static_cast<uint32_t>(r)), v);
     }
     cluster.sync();
     // bin tid summed over the cluster; inclusive suffix sums over bins
     uint32_t tot = 0;
     if (tid < 256) {
-      for (int r = 0; r < kTopkCluster; ++r) tot += cluster.map_shared_rank(h, r)[tid];
+      for (int r = 0; r < kTopkCluster; ++r) tot += sh.slot[pass & 1][r][tid];
     }
     uint32_t suf = tot;
     if (warp < 8) {
@@ -194,8 +216,7 @@ topk_kernel(TopkArgs a) {
     __syncthreads();
     if (!sh.found) {          // counts inconsistent: cannot happen for valid input
       if (tid == 0) record_error(a.status, kStatusIndex);
-      cluster.sync();
-      return;
+      return;                 // every CTA sees the same sums, so all leave here
     }
     prefix |= sh.digit << shift;
     mask |= 255u << shift;
@@ -220,21 +241,22 @@ topk_kernel(TopkArgs a) {
   }
   if (lane == 0) { sh.warp_gt[warp] = gt; sh.warp_eq[warp] = eq; }
   __syncthreads();
-  if (tid == 0) {
+  if (none) cluster_wait();   // no radix pass ran, so the first remote store is here
+  if (tid < kTopkCluster) {
+    // this CTA's counts into its slots of CTA `tid`
     uint32_t g = 0, e = 0;
     for (int w2 = 0; w2 < kTopkWarps; ++w2) { g += sh.warp_gt[w2]; e += sh.warp_eq[w2]; }
-    sh.cta_gt = g;
-    sh.cta_eq = e;
+    st_cluster_u32(mapa_shared(smem_u32(&sh.slice_gt[rank]), static_cast<uint32_t>(tid)), g);
+    st_cluster_u32(mapa_shared(smem_u32(&sh.slice_eq[rank]), static_cast<uint32_t>(tid)), e);
   }
-  cluster.sync();
+  cluster.sync();   // the last cluster barrier: no CTA touches another's memory after it
   // offsets of this CTA's slice (CTAs of lower rank come first)
   uint32_t gt_before = 0, eq_before = 0;
   for (int r = 0; r < rank; ++r) {
-    const TopkShared* o = cluster.map_shared_rank(&sh, r);
-    gt_before += o->cta_gt;
-    eq_before += o->cta_eq;
+    gt_before += sh.slice_gt[r];
+    eq_before += sh.slice_eq[r];
   }
-  const int eq_take_cta = max(0, min(static_cast<int>(sh.cta_eq), take_eq - static_cast<int>(eq_before)));
+  const int eq_take_cta = max(0, min(static_cast<int>(sh.slice_eq[rank]), take_eq - static_cast<int>(eq_before)));
   const long long cta_out = static_cast<long long>(gt_before) + min(static_cast<int>(eq_before), take_eq);
   uint32_t gt_w = 0, eq_w = 0;
   for (int w2 = 0; w2 < warp; ++w2) { gt_w += sh.warp_gt[w2]; eq_w += sh.warp_eq[w2]; }
@@ -253,7 +275,6 @@ topk_kernel(TopkArgs a) {
     pos += __popc(keep_bal);
     eq_seen += __popc(eq_bal);
   }
-  cluster.sync();   // no CTA leaves while another may still read its counts
 }
 
 // Launch with `csize` CTAs per cluster; returns the launch error.
@@ -273,7 +294,7 @@ static cudaError_t launch_topk_cluster(const TopkArgs& a, int csize, cudaStream_
   cfg.blockDim = dim3(kTopkThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
@@ -285,6 +306,11 @@ static cudaError_t launch_topk_cluster(const TopkArgs& a, int csize, cudaStream_
   e = cudaOccupancyMaxActiveClusters(&n_clusters, kernel, &cfg);
   if (e != cudaSuccess) return e;
   if (n_clusters < 1) return cudaErrorInvalidConfiguration;
+  // programmatic dependent launch behind the previous kernel (the gate): the
+  // kernel waits for it before touching memory
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 

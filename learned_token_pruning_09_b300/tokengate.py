@@ -70,6 +70,7 @@ _SIGS = {
     "tg_gated_delta_scan": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
                             _vp],
     "tg_linear_bf16": [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp],
+    "tg_qkv_rope_bf16": [_vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp, _f32, _vp, _vp, _vp, _vp],
     "tg_check_device_status": [_vp],
     "tg_set_watchdog_cycles": [_ll],
     "tg_last_error_string": [],
@@ -483,3 +484,29 @@ def tg_linear_bf16(a: torch.Tensor, w: torch.Tensor, residual: Optional[torch.Te
     _check(lib.tg_linear_bf16(_ptr(a), _ptr(w), _ptr(residual), _ptr(out), m, n, kd, _stream(stream)),
            "tg_linear_bf16")
     return out
+
+
+def tg_qkv_rope_bf16(x: torch.Tensor, w_qkv: torch.Tensor, pos: torch.Tensor, hq: int, hkv: int, head_dim: int,
+                     rope_theta: float = 1.0e6, q_out: Optional[torch.Tensor] = None,
+                     k_out: Optional[torch.Tensor] = None, v_out: Optional[torch.Tensor] = None, stream=None):
+    """(q', k', v): x w_qkv^T split into q [m, hq, D], k and v [m, hkv, D],
+    q and k rotated by RoPE at pos (bf16)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(w_qkv, torch.bfloat16, "w_qkv", 2)
+    _need(pos, torch.int32, "pos", 1)
+    m, kd = x.shape
+    if w_qkv.shape != ((hq + 2 * hkv) * head_dim, kd):
+        raise ValueError("w_qkv must be [(hq + 2 hkv) head_dim, k]")
+    if pos.shape[0] != m:
+        raise ValueError("pos must have one entry per row")
+    e = lambda h: torch.empty((m, h, head_dim), dtype=torch.bfloat16, device=x.device)
+    q_out = e(hq) if q_out is None else q_out
+    k_out = e(hkv) if k_out is None else k_out
+    v_out = e(hkv) if v_out is None else v_out
+    for t, nm, h in ((q_out, "q_out", hq), (k_out, "k_out", hkv), (v_out, "v_out", hkv)):
+        _need(t, torch.bfloat16, nm, 3)
+        if tuple(t.shape) != (m, h, head_dim):
+            raise ValueError(f"{nm} must be [m, {h}, {head_dim}]")
+    _check(lib.tg_qkv_rope_bf16(_ptr(x), _ptr(w_qkv), m, kd, hq, hkv, head_dim, _ptr(pos), float(rope_theta),
+                                _ptr(q_out), _ptr(k_out), _ptr(v_out), _stream(stream)), "tg_qkv_rope_bf16")
+    return q_out, k_out, v_out

@@ -164,6 +164,8 @@ def test_host_validation_rejects_before_launch(tg):
     assert scan(beta=None) == tg.TG_ERR_INVALID_ARG
     assert scan(o=None) == tg.TG_ERR_INVALID_ARG
     assert scan(k=_c(264)) == tg.TG_ERR_INVALID_ARG           # not 16-byte aligned
+    assert scan(v=_c(264)) == tg.TG_ERR_INVALID_ARG
+    assert scan(dv=24) == tg.TG_ERR_INVALID_ARG               # not a multiple of the 16-row blocks
     # the layer around the path: norms, SwiGLU, decode attention
     assert L.tg_rms_norm(p, p, 10, 12, 1e-6, p, None) == tg.TG_ERR_INVALID_ARG       # d not a multiple of 8
     assert L.tg_rms_norm(p, p, 10, 64, -1.0, p, None) == tg.TG_ERR_INVALID_ARG       # negative eps
@@ -196,6 +198,13 @@ def test_host_validation_rejects_before_launch(tg):
     assert L.tg_linear_bf16(p, p, None, p, 10, 32, 96, None) == tg.TG_ERR_INVALID_ARG
     assert L.tg_linear_bf16(p, None, None, p, 10, 32, 64, None) == tg.TG_ERR_INVALID_ARG
     assert L.tg_linear_bf16(p, p, None, p, 0, 32, 64, None) == tg.TG_OK
+    # the fused Q/K/V projection: head size, kdim, theta and pointers checked on the host
+    assert L.tg_qkv_rope_bf16(p, p, 10, 64, 4, 2, 96, p, 1e6, p, p, p, None) == tg.TG_ERR_UNSUPPORTED
+    assert L.tg_qkv_rope_bf16(p, p, 10, 96, 4, 2, 64, p, 1e6, p, p, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_qkv_rope_bf16(p, p, 10, 64, 4, 2, 64, p, 0.0, p, p, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_qkv_rope_bf16(p, p, 10, 64, 4, 2, 64, None, 1e6, p, p, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_qkv_rope_bf16(p, p, 10, 64, 0, 2, 64, p, 1e6, p, p, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_qkv_rope_bf16(p, p, 0, 64, 4, 2, 64, p, 1e6, p, p, p, None) == tg.TG_OK
 
 
 def test_binding_refuses_cpu_tensors(tg):

@@ -1,6 +1,8 @@
 """GPU parity of the stacked token-gated layers of the long-context workload
-(q/k/v projections -> RoPE + token-gated attention -> output projection with
-the residual add) against the fp64 oracle.
+(the Q/K/V projection with RoPE fused into it -> token-gated attention on the
+rotated q', k' -> output projection with the residual add; and the same
+layer through plain projections and the attention call that rotates) against
+the fp64 oracle.
 
 * one layer at full size (131,008 + 64 tokens, K = 8192): inputs are the
   oracle's own gathered kept rows of the seeded residuals; attention outputs
@@ -43,25 +45,56 @@ def kept_inputs(shape):
     return xk, pos, sk, cu_kept
 
 
-def gpu_layer(tg, shape, x_dev, lp, pos, sk, cu_kept):
+def gpu_layer(tg, shape, x_dev, lp, pos, sk, cu_kept, fused=True):
+    """One stacked layer through the library.  fused: the Q/K/V projection
+    with RoPE in its epilogue, then the attention on the rotated q', k' (the
+    path the benchmark times); otherwise three plain projections and the
+    attention call that rotates them itself."""
     t = x_dev.shape[0]
     hq, hkv, dh = shape.hq, shape.hkv, shape.head_dim
     w = dev_bf16(lp["w_qkv"])
-    nq, nk = hq * dh, hkv * dh
-    q = tg.tg_linear_bf16(x_dev, w[:nq].contiguous()).view(t, hq, dh)
-    k = tg.tg_linear_bf16(x_dev, w[nq:nq + nk].contiguous()).view(t, hkv, dh)
-    v = tg.tg_linear_bf16(x_dev, w[nq + nk:].contiguous()).view(t, hkv, dh)
-    o = tg.tg_gated_attention_fwd(q, k, v, pos, sk, dev_f32(lp["gain"]), lp["tau"], 1e6, cu_kept,
-                                  int(torch.diff(cu_kept).max()))
+    max_kept = int(torch.diff(cu_kept).max())
+    if fused:
+        q_rot, k_rot, v = tg.tg_qkv_rope_bf16(x_dev, w, pos, hq, hkv, dh, 1e6)
+        o = tg.tg_gated_attention_rotated(q_rot, k_rot, v, pos, sk, dev_f32(lp["gain"]), lp["tau"], cu_kept,
+                                          max_kept)
+    else:
+        nq, nk = hq * dh, hkv * dh
+        q = tg.tg_linear_bf16(x_dev, w[:nq].contiguous()).view(t, hq, dh)
+        k = tg.tg_linear_bf16(x_dev, w[nq:nq + nk].contiguous()).view(t, hkv, dh)
+        v = tg.tg_linear_bf16(x_dev, w[nq + nk:].contiguous()).view(t, hkv, dh)
+        o = tg.tg_gated_attention_fwd(q, k, v, pos, sk, dev_f32(lp["gain"]), lp["tau"], 1e6, cu_kept, max_kept)
     out = tg.tg_linear_bf16(o.view(t, -1), dev_bf16(lp["w_o"]), residual=x_dev)
     return out, o
 
 
-def test_stacked_layer_full_size(tg):
+@pytest.mark.parametrize("m,kd,hq,hkv,dh", [(1000, 2048, 16, 8, 128), (300, 128, 4, 2, 64), (257, 64, 3, 1, 128),
+                                            (1, 64, 1, 1, 64), (129, 192, 2, 1, 64)])
+def test_qkv_rope_projection(tg, m, kd, hq, hkv, dh):
+    """tg_qkv_rope_bf16 against the oracle: q' and k' are RoPE(x W^T) at the
+    rows' positions, v = x W_v^T, each within one bf16 rounding of the exact
+    result (2^-8 relative, plus 1e-3 for the fp32 accumulation); n below
+    and above one 256-column tile, a partial last tile, positions up to 131k."""
+    rng = np.random.default_rng(m + kd + hq)
+    bf = lambda a: synth.f32_to_bf16_bits(np.asarray(a, np.float32))
+    x = bf(rng.standard_normal((m, kd)))
+    w = bf(rng.standard_normal(((hq + 2 * hkv) * dh, kd)) / np.sqrt(kd))
+    pos = np.sort(rng.choice(131072, m, replace=False)).astype(np.int32)
+    q, k, v = tg.tg_qkv_rope_bf16(dev_bf16(x), dev_bf16(w), dev_i32(pos), hq, hkv, dh, 1e6)
+    assert tg.tg_check_device_status() == tg.TG_OK
+    qkv = (oracle.bf16_decode(x) @ oracle.bf16_decode(w).T).reshape(m, hq + 2 * hkv, dh)
+    refs = (oracle.rope(qkv[:, :hq], pos), oracle.rope(qkv[:, hq:hq + hkv], pos), qkv[:, hq + hkv:])
+    for name, got, ref in zip("qkv", (q, k, v), refs):
+        ok, err, exc = allclose_report(host_f64(got), ref, 1e-3, 2.0 ** -8)
+        assert ok, f"{name}: max |err| {err:.3e} (excess {exc:.3e})"
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_stacked_layer_full_size(tg, fused):
     shape = synth.long_128k()
     xk, pos, sk, cu_kept = kept_inputs(shape)
     lp = synth.layer_params(shape, 0)
-    out, o = gpu_layer(tg, shape, dev_bf16(xk), lp, dev_i32(pos), dev_f32(sk), dev_i32(cu_kept))
+    out, o = gpu_layer(tg, shape, dev_bf16(xk), lp, dev_i32(pos), dev_f32(sk), dev_i32(cu_kept), fused)
     assert tg.tg_check_device_status() == tg.TG_OK
     t = len(pos)
     rng = np.random.default_rng(4)
@@ -101,7 +134,8 @@ def test_every_layer_parameters_scaled_down(tg):
     print(f"27 layer parameter sets: worst max |err| {worst:.3e}")
 
 
-def test_three_layer_composition_scaled_down(tg):
+@pytest.mark.parametrize("fused", [True, False])
+def test_three_layer_composition_scaled_down(tg, fused):
     shape = scaled_shape()
     xk, pos, sk, cu_kept = kept_inputs(shape)
     x_dev = dev_bf16(xk)
@@ -109,7 +143,7 @@ def test_three_layer_composition_scaled_down(tg):
     x_ref = oracle.bf16_decode(xk)
     for layer in range(3):
         lp = synth.layer_params(shape, layer)
-        x_dev, _ = gpu_layer(tg, shape, x_dev, lp, pos_d, sk_d, cu_d)
+        x_dev, _ = gpu_layer(tg, shape, x_dev, lp, pos_d, sk_d, cu_d, fused)
         x_ref, _ = oracle.stacked_layer(x_ref, lp["w_qkv"], lp["w_o"], pos, sk, lp["gain"], lp["tau"], cu_kept,
                                         shape.hq, shape.hkv, shape.head_dim)
     assert tg.tg_check_device_status() == tg.TG_OK
