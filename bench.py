@@ -495,6 +495,7 @@ class Path:
         self.T, self.max_nd, self.max_kept = T, max(shape.n_doc), max(shape.kept_lens)
         e = lambda *s, dt=torch.bfloat16: torch.empty(s, dtype=dt, device=dev)
         self.s = e(shape.n_rows, dt=torch.float32)
+        self.topk_ws = tg.tg_topk_workspace(shape.batch, dev)
         self.kept = e(T, dt=torch.int32)
         self.cu_kept = e(shape.batch + 1, dt=torch.int32)
         self.xk = e(T, d)
@@ -518,11 +519,12 @@ class Path:
 
     # the calls
     def gate(self):
-        self.tg.tg_gate_score(self.X, self.cu, self.nd, self.W1, None, self.W2, self.b2, s_out=self.s)
+        self.tg.tg_gate_score(self.X, self.cu, self.nd, self.W1, None, self.W2, self.b2, s_out=self.s,
+                              topk_ws=self.topk_ws)
 
     def topk(self):
         self.tg.tg_topk_select(self.s, self.cu, self.nd, self.kk, self.max_nd, self.T, kept_idx=self.kept,
-                               cu_kept=self.cu_kept)
+                               cu_kept=self.cu_kept, workspace=self.topk_ws)
 
     def gather(self):
         self.tg.tg_gather_kept(self.X, self.s, self.cu, self.kept, self.cu_kept, self.T, x_kept=self.xk,

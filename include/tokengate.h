@@ -84,6 +84,12 @@ typedef enum {
  *   b2         scalar
  *   h          hidden width, multiple of 16, 16 <= h <= 256
  *   s_out      [n_rows] fp32 output
+ *   topk_ws    NULL, or the workspace of the tg_topk_select call that will
+ *              read these scores (tg_topk_workspace_size(batch) bytes,
+ *              16-byte aligned, batch <= 65535): the gate's epilogue then
+ *              also counts each sequence's scores into the histograms that
+ *              give the top-K its first two radix digits
+ *   topk_ws_bytes  its size
  * Bf16 inputs, fp32 accumulation on the tensor cores, fp32 epilogue.
  * Device-side errors: n_doc out of range -> TG_ERR_DEVICE_INDEX (those rows
  * are then left unwritten).
@@ -91,7 +97,15 @@ typedef enum {
 TG_API tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d,
                         const int32_t* cu_seqlens, const int32_t* n_doc, int32_t batch,
                         const void* w1_bf16, const float* b1, const void* w2_bf16, float b2,
-                        int32_t h, float* s_out, cudaStream_t stream);
+                        int32_t h, float* s_out, void* topk_ws, size_t topk_ws_bytes,
+                        cudaStream_t stream);
+
+/*
+ * Bytes of the top-K workspace for `batch` sequences (0 for batch outside
+ * [1, 65535]): per sequence, counts of the scores' top 8 and top 16 bits of
+ * their order key (1 KB + 256 KB).  Host-only, no CUDA call.
+ */
+TG_API size_t tg_topk_workspace_size(int32_t batch);
 
 /*
  * Top-K selection (same section: "a top-K selector keeps the tokens with the
@@ -109,13 +123,27 @@ TG_API tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d,
  *               a larger n_doc[b] on the device -> TG_ERR_DEVICE_INDEX
  *   kept_idx    [sum_b T_b] int32 output, T_b = min(k[b], n_doc[b]) + n_q[b]
  *   cu_kept     [batch+1] int32 output, prefix sums of T_b
+ *   workspace   NULL, or tg_topk_workspace_size(batch) bytes (16-byte
+ *               aligned, batch <= 65535) that held zeros when first
+ *               allocated.  When the tg_gate_score call that produced s was
+ *               given the same workspace (and s is unchanged since), its
+ *               score histograms give the selection its first two radix
+ *               digits and it runs two passes instead of four.  The call
+ *               zeroes the histograms of every
+ *               sequence it completes, ready for the next gate call.  Counts
+ *               that do not match n_doc (a gate call whose histograms no
+ *               top-K consumed, or none at all) select with the four passes;
+ *               the result is the same either way.  Calls that share one
+ *               workspace must not overlap on the GPU.
+ *   ws_bytes    its size
  * Exact integer result: bit-identical to the definition for any input.
- * Uses no workspace.
+ * The kernel is launched early behind the previous kernel in the stream
+ * (programmatic dependent launch) and waits for it before touching memory.
  */
 TG_API tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* cu_seqlens,
                          const int32_t* n_doc, const int32_t* k, int32_t batch,
                          int32_t max_n_doc, int32_t* kept_idx, int32_t* cu_kept,
-                         cudaStream_t stream);
+                         void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * General prunable spans (the prompt template marks the prunable text; with

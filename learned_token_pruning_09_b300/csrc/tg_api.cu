@@ -146,7 +146,7 @@ static tg_status gate_score_any(const void* x_bf16, int64_t n_rows, int32_t d, c
                                 const int32_t* n_doc, int32_t batch, bool masked, const uint8_t* prunable,
                                 const void* w1_bf16,
                                 const float* b1, const void* w2_bf16, float b2, int32_t h, float* s_out,
-                                cudaStream_t stream) {
+                                void* topk_ws, size_t topk_ws_bytes, cudaStream_t stream) {
   if (n_rows < 0 || n_rows > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_rows out of range");
   if (!masked && batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
   if (d < 64 || d % 64 != 0 || d > (1 << 20)) return fail(TG_ERR_INVALID_ARG, "d must be a positive multiple of 64");
@@ -158,6 +158,13 @@ static tg_status gate_score_any(const void* x_bf16, int64_t n_rows, int32_t d, c
   if (!x_bf16 || !s_out) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(x_bf16) || !aligned16(w1_bf16)) return fail(TG_ERR_INVALID_ARG, "x and w1 must be 16-byte aligned");
   if (!std::isfinite(b2)) return fail(TG_ERR_INVALID_ARG, "b2 must be finite");
+  if (topk_ws) {
+    if (batch > kTopkMaxHistBatch) return fail(TG_ERR_INVALID_ARG, "a top-K workspace needs batch <= %d", kTopkMaxHistBatch);
+    if (topk_ws_bytes < tg_topk_workspace_size(batch))
+      return fail(TG_ERR_WORKSPACE, "top-K workspace of %zu bytes needed, %zu given", tg_topk_workspace_size(batch),
+                  topk_ws_bytes);
+    if (!aligned16(topk_ws)) return fail(TG_ERR_INVALID_ARG, "top-K workspace must be 16-byte aligned");
+  }
   DeviceInfo* di = nullptr;
   tg_status s = device_info(&di);
   if (s != TG_OK) return s;
@@ -176,6 +183,7 @@ static tg_status gate_score_any(const void* x_bf16, int64_t n_rows, int32_t d, c
     if ((s = make_map(&mw, w1_bf16, 2, dims, str, box, "w1")) != TG_OK) return s;
   }
   GateArgs a{};
+  a.hist = static_cast<uint32_t*>(topk_ws);
   a.prunable = prunable;
   a.b1 = b1;
   a.w2 = static_cast<const __nv_bfloat16*>(w2_bf16);
@@ -195,33 +203,47 @@ static tg_status gate_score_any(const void* x_bf16, int64_t n_rows, int32_t d, c
   return ok();
 }
 
+size_t tg_topk_workspace_size(int32_t batch) {
+  if (batch <= 0 || batch > kTopkMaxHistBatch) return 0;
+  return static_cast<size_t>(batch) * kHistWords * sizeof(uint32_t);
+}
+
 tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d, const int32_t* cu_seqlens,
                         const int32_t* n_doc, int32_t batch, const void* w1_bf16, const float* b1,
-                        const void* w2_bf16, float b2, int32_t h, float* s_out, cudaStream_t stream) {
+                        const void* w2_bf16, float b2, int32_t h, float* s_out, void* topk_ws,
+                        size_t topk_ws_bytes, cudaStream_t stream) {
   return gate_score_any(x_bf16, n_rows, d, cu_seqlens, n_doc, batch, false, nullptr, w1_bf16, b1, w2_bf16, b2, h,
-                        s_out, stream);
+                        s_out, topk_ws, topk_ws_bytes, stream);
 }
 
 tg_status tg_gate_score_masked(const void* x_bf16, int64_t n_rows, int32_t d, const uint8_t* prunable,
                                const void* w1_bf16, const float* b1, const void* w2_bf16, float b2, int32_t h,
                                float* s_out, cudaStream_t stream) {
   return gate_score_any(x_bf16, n_rows, d, nullptr, nullptr, 0, true, prunable, w1_bf16, b1, w2_bf16, b2, h, s_out,
-                        stream);
+                        nullptr, 0, stream);
 }
 
 tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* cu_seqlens, const int32_t* n_doc,
                          const int32_t* k, int32_t batch, int32_t max_n_doc, int32_t* kept_idx,
-                         int32_t* cu_kept, cudaStream_t stream) {
+                         int32_t* cu_kept, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   if (batch < 0 || batch > (1 << 24)) return fail(TG_ERR_INVALID_ARG, "batch out of range");
   if (n_rows < 0 || n_rows > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_rows out of range");
   if (max_n_doc < 0) return fail(TG_ERR_INVALID_ARG, "max_n_doc must be >= 0");
   if (batch == 0) return ok();
+  if (workspace) {
+    if (batch > kTopkMaxHistBatch) return fail(TG_ERR_INVALID_ARG, "a top-K workspace needs batch <= %d", kTopkMaxHistBatch);
+    if (ws_bytes < tg_topk_workspace_size(batch))
+      return fail(TG_ERR_WORKSPACE, "top-K workspace of %zu bytes needed, %zu given", tg_topk_workspace_size(batch),
+                  ws_bytes);
+    if (!aligned16(workspace)) return fail(TG_ERR_INVALID_ARG, "top-K workspace must be 16-byte aligned");
+  }
   if (!cu_seqlens || !n_doc || !k || !cu_kept) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
   if (n_rows > 0 && (!s || !kept_idx)) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
   DeviceInfo* di = nullptr;
   tg_status st = device_info(&di);
   if (st != TG_OK) return st;
   TopkArgs a{};
+  a.hist = static_cast<uint32_t*>(workspace);
   a.s = s;
   a.cu_seqlens = cu_seqlens;
   a.n_doc = n_doc;

@@ -452,6 +452,17 @@ __device__ __forceinline__ void rope_sincos(int p, float th, float tl, float* s,
   sincospif(2.0f * frac, s, c);
 }
 
+// Monotone map float -> uint32 used by the top-K and by the gate's score
+// histograms: a larger key means a larger score.  -0.0 is folded onto +0.0
+// (so the two tie and the lower index wins), every NaN maps to 0, below -inf
+// (0x007FFFFF).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0u;
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 // Programmatic dependent launch.  pdl_trigger: this CTA allows the next
 // kernel in the stream (launched with programmatic stream serialization) to
 // start launching; pdl_wait: block until the previous kernel in the stream

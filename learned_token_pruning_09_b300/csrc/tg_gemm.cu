@@ -168,12 +168,14 @@ struct GateTail {
   alignas(16) float w2[256];
 };
 
-__device__ __forceinline__ bool row_is_doc(const GateArgs& a, long long row) {
+// Whether `row` is a document row; *seq = its sequence.
+__device__ __forceinline__ bool row_is_doc(const GateArgs& a, long long row, int* seq) {
   int lo = 0, hi = a.batch - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (__ldg(a.cu_seqlens + mid) <= row) lo = mid; else hi = mid - 1;
   }
+  *seq = lo;
   const int start = __ldg(a.cu_seqlens + lo);
   const int nd = __ldg(a.n_doc + lo);
   const int len = __ldg(a.cu_seqlens + lo + 1) - start;
@@ -322,12 +324,30 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(b) * 8u);
+      int seq = 0;
+      bool counted = false;
+      float sc = 0.0f;
       if (row < a.n_rows) {
         z += a.b2;
         // logsigmoid(z) = -log1p(exp(-z)) (z >= 0), z - log1p(exp(z)) (z < 0)
-        const float sc = (z >= 0.0f) ? -log1pf(expf(-z)) : z - log1pf(expf(z));
-        const bool prun = a.prunable ? __ldg(a.prunable + row) != 0 : row_is_doc(a, row);
+        sc = (z >= 0.0f) ? -log1pf(expf(-z)) : z - log1pf(expf(z));
+        const bool prun = a.prunable ? __ldg(a.prunable + row) != 0 : row_is_doc(a, row, &seq);
         a.s_out[row] = prun ? sc : 0.0f;
+        counted = prun;
+      }
+      if (a.hist) {
+        // the top-K's first two radix digits, counted here: the top 8 and the
+        // top 16 bits of the score's order key, one atomic per distinct
+        // (sequence, bin) of the warp
+        const uint32_t key = order_key(sc);
+        uint32_t* hs = a.hist + static_cast<long long>(seq) * kHistWords;
+        const uint32_t ck = counted ? ((static_cast<uint32_t>(seq) << 8) | (key >> 24)) : 0xFFFFFFFFu;
+        const uint32_t cm = __match_any_sync(0xffffffffu, ck);
+        if (counted && lane == __ffs(cm) - 1) atomicAdd(hs + (key >> 24), static_cast<uint32_t>(__popc(cm)));
+        const uint32_t fk = counted ? ((static_cast<uint32_t>(seq) << 16) | (key >> 16)) : 0xFFFFFFFFu;
+        const uint32_t fm = __match_any_sync(0xffffffffu, fk);
+        if (counted && lane == __ffs(fm) - 1)
+          atomicAdd(hs + kHistCoarse + fine_slot(key >> 16), static_cast<uint32_t>(__popc(fm)));
       }
     }
   }

@@ -22,8 +22,22 @@ struct RopeFreqs {
   float turns_lo[kMaxHeadDimHalf];
 };
 
+// ---- score histograms of the top-K workspace ------------------------------
+// Per sequence: kHistCoarse counts of the top 8 bits of the scores' order
+// keys, then kHistFine counts of their top 16 bits, bin f stored at
+// fine_slot(f): scores cluster in a few hundred consecutive bins, and
+// transposing the two bytes puts those bins 1 KB apart, on many L2 slices,
+// instead of on a handful of cache lines that the gate's atomics would queue
+// on (slowing the residual stream through the same slices).
+constexpr int kHistCoarse = 256;
+constexpr int kHistFine = 65536;
+__host__ __device__ constexpr uint32_t fine_slot(uint32_t f) { return ((f & 255u) << 8) | (f >> 8); }
+constexpr int kHistWords = kHistCoarse + kHistFine;
+constexpr int kTopkMaxHistBatch = 65535;   // the gate packs (sequence, 16-bit bin) into 32 bits
+
 // ---- gate ------------------------------------------------------------------
 struct GateArgs {
+  uint32_t* hist;           // [batch][kHistWords] score histograms to add to, or null
   const uint8_t* prunable;  // [n_rows] per-row mask, or null: the document prefix (n_doc)
   const float* b1;          // [h] or null
   const __nv_bfloat16* w2;  // [h]
@@ -44,6 +58,7 @@ cudaError_t launch_gate(const CUtensorMap& map_x, const CUtensorMap& map_w1, con
 
 // ---- top-K -----------------------------------------------------------------
 struct TopkArgs {
+  uint32_t* hist;           // [batch][kHistWords] the gate's score histograms (zeroed after use), or null
   const float* s;
   const int32_t* cu_seqlens;
   // Prunable rows of each sequence: with `prunable` null, the first n_doc[b]

@@ -39,16 +39,6 @@ constexpr int kTopkMaxSmemKeys = (180 * 1024) / 4;
 constexpr uint32_t kFixedKey = 0xFFFFFFFFu;   // a row outside the prunable mask
 constexpr uint32_t kNoneKey = 0xFFFFFFFEu;    // "K-th key" when no prunable row is kept
 
-// Monotone map float -> uint32: a larger key means a larger score.  -0.0 is
-// folded onto +0.0 (so the two tie and the lower index wins), every NaN maps
-// to 0, below -inf (0x007FFFFF).
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t b = __float_as_uint(f);
-  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0u;
-  if (b == 0x80000000u) b = 0u;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
 struct TopkShared {
   uint32_t slot[2][kTopkClusterMax][256];   // per pass parity: each CTA's histogram, stored by that CTA
   uint32_t local[256];                      // this CTA's histogram of the current pass
@@ -57,11 +47,61 @@ struct TopkShared {
   uint32_t warp_eq[kTopkWarps];
   uint32_t slice_gt[kTopkClusterMax];       // each CTA's kept-above and equal counts, stored by that CTA
   uint32_t slice_eq[kTopkClusterMax];
+
   uint32_t digit;
   int32_t remaining;
   int32_t found;
+  uint32_t total;
   long long base;           // first output slot of this sequence
 };
+
+// The radix digit of the K-th key from 256 bin counts (bin t held by thread
+// t < 256, every thread of the CTA calls): d with suffix(d + 1) < remaining
+// <= suffix(d).  On success *digit is d and *rem the rank of the K-th key
+// inside bin d; *total is the sum of all bins.  Returns false when no bin
+// qualifies (the counts are inconsistent with `remaining`).
+__device__ __forceinline__ bool pick_digit(TopkShared& sh, uint32_t tot, int remaining, uint32_t* digit, int* rem,
+                                           uint32_t* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t suf = tot;
+  if (warp < 8) {
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
+      if (lane + o < 32) suf += v;
+    }
+    if (lane == 0) sh.warp_tot[warp] = suf;
+  }
+  if (tid == 0) sh.found = 0;
+  __syncthreads();
+  if (warp < 8) {
+    for (int w2 = warp + 1; w2 < 8; ++w2) suf += sh.warp_tot[w2];
+    // digit d is the one with suffix(d+1) < remaining <= suffix(d)
+    const uint32_t above = suf - tot;
+    if (static_cast<uint32_t>(remaining) <= suf && above < static_cast<uint32_t>(remaining)) {
+      sh.digit = static_cast<uint32_t>(tid);
+      sh.remaining = remaining - static_cast<int>(above);
+      sh.found = 1;
+    }
+    if (tid == 0) sh.total = suf;
+  }
+  __syncthreads();
+  *digit = sh.digit;
+  *rem = sh.remaining;
+  *total = sh.total;
+  const bool found = sh.found != 0;
+  __syncthreads();          // sh is reused by the next call
+  return found;
+}
+
+// This CTA's share of zeroing sequence b's score histograms (the cluster
+// covers them all), so the workspace is zero for the next gate call.
+__device__ __forceinline__ void zero_hist(uint32_t* hist, int b, int rank, int n_ranks) {
+  constexpr int kVecs = kHistWords / 4;
+  uint4* h = reinterpret_cast<uint4*>(hist + static_cast<long long>(b) * kHistWords);
+  const int per = (kVecs + n_ranks - 1) / n_ranks;
+  const int v1 = min(kVecs, (rank + 1) * per);
+  for (int v = rank * per + static_cast<int>(threadIdx.x); v < v1; v += kTopkThreads) h[v] = make_uint4(0u, 0u, 0u, 0u);
+}
 
 template <bool kSmemKeys, bool kMasked>
 __global__ void __launch_bounds__(kTopkThreads, 1)
@@ -133,10 +173,18 @@ topk_kernel(TopkArgs a) {
 
   if (ke == nd) {             // every prunable row kept, so every row (also nd == 0)
     for (int i = tid; i < n_loc; i += kTopkThreads) out[s0 + i] = lo + s0 + i;
+    if (a.hist) zero_hist(a.hist, b, rank, kTopkCluster);
     return;
   }
-  if (!kMasked && ke == 0) return;   // question only
+  if (!kMasked && ke == 0) {  // question only
+    if (a.hist) zero_hist(a.hist, b, rank, kTopkCluster);
+    return;
+  }
   const bool none = kMasked && ke == 0;   // only the rows outside the mask
+  // the gate's histograms of this sequence's scores (the first two digits);
+  // read before the keys so that the two loads overlap
+  const uint32_t* hc = a.hist ? a.hist + static_cast<long long>(b) * kHistWords : nullptr;
+  const uint32_t cnt0 = (hc && tid < 256) ? __ldcg(hc + tid) : 0u;
   // every CTA of the cluster must be running before any stores into its
   // shared memory: arrive here, wait before the first remote store
   cluster_arrive_relaxed();
@@ -169,7 +217,27 @@ topk_kernel(TopkArgs a) {
   // ---- radix select, 4 passes of 8 bits --------------------------------
   uint32_t prefix = 0, mask = 0;
   int remaining = ke;
-  for (int pass = 0; pass < (none ? 0 : 4); ++pass) {
+  int pass_begin = 0;
+  if (hc) {
+    // the first two digits from the gate's counts: every CTA reads the same
+    // bins and derives the same digits, with no exchange.  Counts that do not
+    // add up (a gate call whose histograms no top-K consumed) fall back to
+    // the four passes.
+    uint32_t d0 = 0, d1 = 0, tot0 = 0, tot1 = 0;
+    int r0 = 0, r1 = 0;
+    bool ok = pick_digit(sh, cnt0, ke, &d0, &r0, &tot0) && tot0 == static_cast<uint32_t>(nd);
+    if (ok) {
+      const uint32_t cnt1 = tid < 256 ? __ldcg(hc + kHistCoarse + fine_slot((d0 << 8) | tid)) : 0u;
+      ok = pick_digit(sh, cnt1, r0, &d1, &r1, &tot1) && tot1 == __ldcg(hc + d0);
+    }
+    if (ok) {
+      prefix = (d0 << 24) | (d1 << 16);
+      mask = 0xFFFF0000u;
+      remaining = r1;
+      pass_begin = 2;
+    }
+  }
+  for (int pass = pass_begin; pass < (none ? 0 : 4); ++pass) {
     const int shift = 24 - 8 * pass;
     if (tid < 256) sh.local[tid] = 0;
     __syncthreads();
@@ -180,7 +248,7 @@ topk_kernel(TopkArgs a) {
     __syncthreads();
     // this CTA's histogram into its slot of every CTA (two threads per bin,
     // each covering half of the ranks)
-    if (pass == 0) cluster_wait();
+    if (pass == pass_begin) cluster_wait();
     {
       const uint32_t bin = static_cast<uint32_t>(tid) & 255u;
       const uint32_t v = sh.local[bin];
@@ -188,39 +256,20 @@ topk_kernel(TopkArgs a) {
       for (int r = tid >> 8; r < kTopkCluster; r += 2) st_cluster_u32(mapa_shared(dst, static_cast<uint32_t>(r)), v);
     }
     cluster.sync();
-    // bin tid summed over the cluster; inclusive suffix sums over bins
+    // bin tid summed over the cluster, then this pass's digit
     uint32_t tot = 0;
     if (tid < 256) {
       for (int r = 0; r < kTopkCluster; ++r) tot += sh.slot[pass & 1][r][tid];
     }
-    uint32_t suf = tot;
-    if (warp < 8) {
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
-        if (lane + o < 32) suf += v;
-      }
-      if (lane == 0) sh.warp_tot[warp] = suf;
-    }
-    if (tid == 0) sh.found = 0;
-    __syncthreads();
-    if (warp < 8) {
-      for (int w2 = warp + 1; w2 < 8; ++w2) suf += sh.warp_tot[w2];
-      // digit d is the one with suffix(d+1) < remaining <= suffix(d)
-      const uint32_t above = suf - tot;
-      if (static_cast<uint32_t>(remaining) <= suf && above < static_cast<uint32_t>(remaining)) {
-        sh.digit = static_cast<uint32_t>(tid);
-        sh.remaining = remaining - static_cast<int>(above);
-        sh.found = 1;
-      }
-    }
-    __syncthreads();
-    if (!sh.found) {          // counts inconsistent: cannot happen for valid input
+    uint32_t digit = 0, total = 0;
+    int rem = 0;
+    if (!pick_digit(sh, tot, remaining, &digit, &rem, &total)) {   // cannot happen for valid input
       if (tid == 0) record_error(a.status, kStatusIndex);
       return;                 // every CTA sees the same sums, so all leave here
     }
-    prefix |= sh.digit << shift;
+    prefix |= digit << shift;
     mask |= 255u << shift;
-    remaining = sh.remaining;
+    remaining = rem;
   }
   const uint32_t kth = none ? kNoneKey : prefix;   // exact K-th largest key
   const int take_eq = none ? 0 : remaining;         // keys equal to kth that are kept
@@ -250,6 +299,8 @@ topk_kernel(TopkArgs a) {
     st_cluster_u32(mapa_shared(smem_u32(&sh.slice_eq[rank]), static_cast<uint32_t>(tid)), e);
   }
   cluster.sync();   // the last cluster barrier: no CTA touches another's memory after it
+  // every CTA read the histograms before its first push, so they can be cleared
+  if (a.hist) zero_hist(a.hist, b, rank, kTopkCluster);
   // offsets of this CTA's slice (CTAs of lower rank come first)
   uint32_t gt_before = 0, eq_before = 0;
   for (int r = 0; r < rank; ++r) {

@@ -96,11 +96,13 @@ class SyntheticModel:
         h, cache = self._attn_block(x, self.L, pos, cu, max_len, zeros_s, self.zero_gain, 1.0)
         caches.append(cache)
         nd = torch.as_tensor(np.asarray(n_doc, np.int32)).to(dev)
-        s = tg.tg_gate_score(h, cu, nd, self.gate["w1"], self.gate["b1"], self.gate["w2"], self.gate["b2"])
+        ws = tg.tg_topk_workspace(len(seqlens), dev)
+        s = tg.tg_gate_score(h, cu, nd, self.gate["w1"], self.gate["b1"], self.gate["w2"], self.gate["b2"],
+                             topk_ws=ws)
         kept_len = tg.kept_lengths(seqlens, n_doc, k)
         n_kept = int(sum(kept_len))
         kept, cu_kept = tg.tg_topk_select(s, cu, nd, torch.as_tensor(np.asarray(k, np.int32)).to(dev), max(n_doc),
-                                          n_kept)
+                                          n_kept, workspace=ws)
         hk, pos_k, s_k = tg.tg_gather_kept(h, s, cu, kept, cu_kept, n_kept)
         xk = self._mlp_block(hk, self.L)
         max_kept = max(kept_len)

@@ -48,8 +48,9 @@ lib = _load()
 _vp, _i64, _i32, _f32, _sz, _ll = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
                                    ctypes.c_size_t, ctypes.c_longlong)
 _SIGS = {
-    "tg_gate_score": [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _f32, _i32, _vp, _vp],
-    "tg_topk_select": [_vp, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp],
+    "tg_gate_score": [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _f32, _i32, _vp, _vp, _sz, _vp],
+    "tg_topk_workspace_size": [_i32],
+    "tg_topk_select": [_vp, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _sz, _vp],
     "tg_gate_score_masked": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _f32, _i32, _vp, _vp],
     "tg_topk_select_masked": [_vp, _i64, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
     "tg_gather_kept": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp],
@@ -81,6 +82,7 @@ for _name, _args in _SIGS.items():
     _f.argtypes = _args
     _f.restype = ctypes.c_int
 lib.tg_attention_workspace_size.restype = ctypes.c_size_t
+lib.tg_topk_workspace_size.restype = ctypes.c_size_t
 lib.tg_attention_bwd_workspace_size.restype = ctypes.c_size_t
 lib.tg_decode_workspace_size.restype = ctypes.c_size_t
 lib.tg_last_error_string.restype = ctypes.c_char_p
@@ -128,11 +130,22 @@ def tg_check_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
     return lib.tg_check_device_status(_stream(stream))
 
 
+def tg_topk_workspace(batch: int, device="cuda") -> torch.Tensor:
+    """A zero-filled top-K workspace for ``batch`` sequences (the gate's score
+    histograms), to pass to both tg_gate_score and tg_topk_select."""
+    n = int(lib.tg_topk_workspace_size(int(batch)))
+    if n == 0:
+        raise ValueError("batch must be in [1, 65535] for a top-K workspace")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
 def tg_gate_score(x: torch.Tensor, cu_seqlens: torch.Tensor, n_doc: torch.Tensor, w1: torch.Tensor,
                   b1: Optional[torch.Tensor], w2: torch.Tensor, b2: float,
-                  s_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                  s_out: Optional[torch.Tensor] = None, topk_ws: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
     """Gate scores s [n_rows] fp32 (logsigmoid of the gate MLP logit for
-    document rows, 0 for question rows)."""
+    document rows, 0 for question rows); with ``topk_ws`` also the score
+    histograms that tg_topk_select starts from."""
     _need(x, torch.bfloat16, "x", 2)
     _need(w1, torch.bfloat16, "w1", 2)
     _need(w2, torch.bfloat16, "w2", 1)
@@ -147,8 +160,10 @@ def tg_gate_score(x: torch.Tensor, cu_seqlens: torch.Tensor, n_doc: torch.Tensor
     if s_out is None:
         s_out = torch.empty(n_rows, dtype=torch.float32, device=x.device)
     _need(s_out, torch.float32, "s_out", 1)
+    ws_bytes = 0 if topk_ws is None else topk_ws.numel() * topk_ws.element_size()
     _check(lib.tg_gate_score(_ptr(x), n_rows, d, _ptr(cu_seqlens), _ptr(n_doc), n_doc.shape[0], _ptr(w1),
-                             _ptr(b1), _ptr(w2), float(b2), h, _ptr(s_out), _stream(stream)), "tg_gate_score")
+                             _ptr(b1), _ptr(w2), float(b2), h, _ptr(s_out), _ptr(topk_ws), ws_bytes,
+                             _stream(stream)), "tg_gate_score")
     return s_out
 
 
@@ -159,9 +174,11 @@ def kept_lengths(seqlens: Sequence[int], n_doc: Sequence[int], k: Sequence[int])
 
 def tg_topk_select(s: torch.Tensor, cu_seqlens: torch.Tensor, n_doc: torch.Tensor, k: torch.Tensor,
                    max_n_doc: int, n_kept: int, kept_idx: Optional[torch.Tensor] = None,
-                   cu_kept: Optional[torch.Tensor] = None, stream=None):
+                   cu_kept: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
     """Kept row ids [n_kept] int32 and cu_kept [batch+1] int32.  ``n_kept``
-    (host) sizes the output: sum over sequences of min(k, n_doc) + n_q."""
+    (host) sizes the output: sum over sequences of min(k, n_doc) + n_q.
+    ``workspace``: the one given to the tg_gate_score call that produced s
+    (see tg_topk_workspace), or None."""
     _need(s, torch.float32, "s", 1)
     for t, nme in ((cu_seqlens, "cu_seqlens"), (n_doc, "n_doc"), (k, "k")):
         _need(t, torch.int32, nme, 1)
@@ -170,8 +187,10 @@ def tg_topk_select(s: torch.Tensor, cu_seqlens: torch.Tensor, n_doc: torch.Tenso
         kept_idx = torch.empty(max(n_kept, 1), dtype=torch.int32, device=s.device)[:n_kept]
     if cu_kept is None:
         cu_kept = torch.empty(batch + 1, dtype=torch.int32, device=s.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.tg_topk_select(_ptr(s), s.shape[0], _ptr(cu_seqlens), _ptr(n_doc), _ptr(k), batch,
-                              int(max_n_doc), _ptr(kept_idx), _ptr(cu_kept), _stream(stream)), "tg_topk_select")
+                              int(max_n_doc), _ptr(kept_idx), _ptr(cu_kept), _ptr(workspace), ws_bytes,
+                              _stream(stream)), "tg_topk_select")
     return kept_idx, cu_kept
 
 

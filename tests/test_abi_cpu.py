@@ -63,19 +63,28 @@ def test_host_validation_rejects_before_launch(tg):
     L = tg.lib
     p = _c(256)      # a fake 16-byte-aligned address: never dereferenced
     # gate: d not a multiple of 64, h out of range, null weights, misalignment
-    assert L.tg_gate_score(p, 10, 63, p, p, 1, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_gate_score(p, 10, 64, p, p, 1, p, None, p, 0.0, 8, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_gate_score(p, 10, 64, p, p, 1, p, None, p, 0.0, 272, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_gate_score(p, 10, 64, p, p, 1, None, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_gate_score(_c(258), 10, 64, p, p, 1, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_gate_score(p, 10, 64, p, p, 0, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_gate_score(p, 10, 64, p, p, 1, p, None, p, float("nan"), 64, p, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 63, p, p, 1, p, None, p, 0.0, 64, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 1, p, None, p, 0.0, 8, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 1, p, None, p, 0.0, 272, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 1, None, None, p, 0.0, 64, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(_c(258), 10, 64, p, p, 1, p, None, p, 0.0, 64, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 0, p, None, p, 0.0, 64, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 1, p, None, p, float("nan"), 64, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
     assert b"multiple of 16" in L.tg_last_error_string() or L.tg_last_error_string()
     # top-K
-    assert L.tg_topk_select(p, 10, p, p, p, -1, 5, p, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_topk_select(p, 10, p, p, p, 1, -1, p, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_topk_select(p, 10, None, p, p, 1, 5, p, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_topk_select(p, 10, p, p, p, 0, 5, p, p, None) == tg.TG_OK       # empty batch: no-op
+    assert L.tg_topk_select(p, 10, p, p, p, -1, 5, p, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select(p, 10, p, p, p, 1, -1, p, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select(p, 10, None, p, p, 1, 5, p, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select(p, 10, p, p, p, 0, 5, p, p, None, 0, None) == tg.TG_OK       # empty batch: no-op
+    # the top-K workspace (the gate's score histograms): size, alignment, batch limit
+    ws = L.tg_topk_workspace_size(3)
+    assert ws == 3 * (256 + 65536) * 4
+    assert L.tg_topk_workspace_size(0) == 0 and L.tg_topk_workspace_size(65536) == 0
+    assert L.tg_topk_select(p, 10, p, p, p, 3, 5, p, p, p, ws - 4, None) == tg.TG_ERR_WORKSPACE
+    assert L.tg_topk_select(p, 10, p, p, p, 3, 5, p, p, _c(264), ws, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select(p, 10, p, p, p, 70000, 5, p, p, p, ws, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score(p, 10, 64, p, p, 3, p, None, p, 0.0, 64, p, p, ws - 4, None) == tg.TG_ERR_WORKSPACE
+    assert L.tg_gate_score(p, 10, 64, p, p, 3, p, None, p, 0.0, 64, p, _c(264), ws, None) == tg.TG_ERR_INVALID_ARG
     # general prunable spans
     assert L.tg_gate_score_masked(p, 10, 64, None, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
     assert L.tg_gate_score_masked(p, 10, 63, p, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG

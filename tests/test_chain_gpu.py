@@ -49,20 +49,23 @@ def kept_set_differences_are_near_ties(kept_gpu, kept_ref, s_ref, shape):
     return len(diff)
 
 
-@pytest.mark.parametrize("name", ["qwen3-1.7b-16k", "long-128k"])
+@pytest.mark.parametrize("name", ["qwen3-1.7b-16k", "long-128k", "ragged-8"])
 def test_document_chain_end_to_end(tg, name):
     shape = synth.ALL_SHAPES[name]()
     x, p = synth.residuals(shape), synth.gate_weights(shape)
     cu_d, nd_d = dev_i32(shape.cu_seqlens), dev_i32(shape.n_doc)
     X = dev_bf16(x)
-    s = tg.tg_gate_score(X, cu_d, nd_d, dev_bf16(p["w1"]), None, dev_bf16(p["w2"]), p["b2"])
-    kept, cu_kept = tg.tg_topk_select(s, cu_d, nd_d, dev_i32(shape.k), max(shape.n_doc), shape.n_kept)
+    ws = tg.tg_topk_workspace(shape.batch)
+    s = tg.tg_gate_score(X, cu_d, nd_d, dev_bf16(p["w1"]), None, dev_bf16(p["w2"]), p["b2"], topk_ws=ws)
+    kept, cu_kept = tg.tg_topk_select(s, cu_d, nd_d, dev_i32(shape.k), max(shape.n_doc), shape.n_kept, workspace=ws)
     xk, pos, sk = tg.tg_gather_kept(X, s, cu_d, kept, cu_kept, shape.n_kept)
     ai = synth.attention_inputs(shape)
     o, lse = tg.tg_gated_attention_fwd(dev_bf16(ai["q"]), dev_bf16(ai["k"]), dev_bf16(ai["v"]), pos, sk,
                                        dev_f32(ai["gain"]), ai["tau"], 1e6, cu_kept, max(shape.kept_lens),
                                        want_lse=True)
     assert tg.tg_check_device_status() == tg.TG_OK
+    # the top-K cleared the gate's score histograms for the next call
+    assert int(ws.count_nonzero()) == 0
 
     # gate
     s_gpu = s.cpu().numpy()

@@ -114,3 +114,71 @@ def test_gather_rejects_out_of_sequence_index(tg):
     tg.tg_gather_kept(dev_bf16(x), dev_f32(s), dev_i32(cu), dev_i32(kept), dev_i32(cu_kept), 5)
     assert tg.tg_check_device_status() == tg.TG_ERR_DEVICE_INDEX
     assert tg.tg_check_device_status() == tg.TG_OK      # cleared
+
+
+# ---------------------------------------------------------------------------
+# the top-K workspace: the gate's score histograms give the first two radix
+# digits (the result must be the same exact selection)
+# ---------------------------------------------------------------------------
+
+
+def gate_then_topk(tg, shape, x, p, ws, gate_calls=1):
+    cu, nd = dev_i32(shape.cu_seqlens), dev_i32(shape.n_doc)
+    X = dev_bf16(x)
+    for _ in range(gate_calls):
+        s = tg.tg_gate_score(X, cu, nd, dev_bf16(p["w1"]), None, dev_bf16(p["w2"]), p["b2"], topk_ws=ws)
+    kept, cu_kept = tg.tg_topk_select(s, cu, nd, dev_i32(shape.k), max(list(shape.n_doc) + [0]), shape.n_kept,
+                                      workspace=ws)
+    assert tg.tg_check_device_status() == tg.TG_OK
+    return s.cpu().numpy(), kept.cpu().numpy(), cu_kept.cpu().numpy()
+
+
+@pytest.mark.parametrize("case", ["tiny", "qwen3-1.7b-16k", "edges"])
+def test_topk_from_gate_histograms_is_exact(tg, case):
+    """Gate with the workspace, then top-K with it: bit-exact against the
+    oracle's top-K of the GPU's own scores, including K = 0, K >= n_doc, an
+    empty document and one-row documents; the workspace is zero afterwards,
+    and a second round on the same workspace is exact again."""
+    if case == "edges":
+        shape = synth.custom("edges", [0, 1, 300, 300, 1000, 129, 4096, 255, 256],
+                             [5, 3, 0, 17, 64, 1, 64, 9, 2], [4, 1, 0, 300, 999, 64, 4000, 1, 255],
+                             d=256, h=64, seed=77)
+    else:
+        shape = synth.ALL_SHAPES[case]()
+    x, p = synth.residuals(shape), synth.gate_weights(shape)
+    ws = tg.tg_topk_workspace(shape.batch)
+    for _ in range(2):
+        s, kept, cu_kept = gate_then_topk(tg, shape, x, p, ws)
+        ekept, ecu = oracle.topk_select(s, shape.cu_seqlens, shape.n_doc, shape.k)
+        np.testing.assert_array_equal(cu_kept, ecu)
+        np.testing.assert_array_equal(kept, ekept)
+        assert int(ws.count_nonzero()) == 0
+
+
+def test_topk_stale_histograms_fall_back_exactly(tg):
+    """Two gate calls into one workspace before the top-K (the counts then
+    exceed n_doc): the selection takes the four radix passes and is still
+    exact, and it leaves the workspace zero, so the next round is exact on
+    the histogram path again."""
+    shape = synth.custom("stale", [3000, 20, 700], [40, 5, 0], [900, 3, 700], d=256, h=64, seed=78)
+    x, p = synth.residuals(shape), synth.gate_weights(shape)
+    ws = tg.tg_topk_workspace(shape.batch)
+    for calls in (2, 1):
+        s, kept, cu_kept = gate_then_topk(tg, shape, x, p, ws, gate_calls=calls)
+        ekept, ecu = oracle.topk_select(s, shape.cu_seqlens, shape.n_doc, shape.k)
+        np.testing.assert_array_equal(kept, ekept)
+        np.testing.assert_array_equal(cu_kept, ecu)
+        assert int(ws.count_nonzero()) == 0
+
+
+def test_topk_workspace_without_gate_histograms(tg):
+    """A workspace with no gate counts in it (scores from elsewhere): exact."""
+    shape = synth.long_128k()
+    s = synth.score_draws(shape)
+    ws = tg.tg_topk_workspace(shape.batch)
+    kept, cu_kept = tg.tg_topk_select(dev_f32(s), dev_i32(shape.cu_seqlens), dev_i32(shape.n_doc),
+                                      dev_i32(shape.k), max(shape.n_doc), shape.n_kept, workspace=ws)
+    assert tg.tg_check_device_status() == tg.TG_OK
+    ekept, ecu = oracle.topk_select(s, shape.cu_seqlens, shape.n_doc, shape.k)
+    np.testing.assert_array_equal(kept.cpu().numpy(), ekept)
+    assert int(ws.count_nonzero()) == 0
