@@ -191,6 +191,9 @@ TG_API tg_status tg_topk_select_masked(const float* s, int64_t n_rows, const int
  *   n_kept  host-side total kept rows (= cu_kept[batch])
  *   x_kept_bf16 [n_kept, d] bf16, pos_kept [n_kept] int32, s_kept [n_kept]
  *   fp32 outputs; any of the three may be NULL to skip it.
+ * d is a multiple of 8 and x_bf16, x_kept_bf16 are 16-byte aligned (rows
+ * are moved by the bulk-copy engine through shared memory); otherwise
+ * TG_ERR_INVALID_ARG.
  * A kept index outside its sequence -> TG_ERR_DEVICE_INDEX, row skipped.
  * The kernel is launched early behind the previous kernel in the stream
  * (programmatic dependent launch) and waits for it before reading anything.

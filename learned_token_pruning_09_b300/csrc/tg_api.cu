@@ -323,6 +323,7 @@ tg_status tg_gather_kept(const void* x_bf16, int64_t n_rows, int32_t d, const fl
   a.pos_kept = pos_kept;
   a.s_kept = s_kept;
   a.status = di->status;
+  a.watchdog = g_watchdog_cycles;
   a.num_sms = di->num_sms;
   cudaError_t e = launch_gather(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");

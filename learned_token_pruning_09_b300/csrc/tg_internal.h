@@ -95,6 +95,7 @@ struct GatherArgs {
   int32_t* pos_kept;
   float* s_kept;
   unsigned int* status;
+  long long watchdog;
   int num_sms;
 };
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t st);

@@ -36,6 +36,7 @@ constexpr int kTopkClusterPortable = 8;
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkMaxSmemKeys = (180 * 1024) / 4;
+constexpr int kTopkBalChunks = 32;      // 32-key chunks per warp whose ballots the compaction keeps
 constexpr uint32_t kFixedKey = 0xFFFFFFFFu;   // a row outside the prunable mask
 constexpr uint32_t kNoneKey = 0xFFFFFFFEu;    // "K-th key" when no prunable row is kept
 
@@ -47,6 +48,8 @@ struct TopkShared {
   uint32_t warp_eq[kTopkWarps];
   uint32_t slice_gt[kTopkClusterMax];       // each CTA's kept-above and equal counts, stored by that CTA
   uint32_t slice_eq[kTopkClusterMax];
+  uint32_t bal_gt[kTopkWarps][kTopkBalChunks];   // per warp and 32-key chunk: keys above / equal to the K-th
+  uint32_t bal_eq[kTopkWarps][kTopkBalChunks];
 
   uint32_t digit;
   int32_t remaining;
@@ -190,19 +193,20 @@ topk_kernel(TopkArgs a) {
   cluster_arrive_relaxed();
 
   if (kSmemKeys) {
-    // eight loads in flight per thread before any is used (the scores were
-    // just written and sit in L2; one at a time would serialise its latency)
-    for (int i0 = tid; i0 < n_loc; i0 += 8 * kTopkThreads) {
-      float v[8];
-      uint8_t m[8];
+    // sixteen loads in flight per thread before any is used (the scores were
+    // just written and sit in L2; one at a time would serialise its latency):
+    // a 131k-row sequence's slice is one round
+    for (int i0 = tid; i0 < n_loc; i0 += 16 * kTopkThreads) {
+      float v[16];
+      uint8_t m[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const int i = i0 + u * kTopkThreads;
         v[u] = i < n_loc ? __ldg(src + i) : 0.0f;
         m[u] = (kMasked && i < n_loc) ? __ldg(msk + i) : 1;
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const int i = i0 + u * kTopkThreads;
         if (i < n_loc) keys_smem[i] = m[u] ? order_key(v[u]) : kFixedKey;
       }
@@ -275,18 +279,36 @@ topk_kernel(TopkArgs a) {
   const int take_eq = none ? 0 : remaining;         // keys equal to kth that are kept
 
   // ---- ordered compaction ---------------------------------------------
+  // each warp a segment of the slice, in 32-key chunks; the counting pass
+  // keeps each chunk's ballots when they fit, so that the writing pass needs
+  // neither the keys nor the comparisons again
   const int seg = ((n_loc + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
   const int w0 = min(n_loc, warp * seg);
   const int w1 = min(n_loc, w0 + seg);
+  const bool keep_bal = seg / 32 <= kTopkBalChunks;      // the same in every warp
+  const int n_chunks = (w1 - w0 + 31) / 32;
+  const uint32_t lt_mask = (1u << lane) - 1u;
   uint32_t gt = 0, eq = 0;
-  for (int i = w0 + lane; i < w1; i += 32) {
-    const uint32_t key = key_at(i);
-    gt += key > kth;
-    eq += key == kth;
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    gt += __shfl_down_sync(0xffffffffu, gt, o);
-    eq += __shfl_down_sync(0xffffffffu, eq, o);
+  if (keep_bal) {
+    for (int c = 0; c < n_chunks; ++c) {
+      const int i = w0 + c * 32 + lane;
+      const uint32_t key = i < w1 ? key_at(i) : 0u;
+      const uint32_t gb = __ballot_sync(0xffffffffu, i < w1 && key > kth);
+      const uint32_t eb = __ballot_sync(0xffffffffu, i < w1 && key == kth);
+      if (lane == 0) { sh.bal_gt[warp][c] = gb; sh.bal_eq[warp][c] = eb; }
+      gt += __popc(gb);
+      eq += __popc(eb);
+    }
+  } else {
+    for (int i = w0 + lane; i < w1; i += 32) {
+      const uint32_t key = key_at(i);
+      gt += key > kth;
+      eq += key == kth;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      gt += __shfl_down_sync(0xffffffffu, gt, o);
+      eq += __shfl_down_sync(0xffffffffu, eq, o);
+    }
   }
   if (lane == 0) { sh.warp_gt[warp] = gt; sh.warp_eq[warp] = eq; }
   __syncthreads();
@@ -313,7 +335,20 @@ topk_kernel(TopkArgs a) {
   for (int w2 = 0; w2 < warp; ++w2) { gt_w += sh.warp_gt[w2]; eq_w += sh.warp_eq[w2]; }
   long long pos = cta_out + gt_w + min(static_cast<int>(eq_w), eq_take_cta);
   int eq_seen = static_cast<int>(eq_w);
-  const uint32_t lt_mask = (1u << lane) - 1u;
+  if (keep_bal) {
+    for (int c = 0; c < n_chunks; ++c) {
+      uint32_t kb = sh.bal_gt[warp][c];
+      const uint32_t eb = sh.bal_eq[warp][c];
+      if (eb) {           // keys equal to the K-th: the first eq_take_cta of them in row order
+        const bool take = ((eb >> lane) & 1u) && eq_seen + __popc(eb & lt_mask) < eq_take_cta;
+        kb |= __ballot_sync(0xffffffffu, take);
+        eq_seen += __popc(eb);
+      }
+      if ((kb >> lane) & 1u) out[pos + __popc(kb & lt_mask)] = lo + s0 + w0 + c * 32 + lane;
+      pos += __popc(kb);
+    }
+    return;
+  }
   for (int i0 = w0; i0 < w1; i0 += 32) {
     const int i = i0 + lane;
     const uint32_t key = (i < w1) ? key_at(i) : 0u;

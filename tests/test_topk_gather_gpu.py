@@ -104,6 +104,43 @@ def test_gather_bit_exact(tg, name):
     np.testing.assert_array_equal(sk.cpu().numpy().view(np.uint32), es.view(np.uint32))
 
 
+@pytest.mark.parametrize("d", [8, 72, 4096])
+def test_gather_widths_and_rounds(tg, d):
+    """Rows of 16 bytes up to 8 KB: at d = 4096 each CTA copies its range in
+    several rounds of shared-memory slots; every kept row must land exactly."""
+    shape = synth.custom("gather-d%d" % d, [9000, 1, 4000, 131], [3, 0, 50, 2], [5000, 1, 3999, 1],
+                         d=d, seed=4242 + d)
+    x = synth.residuals(shape)
+    s = synth.score_draws(shape)
+    kept, cu_kept = oracle.topk_select(s, shape.cu_seqlens, shape.n_doc, shape.k)
+    ex, epos, es = oracle.gather_kept(x, s, shape.cu_seqlens, kept, cu_kept)
+    xk, pos, sk = tg.tg_gather_kept(dev_bf16(x), dev_f32(s), dev_i32(shape.cu_seqlens), dev_i32(kept),
+                                    dev_i32(cu_kept), len(kept))
+    assert tg.tg_check_device_status() == tg.TG_OK
+    np.testing.assert_array_equal(host_bits(xk), ex)
+    np.testing.assert_array_equal(pos.cpu().numpy(), epos)
+    np.testing.assert_array_equal(sk.cpu().numpy().view(np.uint32), es.view(np.uint32))
+
+
+def test_gather_invalid_id_inside_a_long_range(tg):
+    """One id outside its sequence, in the middle of a range that takes
+    several rounds: it is reported, and every other row is still copied."""
+    shape = synth.custom("gather-bad", [20000, 7000], [0, 0], [15000, 6000], d=4096, seed=99)
+    x = synth.residuals(shape)
+    s = synth.score_draws(shape)
+    kept, cu_kept = oracle.topk_select(s, shape.cu_seqlens, shape.n_doc, shape.k)
+    bad = 7777
+    kept_bad = kept.copy()
+    kept_bad[bad] = 20000 + 5                    # a row of the second sequence
+    ex, _, _ = oracle.gather_kept(x, s, shape.cu_seqlens, kept, cu_kept)
+    xk, _, _ = tg.tg_gather_kept(dev_bf16(x), dev_f32(s), dev_i32(shape.cu_seqlens), dev_i32(kept_bad),
+                                 dev_i32(cu_kept), len(kept))
+    assert tg.tg_check_device_status() == tg.TG_ERR_DEVICE_INDEX
+    got = host_bits(xk)
+    rows = np.arange(len(kept)) != bad
+    np.testing.assert_array_equal(got[rows], ex[rows])
+
+
 def test_gather_rejects_out_of_sequence_index(tg):
     """A kept id outside its sequence is reported, not read."""
     cu = np.array([0, 10, 20], np.int32)
@@ -180,5 +217,89 @@ def test_topk_workspace_without_gate_histograms(tg):
                                       dev_i32(shape.k), max(shape.n_doc), shape.n_kept, workspace=ws)
     assert tg.tg_check_device_status() == tg.TG_OK
     ekept, ecu = oracle.topk_select(s, shape.cu_seqlens, shape.n_doc, shape.k)
+    np.testing.assert_array_equal(kept.cpu().numpy(), ekept)
+    assert int(ws.count_nonzero()) == 0
+
+
+# White-box: the workspace filled on the host with the histograms the gate
+# would count (coarse bins of the top 8 bits of each score's order key, fine
+# bins of the top 16 bits at the transposed slot ((f & 255) << 8) | (f >> 8)),
+# for score vectors the gate would rarely produce: many keys tied in, or
+# sharing, the K-th key's 16-bit bin.
+
+def order_keys(s):
+    b = np.asarray(s, np.float32).view(np.uint32).copy()
+    b[(b & 0x7FFFFFFF) > 0x7F800000] = 0          # NaN
+    b[b == 0x80000000] = 0                          # -0 as +0
+    return np.where(b & 0x80000000, ~b, b | 0x80000000).astype(np.uint32)
+
+
+def host_histograms(s, cu, n_doc):
+    ws = np.zeros((len(n_doc), 256 + 65536), np.uint32)
+    for b, nd in enumerate(n_doc):
+        keys = order_keys(s[cu[b]: cu[b] + nd])
+        np.add.at(ws[b], keys >> 24, 1)
+        f = keys >> 16
+        np.add.at(ws[b], 256 + (((f & 255) << 8) | (f >> 8)), 1)
+    return ws
+
+
+def tied_scores(rng, nd, k, n_tied, n_near, contiguous=False):
+    """Scores spread evenly over 24,576 of the 16-bit bins (positive floats
+    with random bit patterns, about 5 per bin at 131k rows), then n_tied rows
+    set to one value v with k - n_tied // 2 other rows above it (so the K-th
+    key is v and only some of the ties are taken), and n_near rows set a few
+    ulps above or below v (the same 16-bit bin, other keys).  `contiguous`
+    puts those rows in one run (one slice of the selector then holds them
+    all) instead of scattering them."""
+    s = rng.integers(0x10000000, 0x70000000, nd, dtype=np.int64).astype(np.uint32).view(np.float32)
+    if contiguous:
+        rows = int(rng.integers(0, nd - n_tied - n_near)) + np.arange(n_tied + n_near)
+    else:
+        rows = rng.choice(nd, n_tied + n_near, replace=False)
+    rest = np.setdiff1d(np.arange(nd), rows)
+    above = k - n_tied // 2
+    v = np.sort(s[rest])[::-1][above]                 # `above` other rows lie strictly above v
+    s[rows[:n_tied]] = v
+    near = v.view(np.int32) + rng.integers(-3, 4, n_near).astype(np.int32)
+    s[rows[n_tied:]] = near.view(np.float32)
+    return s
+
+
+def kth_bin_sizes(s, cu, n_doc, ks):
+    out = []
+    for b, (nd, k) in enumerate(zip(n_doc, ks)):
+        keys = order_keys(s[cu[b]: cu[b] + nd])
+        kth = np.sort(keys)[::-1][min(k, nd) - 1]
+        out.append(int(np.sum((keys >> 16) == (kth >> 16))))
+    return out
+
+
+@pytest.mark.parametrize("n_tied,n_near,contiguous", [(1, 0, False), (40, 0, False), (200, 30, False),
+                                                      (300, 0, False), (2000, 100, False), (200, 0, True),
+                                                      (300, 0, True), (3000, 50, True)])
+def test_topk_histogram_start_with_ties(tg, n_tied, n_near, contiguous):
+    """The first two digits from the histograms, then the last two radix
+    passes over many keys in the K-th key's 16-bit bin, exact ties among
+    them scattered over the selector's slices or in one run inside one
+    slice: bit-exact, ties taken lowest row first across the slices."""
+    rng = np.random.default_rng(1000 + n_tied + contiguous)
+    n_doc = [131_008, 5_000, 700]
+    n_q = [64, 3, 0]
+    ks = [8_192, 1_000, 300]
+    cu = np.concatenate([[0], np.cumsum(np.array(n_doc) + np.array(n_q))]).astype(np.int32)
+    s = np.zeros(int(cu[-1]), np.float32)
+    for b in range(3):
+        s[cu[b]: cu[b] + n_doc[b]] = tied_scores(rng, n_doc[b], ks[b], min(n_tied, n_doc[b] // 8),
+                                                    min(n_near, n_doc[b] // 8), contiguous)
+        s[cu[b] + n_doc[b]: cu[b + 1]] = rng.standard_normal(n_q[b])
+    print("keys in the K-th key's 16-bit bin:", kth_bin_sizes(s, cu, n_doc, ks))
+    ws = torch.from_numpy(host_histograms(s, cu, n_doc).reshape(-1).view(np.uint8)).cuda()
+    n_kept = sum(min(k, n) + q for k, n, q in zip(ks, n_doc, n_q))
+    kept, cu_kept = tg.tg_topk_select(dev_f32(s), dev_i32(cu), dev_i32(n_doc), dev_i32(ks), max(n_doc), n_kept,
+                                      workspace=ws)
+    assert tg.tg_check_device_status() == tg.TG_OK
+    ekept, ecu = oracle.topk_select(s, cu, n_doc, ks)
+    np.testing.assert_array_equal(cu_kept.cpu().numpy(), ecu)
     np.testing.assert_array_equal(kept.cpu().numpy(), ekept)
     assert int(ws.count_nonzero()) == 0
