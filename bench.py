@@ -213,18 +213,29 @@ def measure_deltanet(dev, flush, steps, peaks, name="deltanet-32k-k4096"):
     beta = torch.as_tensor(inp["beta"]).to(dev)
     cu = torch.as_tensor(inp["cu_kept"]).to(dev)
     o = torch.empty_like(v)
-    tg.tg_gated_delta_scan(q, k, v, g, beta, cu, o=o)
-    torch.cuda.synchronize()
-    graph, evs = capture_step([("scan", lambda: tg.tg_gated_delta_scan(q, k, v, g, beta, cu, o=o))])
-    replay_timed(graph, evs, flush, 3)
-    us = float(replay_timed(graph, evs, flush, steps).mean()) * 1e3
-    if tg.tg_check_device_status() != tg.TG_OK:
-        raise RuntimeError("device status after the scan: " + tg.lib.tg_last_error_string().decode())
     t = int(inp["cu_kept"][-1])
+    nb = len(inp["cu_kept"]) - 1
+    ws = torch.empty(tg.tg_gated_delta_scan_workspace_size(t, nb, cfg["hv"], cfg["dk"], cfg["dv"]),
+                     dtype=torch.uint8, device=dev)
+
+    def timed(chunked):
+        call = lambda: tg.tg_gated_delta_scan(q, k, v, g, beta, cu, o=o, workspace=ws, chunked=chunked)
+        call()
+        torch.cuda.synchronize()
+        graph, evs = capture_step([("scan", call)])
+        replay_timed(graph, evs, flush, 3)
+        us = float(replay_timed(graph, evs, flush, steps).mean()) * 1e3
+        if tg.tg_check_device_status() != tg.TG_OK:
+            raise RuntimeError("device status after the scan: " + tg.lib.tg_last_error_string().decode())
+        return us
+
+    us = timed(True)
+    us_token = timed(False)
     byts = deltanet_bytes(t, cfg["hk"], cfg["hv"], cfg["dk"], cfg["dv"])
     return {"workload": name, "tokens": t, "hk": cfg["hk"], "hv": cfg["hv"], "dk": cfg["dk"], "dv": cfg["dv"],
-            "us": us, "gbs": byts / (us * 1e-6) / 1e9, "bytes": byts,
-            "frac_of_measured_hbm": byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+            "form": "chunked (tf32 tensor cores, workspace)", "us": us, "gbs": byts / (us * 1e-6) / 1e9,
+            "bytes": byts, "frac_of_measured_hbm": byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+            "workspace_bytes": int(ws.numel()), "token_by_token_us": us_token}
 
 
 def max_over_ranks(values, device):

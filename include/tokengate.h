@@ -346,16 +346,31 @@ TG_API size_t tg_attention_bwd_workspace_size(int64_t n_kept, int32_t hq);
  *   initial_state [batch, hv, dv, dk] fp32 or NULL
  *   o      [n_kept, hv, dv] bf16 output
  *   final_state   [batch, hv, dv, dk] fp32 output, or NULL
- * Every pointer 16-byte aligned.  fp32 state and arithmetic; o rounded once
- * to bf16.  No workspace.
- * Device-side errors: cu_kept out of range -> TG_ERR_DEVICE_INDEX.
+ *   workspace     NULL, or tg_gated_delta_scan_workspace_size(...) bytes,
+ *                 256-byte aligned: the chunked form on the tensor cores
+ *                 (chunks of 64 tokens; per-chunk products in parallel, then
+ *                 the state carried from chunk to chunk; tf32 MMAs on fp32
+ *                 operands).  Needs dv <= 128; with a larger dv, or NULL,
+ *                 the scan runs token by token on the CUDA cores (fp32) and
+ *                 the workspace is not touched.
+ * Every other pointer 16-byte aligned.  fp32 state and accumulation; o
+ * rounded once to bf16.
+ * Errors: a workspace smaller than the size -> TG_ERR_WORKSPACE.
+ * Device-side errors: cu_kept out of range -> TG_ERR_DEVICE_INDEX; a chunked
+ * kernel's wait past the watchdog -> TG_ERR_TIMEOUT.
  */
 TG_API tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v,
                               const float* g, const float* beta, const int32_t* cu_kept,
                               int32_t batch, int64_t n_kept, int32_t hk, int32_t hv,
                               int32_t dk, int32_t dv, float scale,
                               const float* initial_state, void* o, float* final_state,
-                              cudaStream_t stream);
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of the chunked scan's workspace: 0 when the shape does not take the
+ * chunked form (dk not 64 or 128, dv not a multiple of 16 in [16, 128], or
+ * batch < 1).  Host-only, no CUDA call. */
+TG_API size_t tg_gated_delta_scan_workspace_size(int64_t n_kept, int32_t batch, int32_t hv, int32_t dk,
+                                                 int32_t dv);
 
 /*
  * The layer around the pruned path, for the whole pruned prefill and its

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libtokengate.so")
 SOURCES = ["tg_api.cu", "tg_gemm.cu", "tg_topk.cu", "tg_gather.cu", "tg_rope.cu", "tg_attention.cu",
-           "tg_attention_bwd.cu", "tg_deltanet.cu", "tg_model.cu"]
+           "tg_attention_bwd.cu", "tg_deltanet.cu", "tg_deltanet_chunked.cu", "tg_model.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

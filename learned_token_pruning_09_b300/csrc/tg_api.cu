@@ -529,10 +529,16 @@ tg_status tg_gated_attention_bwd(const void* q_rot, const void* k_rot, const voi
   return ok();
 }
 
+size_t tg_gated_delta_scan_workspace_size(int64_t n_kept, int32_t batch, int32_t hv, int32_t dk, int32_t dv) {
+  if (batch < 1 || hv < 1 || n_kept < 0 || n_kept > 0x7FFFFFFF) return 0;
+  if ((dk != 64 && dk != 128) || dv < 16 || dv > 128 || dv % 16 != 0) return 0;
+  return delta_chunked_ws_bytes(n_kept, batch, hv, dk, dv);
+}
+
 tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v, const float* g, const float* beta,
                               const int32_t* cu_kept, int32_t batch, int64_t n_kept, int32_t hk, int32_t hv,
                               int32_t dk, int32_t dv, float scale, const float* initial_state, void* o,
-                              float* final_state, cudaStream_t stream) {
+                              float* final_state, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (batch < 1) return fail(TG_ERR_INVALID_ARG, "batch must be >= 1");
   if (n_kept < 0 || n_kept > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_kept out of range");
   if (hk < 1 || hv < 1 || hv % hk != 0) return fail(TG_ERR_INVALID_ARG, "hv must be a positive multiple of hk");
@@ -545,6 +551,11 @@ tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v, const
     return fail(TG_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
   if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
     return fail(TG_ERR_INVALID_ARG, "initial_state and final_state must be 16-byte aligned");
+  const size_t ws_need = tg_gated_delta_scan_workspace_size(n_kept, batch, hv, dk, dv);
+  const bool chunked = workspace != nullptr && ws_need > 0;
+  if (chunked && workspace_bytes < ws_need) return fail(TG_ERR_WORKSPACE, "delta scan workspace too small");
+  if (chunked && reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(TG_ERR_INVALID_ARG, "delta scan workspace must be 256-byte aligned");
   DeviceInfo* di = nullptr;
   tg_status st = device_info(&di);
   if (st != TG_OK) return st;
@@ -552,7 +563,9 @@ tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v, const
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_kept = cu_kept; a.batch = batch; a.n_kept = n_kept;
   a.hk = hk; a.hv = hv; a.dk = dk; a.dv = dv; a.scale = scale; a.initial_state = initial_state; a.o = o;
   a.final_state = final_state; a.status = di->status;
-  const cudaError_t e = launch_delta_scan(a, stream);
+  a.ws = chunked ? workspace : nullptr;
+  a.watchdog = g_watchdog_cycles;
+  const cudaError_t e = chunked ? launch_delta_scan_chunked(a, stream) : launch_delta_scan(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gated delta scan launch");
   return ok();
 }

@@ -184,8 +184,13 @@ struct ScanArgs {
   void* o;                    // [T, hv, dv] bf16
   float* final_state;         // [batch, hv, dv, dk] or null
   unsigned int* status;
+  void* ws;                   // chunked form: per-chunk products (delta_chunked_ws_bytes), or null
+  long long watchdog;
 };
 cudaError_t launch_delta_scan(const ScanArgs& a, cudaStream_t st);
+// chunked form on the tensor cores (dk 64 or 128, dv <= 128), with a workspace
+cudaError_t launch_delta_scan_chunked(const ScanArgs& a, cudaStream_t st);
+size_t delta_chunked_ws_bytes(long long n_kept, int batch, int hv, int dk, int dv);
 
 // ---- the layer around the pruned path: norms, SwiGLU, decode attention -----
 cudaError_t launch_rms_norm(const void* x, const void* w, long long rows, int d, float eps, void* y, int num_sms,

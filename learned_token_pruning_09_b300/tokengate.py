@@ -69,7 +69,8 @@ _SIGS = {
     "tg_decode_attention": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _vp, _vp, _f32, _i32, _i32, _i32, _vp,
                             _vp, _sz, _vp],
     "tg_gated_delta_scan": [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
-                            _vp],
+                            _vp, _sz, _vp],
+    "tg_gated_delta_scan_workspace_size": [_i64, _i32, _i32, _i32, _i32],
     "tg_linear_bf16": [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp],
     "tg_qkv_rope_bf16": [_vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp, _f32, _vp, _vp, _vp, _vp],
     "tg_check_device_status": [_vp],
@@ -85,6 +86,7 @@ lib.tg_attention_workspace_size.restype = ctypes.c_size_t
 lib.tg_topk_workspace_size.restype = ctypes.c_size_t
 lib.tg_attention_bwd_workspace_size.restype = ctypes.c_size_t
 lib.tg_decode_workspace_size.restype = ctypes.c_size_t
+lib.tg_gated_delta_scan_workspace_size.restype = ctypes.c_size_t
 lib.tg_last_error_string.restype = ctypes.c_char_p
 lib.tg_version.restype = ctypes.c_char_p
 lib.tg_set_watchdog_cycles.restype = None
@@ -399,12 +401,20 @@ def tg_gated_attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, po
     return (o, lse) if lse is not None else o
 
 
+def tg_gated_delta_scan_workspace_size(n_kept: int, batch: int, hv: int, dk: int, dv: int) -> int:
+    return int(lib.tg_gated_delta_scan_workspace_size(int(n_kept), int(batch), int(hv), int(dk), int(dv)))
+
+
 def tg_gated_delta_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
                         cu_kept: torch.Tensor, scale: Optional[float] = None,
                         initial_state: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
-                        final_state: Optional[torch.Tensor] = None, want_state: bool = False, stream=None):
+                        final_state: Optional[torch.Tensor] = None, want_state: bool = False,
+                        workspace: Optional[torch.Tensor] = None, chunked: bool = True, stream=None):
     """o [T, hv, dv] bf16 (and the final states [B, hv, dv, dk] fp32 when
-    requested or given): the gated delta rule over the kept tokens."""
+    requested or given): the gated delta rule over the kept tokens.
+    ``chunked``: the tensor-core chunked form, with ``workspace`` (allocated
+    here when None) of tg_gated_delta_scan_workspace_size bytes; False, or a
+    shape the chunked form does not take, runs the token-by-token kernel."""
     _need(q, torch.bfloat16, "q", 3)
     _need(k, torch.bfloat16, "k", 3)
     _need(v, torch.bfloat16, "v", 3)
@@ -425,8 +435,14 @@ def tg_gated_delta_scan(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: to
     if final_state is None and want_state:
         final_state = torch.empty((batch, hv, dv, dk), dtype=torch.float32, device=q.device)
     sc = (1.0 / dk ** 0.5) if scale is None else float(scale)
+    ws_bytes = tg_gated_delta_scan_workspace_size(t, batch, hv, dk, dv) if chunked else 0
+    if ws_bytes == 0:
+        workspace = None
+    elif workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     _check(lib.tg_gated_delta_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_kept), batch, t, hk, hv,
-                                   dk, dv, sc, _ptr(initial_state), _ptr(o), _ptr(final_state), _stream(stream)),
+                                   dk, dv, sc, _ptr(initial_state), _ptr(o), _ptr(final_state), _ptr(workspace),
+                                   workspace.numel() if workspace is not None else 0, _stream(stream)),
            "tg_gated_delta_scan")
     return (o, final_state) if final_state is not None else o
 

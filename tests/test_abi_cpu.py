@@ -157,12 +157,13 @@ def test_host_validation_rejects_before_launch(tg):
     assert L.tg_attention_bwd_workspace_size(0, 16) == 0
     # pruned Gated DeltaNet scan
     sc = dict(q=p, k=p, v=p, g=p, beta=p, cu=p, b=1, t=100, hk=16, hv=32, dk=128, dv=128, scale=0.088,
-              s0=None, o=p, s1=None)
+              s0=None, o=p, s1=None, ws=None, wsb=0)
 
     def scan(**kw):
         a = dict(sc, **kw)
         return L.tg_gated_delta_scan(a["q"], a["k"], a["v"], a["g"], a["beta"], a["cu"], a["b"], a["t"], a["hk"],
-                                     a["hv"], a["dk"], a["dv"], a["scale"], a["s0"], a["o"], a["s1"], None)
+                                     a["hv"], a["dk"], a["dv"], a["scale"], a["s0"], a["o"], a["s1"], a["ws"],
+                                     a["wsb"], None)
     assert scan(hv=24) == tg.TG_ERR_INVALID_ARG               # hv not a multiple of hk
     assert scan(dk=96) == tg.TG_ERR_UNSUPPORTED
     assert scan(dv=0) == tg.TG_ERR_INVALID_ARG
@@ -175,6 +176,16 @@ def test_host_validation_rejects_before_launch(tg):
     assert scan(k=_c(264)) == tg.TG_ERR_INVALID_ARG           # not 16-byte aligned
     assert scan(v=_c(264)) == tg.TG_ERR_INVALID_ARG
     assert scan(dv=24) == tg.TG_ERR_INVALID_ARG               # not a multiple of the 16-row blocks
+    # the chunked form's workspace: per (chunk slot, value head) the [W2; Qe]
+    # and Kd^T images, W1^T, Oloc^T and gamma_C; slots = n_kept / 64 + batch + 1
+    wsz = L.tg_gated_delta_scan_workspace_size
+    assert wsz(100, 1, 32, 128, 128) == (100 // 64 + 2) * 32 * (128 * 128 * 4 + 128 * 64 * 4 + 2 * 128 * 64 * 4 + 16)
+    assert wsz(100, 1, 32, 128, 256) == 0                    # dv > 128: token-by-token kernel only
+    assert wsz(100, 1, 32, 96, 128) == 0
+    assert wsz(100, 0, 32, 128, 128) == 0
+    assert wsz(0, 3, 4, 64, 64) > 0
+    assert scan(ws=p, wsb=10) == tg.TG_ERR_WORKSPACE
+    assert scan(ws=_c(272), wsb=1 << 40) == tg.TG_ERR_INVALID_ARG   # not 256-byte aligned
     # the layer around the path: norms, SwiGLU, decode attention
     assert L.tg_rms_norm(p, p, 10, 12, 1e-6, p, None) == tg.TG_ERR_INVALID_ARG       # d not a multiple of 8
     assert L.tg_rms_norm(p, p, 10, 64, -1.0, p, None) == tg.TG_ERR_INVALID_ARG       # negative eps
