@@ -84,6 +84,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src, u
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
+__device__ __forceinline__ void bulk_copy_s2g(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(dst), "r"(smem_u32(src_smem)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Byte offset of fp32 element (r, k) in a K-major tile with 128-byte swizzle:
 // K-blocks of 32 elements, each `rows` rows of 128 bytes; the 16-byte chunk
@@ -138,20 +145,20 @@ size_t delta_chunked_ws_bytes(long long n_kept, int batch, int hv, int dk, int d
 // ---------------------------------------------------------------------------
 // The kernel is written for a small instruction footprint (rolled loops over
 // 16-byte pieces and 16-column TMEM tiles, rows re-read from L1/L2 rather than
-// held in registers): two CTAs share an SM, each in its own phase, and fully
-// unrolled phases spent most of their time fetching instructions.
+// held in registers) and a small shared-memory and TMEM share, so that three
+// CTAs fit an SM and hide one another's latencies: every MMA operand passes
+// through one 32 KB buffer (the Gram product in 64-wide halves of the key
+// dims, then the four other products one after another), and the
+// accumulators use 128 TMEM columns.
 template <int DK>
 struct PrepSmem {
-  static constexpr int kAG = (128 * DK * 4 > 2 * 128 * kChunk * 4) ? 128 * DK * 4 : 2 * 128 * kChunk * 4;
-  alignas(1024) uint8_t ag[kAG];            // [k^; q^] (MMA A), then (beta v)^T | (beta gamma k^)^T, then W1^T | W2^T
+  alignas(1024) uint8_t buf[2 * 128 * 128];        // one [128 rows][64] fp32 MMA A operand (2 K-blocks)
   alignas(1024) uint8_t at[kChunk * kAStride * 4];   // A (plain rows), then T (swizzled [i][j])
   alignas(1024) uint8_t mq[kChunk * kChunk * 4];   // Mq, swizzled [i][j]
-  alignas(16) float tsc[32][36];           // T22, [row][column]
-  alignas(16) float xsc[32][36];            // T22 A21
   float G[kChunk];
   float beta[kChunk];
   float gam[kChunk];                        // exp(G)
-  float rn[kChunk];                         // 1 / |k_t|
+  float rn[128];                            // 1 / |k_t| (rows 0..63), scale / |q_t| (64..127)
   uint64_t bar;
   uint32_t tmem_base;
 };
@@ -195,8 +202,35 @@ delta_prep_kernel(ScanArgs a, long long slots) {
   const long long u = static_cast<long long>(x) * a.hv + h;
   float* bq = ws.bq + u * 128 * DK;
   float* kdT = ws.kd + u * DK * kChunk;
-  const uint32_t ag = smem_u32(sm.ag), at = smem_u32(sm.at), mq = smem_u32(sm.mq);
+  const uint32_t bufa = smem_u32(sm.buf), at = smem_u32(sm.at), mq = smem_u32(sm.mq);
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  uint32_t phase = 0;                       // of the MMA barrier
+  bool ok = true;
+  auto mma_wait = [&]() {
+    ok = mbar_wait(&sm.bar, phase & 1u, ok ? a.watchdog : kDrainCycles, a.status, kStatusTimeout) && ok;
+    ++phase;
+    tc_fence_after();
+  };
+  // one MMA of M 128, N 64 over K = 64 (8 steps) from the buffer and a B tile
+  // whose K-blocks hold b_rows rows (64 for T and Mq, 128 for the buffer itself)
+  auto mma_buf = [&](uint32_t d_col, uint32_t b_addr, int b_rows, bool accumulate) {
+    if (warp == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_tf32_f32(128, 64);
+      const uint64_t da = smem_desc_sw128(bufa, 16, 1024);
+      const uint64_t db = smem_desc_sw128(b_addr, 16, 1024);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_tf32_ss_warp(sm.tmem_base + d_col, da + (sw_kstep(128, ks) >> 4), db + (sw_kstep(b_rows, ks) >> 4),
+                         idesc, (accumulate || ks > 0) ? 1u : 0u);
+      mma_commit_warp(&sm.bar);
+    }
+  };
+  auto to_async = [&]() {                   // this thread's shared-memory writes, then the CTA
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+  };
 
   // 0. cumulative log-decays and write strengths of the chunk
   if (warp == 0) {
@@ -213,7 +247,7 @@ delta_prep_kernel(ScanArgs a, long long slots) {
     sm.gam[lane] = expf(g0); sm.gam[lane + 32] = expf(g1);
     sm.beta[lane] = b0; sm.beta[lane + 32] = b1;
   }
-  if (warp == 1) { tmem_alloc(&sm.tmem_base, 256); tmem_relinquish(); }
+  if (warp == 1) { tmem_alloc(&sm.tmem_base, 128); tmem_relinquish(); }
   if (tid == 0) { mbar_init(&sm.bar, 1); fence_barrier_init(); }
   tc_fence_before();
   __syncthreads();
@@ -225,11 +259,12 @@ delta_prep_kernel(ScanArgs a, long long slots) {
   const bool valid_t = t < n;
   const uint4* krow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.k) +
                                                      (static_cast<long long>(t0 + t) * a.hk + kh) * DK);
+  const uint4* src = is_k ? krow : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
+                                                                  (static_cast<long long>(t0 + t) * a.hk + kh) * DK);
+  const int row = is_k ? t : 64 + t;
 
-  // 1. k^ (threads 0..63, also Kd^T) and q^ (64..127) rows into the tile, tf32
+  // 1. the norms of the k (threads 0..63) and q (64..127) rows
   {
-    const uint4* src = is_k ? krow : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
-                                                                     (static_cast<long long>(t0 + t) * a.hk + kh) * DK);
     float ss = 0.f;
 #pragma unroll 4
     for (int p = 0; p < DK / 8; ++p) {
@@ -238,85 +273,51 @@ delta_prep_kernel(ScanArgs a, long long slots) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
     }
-    const float rn = (is_k ? 1.f : a.scale) * rsqrtf(ss + 1e-6f);
-    if (is_k) sm.rn[t] = rn;
+    sm.rn[row] = (is_k ? 1.f : a.scale) * rsqrtf(ss + 1e-6f);
+  }
+  // 2. D[0..63] = [k^; q^] k^^T over the key dims in halves of 64: each half
+  //    of the rows into the buffer (tf32), with Kd^T and gamma q^ of those dims
+  //    to the workspace, then its MMA
+  for (int hf = 0; hf < DK / 64; ++hf) {
+    if (hf > 0) __syncthreads();            // every thread has read the previous half
+    const float rn = sm.rn[row];
     const float kdc = expf(GC - sm.G[t]);
-    const int row = is_k ? t : 64 + t;
 #pragma unroll 2
-    for (int p = 0; p < DK / 8; ++p) {
+    for (int p = 0; p < 8; ++p) {
       float f[8];
-      bf16x8(valid_t ? __ldg(src + p) : make_uint4(0, 0, 0, 0), f);
+      bf16x8(valid_t ? __ldg(src + hf * 8 + p) : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] *= rn;
-      *reinterpret_cast<float4*>(sm.ag + sw_off(128, row, 8 * p)) =
+      *reinterpret_cast<float4*>(sm.buf + sw_off(128, row, 8 * p)) =
           make_float4(to_tf32(f[0]), to_tf32(f[1]), to_tf32(f[2]), to_tf32(f[3]));
-      *reinterpret_cast<float4*>(sm.ag + sw_off(128, row, 8 * p + 4)) =
+      *reinterpret_cast<float4*>(sm.buf + sw_off(128, row, 8 * p + 4)) =
           make_float4(to_tf32(f[4]), to_tf32(f[5]), to_tf32(f[6]), to_tf32(f[7]));
       if (is_k) {
-        // Kd^T image: rows 8p..8p+7 (key dims), column t (token)
+        // Kd^T image: rows (key dims) 64 hf + 8p .. +7, column t (token)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) kdT[sw_off(DK, 8 * p + e, t) >> 2] = to_tf32(kdc * f[e]);
+        for (int e = 0; e < 8; ++e) kdT[sw_off(DK, hf * 64 + 8 * p + e, t) >> 2] = to_tf32(kdc * f[e]);
       }
     }
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  // gamma q^ into the bq image rows 64..127 (completed to Qe in step 8): the
-  // q^ rows of the tile have the image's layout, so whole 16-byte pieces go
-  // out, consecutive threads on consecutive pieces
-  for (int e = tid; e < (DK / 32) * 512; e += kPrepThreads) {
-    const int kb = e >> 9, rr = (e >> 3) & 63;
-    const uint32_t off = kb * 16384 + (64 + rr) * 128 + (e & 7) * 16;
-    float4 v = *reinterpret_cast<const float4*>(sm.ag + off);
-    const float gm = sm.gam[rr];
-    v.x *= gm; v.y *= gm; v.z *= gm; v.w *= gm;
-    *reinterpret_cast<float4*>(reinterpret_cast<char*>(bq) + off) = v;
-  }
-  // 2. D[0..63] = [k^; q^] k^^T  (M 128, N 64, K dk)
-  if (warp == 0) {
-    tc_fence_after();
-    const uint32_t idesc = idesc_tf32_f32(128, 64);
-    const uint64_t da = smem_desc_sw128(ag, 16, 1024);
-#pragma unroll
-    for (int ks = 0; ks < DK / 8; ++ks) {
-      const uint32_t off = sw_kstep(128, ks) >> 4;
-      mma_tf32_ss_warp(tmem, da + off, da + off, idesc, ks > 0 ? 1u : 0u);
+    to_async();
+    // gamma q^ into the bq image rows 64..127 (completed to Qe in step 8): the
+    // buffer's q^ rows have the image's layout (K-blocks of 32 dims, 128 rows),
+    // so whole 16-byte pieces go out, consecutive threads on consecutive pieces
+    for (int e = tid; e < 2 * 512; e += kPrepThreads) {
+      const int kb = e >> 9, rr = (e >> 3) & 63;
+      const uint32_t off = kb * 16384 + (64 + rr) * 128 + (e & 7) * 16;
+      float4 v = *reinterpret_cast<const float4*>(sm.buf + off);
+      const float gm = sm.gam[rr];
+      v.x *= gm; v.y *= gm; v.z *= gm; v.w *= gm;
+      *reinterpret_cast<float4*>(reinterpret_cast<char*>(bq) + (2 * hf + kb) * 16384 + (64 + rr) * 128 + (e & 7) * 16) = v;
     }
-    mma_commit_warp(&sm.bar);
+    mma_buf(0, bufa, 128, hf > 0);          // B: the buffer's k^ rows 0..63
+    mma_wait();
   }
-  bool ok = mbar_wait(&sm.bar, 0, a.watchdog, a.status, kStatusTimeout);
-  tc_fence_after();
-  // 3. over the tile (its MMA is done) the right-hand sides: (beta v)^T in
-  //    the first 32 KB, (beta gamma k^)^T in the second, column t from rows
-  //    re-read from L1/L2; then A (plain rows) and Mq (swizzled) from the
-  //    Gram products
-  uint8_t* rhs_v = sm.ag;
-  uint8_t* rhs_k = sm.ag + 128 * kChunk * 4;
-  if (is_k) {
-    const float sc = sm.beta[t] * sm.gam[t] * sm.rn[t];
-#pragma unroll 2
-    for (int p = 0; p < DK / 8; ++p) {
-      float f[8];
-      bf16x8(valid_t ? __ldg(krow + p) : make_uint4(0, 0, 0, 0), f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) *reinterpret_cast<float*>(rhs_k + sw_off(128, 8 * p + e, t)) = to_tf32(sc * f[e]);
-    }
-  } else {
-    const float bt = sm.beta[t];
-    const uint4* vrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) +
-                                                       (static_cast<long long>(t0 + t) * a.hv + h) * dv);
-#pragma unroll 2
-    for (int p = 0; p < dv / 8; ++p) {
-      float f[8];
-      bf16x8(valid_t ? __ldg(vrow + p) : make_uint4(0, 0, 0, 0), f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) *reinterpret_cast<float*>(rhs_v + sw_off(128, 8 * p + e, t)) = to_tf32(bt * f[e]);
-    }
-  }
+  // 3. A (plain rows, threads 0..63) and Mq (swizzled, 64..127) from the Gram
+  //    products; exp(G_i - G_j) <= 1 for j <= i on the ex2 unit (relative
+  //    error ~2^-22)
   {
-    // exp(G_i - G_j) <= 1 for j <= i, on the ex2 unit (relative error ~2^-22)
-    const int i = t;                     // row of the Gram product in this lane
+    const int i = t;
     const float Gi = sm.G[i] * 1.44269504088896341f;
     float* arow = reinterpret_cast<float*>(sm.at) + i * kAStride;
     const float bi = sm.beta[i];
@@ -349,8 +350,11 @@ delta_prep_kernel(ScanArgs a, long long slots) {
   //    the diagonal blocks T11 = (I + A11)^-1 and T22 = (I + A22)^-1 by
   //    forward substitution, T_i = e_i - sum_{j<i} A_ij T_j (warps 0 and 1 at
   //    the same time, one column per lane, in registers); then Y = T22 A21
-  //    (warp 1, one column per lane) and T21 = -Y T11 (warp 0); T12 = 0.
+  //    (warp 1, one column per lane) and T21 = -Y T11 (warp 0); T12 = 0.  The
+  //    scratch for T22 and Y is the (free) buffer.
   if (warp < 2) {
+    float (*tsc)[36] = reinterpret_cast<float(*)[36]>(sm.buf);
+    float (*ysc)[36] = reinterpret_cast<float(*)[36]>(sm.buf + 32 * 36 * 4);
     const int k = lane;
     const int o = warp * 32;               // the block's first row and column
     const float* A = reinterpret_cast<const float*>(sm.at);
@@ -372,7 +376,7 @@ delta_prep_kernel(ScanArgs a, long long slots) {
     }
     if (warp == 1) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) sm.tsc[i][k] = tc[i];        // T22, [row][column]
+      for (int i = 0; i < 32; ++i) tsc[i][k] = tc[i];        // T22, [row][column]
       __syncwarp();
       // Y = T22 A21, column k: A21's column in registers, T22's rows broadcast
 #pragma unroll
@@ -382,13 +386,13 @@ delta_prep_kernel(ScanArgs a, long long slots) {
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
         for (int m4 = 0; m4 < 8; ++m4) {
-          const float4 tv = *reinterpret_cast<const float4*>(&sm.tsc[i][4 * m4]);
+          const float4 tv = *reinterpret_cast<const float4*>(&tsc[i][4 * m4]);
           s0 = fmaf(tv.x, tc[4 * m4], s0);
           s1 = fmaf(tv.y, tc[4 * m4 + 1], s1);
           s2 = fmaf(tv.z, tc[4 * m4 + 2], s2);
           s3 = fmaf(tv.w, tc[4 * m4 + 3], s3);
         }
-        sm.xsc[i][k] = (s0 + s1) + (s2 + s3);
+        ysc[i][k] = (s0 + s1) + (s2 + s3);
       }
     }
     asm volatile("bar.sync 1, 64;" ::: "memory");     // Y and T22 in the scratch; A is read
@@ -399,7 +403,7 @@ delta_prep_kernel(ScanArgs a, long long slots) {
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 yv = *reinterpret_cast<const float4*>(&sm.xsc[i][4 * j4]);
+          const float4 yv = *reinterpret_cast<const float4*>(&ysc[i][4 * j4]);
           s0 = fmaf(-yv.x, tc[4 * j4], s0);
           s1 = fmaf(-yv.y, tc[4 * j4 + 1], s1);
           s2 = fmaf(-yv.z, tc[4 * j4 + 2], s2);
@@ -413,57 +417,60 @@ delta_prep_kernel(ScanArgs a, long long slots) {
       // T22 and T12 = 0
 #pragma unroll 1
       for (int i = 0; i < 32; ++i) {
-        *reinterpret_cast<float*>(sm.at + sw_off(kChunk, 32 + i, 32 + k)) = to_tf32(sm.tsc[i][k]);
+        *reinterpret_cast<float*>(sm.at + sw_off(kChunk, 32 + i, 32 + k)) = to_tf32(tsc[i][k]);
         *reinterpret_cast<float*>(sm.at + sw_off(kChunk, i, 32 + k)) = 0.f;
       }
     }
   }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
-  // 5. W1^T = (beta v)^T T^T  (TMEM 64..127),  W2^T = (beta gamma k^)^T T^T  (128..191)
-  if (warp == 0) {
-    tc_fence_after();
-    const uint32_t idesc = idesc_tf32_f32(128, 64);
-    const uint64_t dv_ = smem_desc_sw128(smem_u32(rhs_v), 16, 1024);
-    const uint64_t dk_ = smem_desc_sw128(smem_u32(rhs_k), 16, 1024);
-    const uint64_t dt = smem_desc_sw128(at, 16, 1024);
+  // 5. W1^T = (beta v)^T T^T (TMEM 64..127), then W2^T = (beta gamma k^)^T T^T
+  //    (TMEM 0..63), each right-hand side through the buffer, column t from
+  //    the rows re-read from L1/L2
+  if (!is_k) {
+    const float bt = sm.beta[t];
+    const uint4* vrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) +
+                                                       (static_cast<long long>(t0 + t) * a.hv + h) * dv);
+#pragma unroll 2
+    for (int p = 0; p < dv / 8; ++p) {
+      float f[8];
+      bf16x8(valid_t ? __ldg(vrow + p) : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
-    for (int ks = 0; ks < kChunk / 8; ++ks) {
-      const uint32_t oa = sw_kstep(128, ks) >> 4, ob = sw_kstep(kChunk, ks) >> 4;
-      mma_tf32_ss_warp(tmem + 64, dv_ + oa, dt + ob, idesc, ks > 0 ? 1u : 0u);
-      mma_tf32_ss_warp(tmem + 128, dk_ + oa, dt + ob, idesc, ks > 0 ? 1u : 0u);
+      for (int e = 0; e < 8; ++e) *reinterpret_cast<float*>(sm.buf + sw_off(128, 8 * p + e, t)) = to_tf32(bt * f[e]);
     }
-    mma_commit_warp(&sm.bar);
   }
-  ok = mbar_wait(&sm.bar, 1, ok ? a.watchdog : kDrainCycles, a.status, kStatusTimeout) && ok;
-  tc_fence_after();
-  // 6. W1^T and W2^T rows back over the right-hand sides as the next A
-  //    operands; W1 (token rows) and W2 (the bq image rows 0..63) out
+  to_async();
+  mma_buf(64, at, kChunk, false);
+  mma_wait();
+  if (is_k) {
+    const float sc = sm.beta[t] * sm.gam[t] * sm.rn[t];
+#pragma unroll 2
+    for (int p = 0; p < DK / 8; ++p) {
+      float f[8];
+      bf16x8(valid_t ? __ldg(krow + p) : make_uint4(0, 0, 0, 0), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) *reinterpret_cast<float*>(sm.buf + sw_off(128, 8 * p + e, t)) = to_tf32(sc * f[e]);
+    }
+  }
+  to_async();
+  mma_buf(0, at, kChunk, false);
+  mma_wait();
+  // 6. W1^T rows into the buffer as the next A operand, W1 (token rows) out;
+  //    then Oloc^T = W1^T Mq^T (TMEM 64..127)
   {
-    const int r = tid;                  // TMEM lane = row (value row for W1^T, key dim for W2^T)
+    const int r = tid;                  // TMEM lane = value row
     float* w1u = ws.w1 + u * kChunk * dv;
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
-      uint32_t r1[16], r2[16];
+      uint32_t r1[16];
       tmem_ld16(tmem + lane_base + 64 + q * 16, r1);
-      tmem_ld16(tmem + lane_base + 128 + q * 16, r2);
       tmem_ld_wait();
 #pragma unroll
       for (int jj = 0; jj < 16; jj += 4) {
         const int j = q * 16 + jj;
-        float w1v[4], w2v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          w1v[e] = to_tf32(__uint_as_float(r1[jj + e]));
-          w2v[e] = to_tf32(__uint_as_float(r2[jj + e]));
-        }
-        *reinterpret_cast<float4*>(rhs_v + sw_off(128, r, j)) = make_float4(w1v[0], w1v[1], w1v[2], w1v[3]);
-        *reinterpret_cast<float4*>(rhs_k + sw_off(128, r, j)) = make_float4(w2v[0], w2v[1], w2v[2], w2v[3]);
-        if (r < DK) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) bq[sw_off(128, j + e, r) >> 2] = w2v[e];
-        }
+        *reinterpret_cast<float4*>(sm.buf + sw_off(128, r, j)) =
+            make_float4(to_tf32(__uint_as_float(r1[jj])), to_tf32(__uint_as_float(r1[jj + 1])),
+                        to_tf32(__uint_as_float(r1[jj + 2])), to_tf32(__uint_as_float(r1[jj + 3])));
         if (r < dv) {
           // token rows: the warp's 32 value rows of one token are one 128-byte line
 #pragma unroll
@@ -472,35 +479,48 @@ delta_prep_kernel(ScanArgs a, long long slots) {
       }
     }
   }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  // 7. (Mq W2)^T = W2^T Mq^T  (TMEM 0..63),  Oloc^T = W1^T Mq^T  (192..255)
-  if (warp == 0) {
-    tc_fence_after();
-    const uint32_t idesc = idesc_tf32_f32(128, 64);
-    const uint64_t dv_ = smem_desc_sw128(smem_u32(rhs_v), 16, 1024);
-    const uint64_t dk_ = smem_desc_sw128(smem_u32(rhs_k), 16, 1024);
-    const uint64_t dm = smem_desc_sw128(mq, 16, 1024);
-#pragma unroll
-    for (int ks = 0; ks < kChunk / 8; ++ks) {
-      const uint32_t oa = sw_kstep(128, ks) >> 4, ob = sw_kstep(kChunk, ks) >> 4;
-      mma_tf32_ss_warp(tmem + 0, dk_ + oa, dm + ob, idesc, ks > 0 ? 1u : 0u);
-      mma_tf32_ss_warp(tmem + 192, dv_ + oa, dm + ob, idesc, ks > 0 ? 1u : 0u);
-    }
-    mma_commit_warp(&sm.bar);
-  }
-  ok = mbar_wait(&sm.bar, 0, ok ? a.watchdog : kDrainCycles, a.status, kStatusTimeout) && ok;
-  tc_fence_after();
-  // 8. Qe = gamma q^ - Mq W2 into the bq image rows 64..127; Oloc (token rows)
+  to_async();
+  mma_buf(64, mq, kChunk, false);
+  mma_wait();
+  // 7. Oloc (token rows) out; W2^T rows into the buffer and W2 into the bq
+  //    image rows 0..63; then (Mq W2)^T = W2^T Mq^T (TMEM 0..63)
   {
     const int r = tid;
     float* olu = ws.ol + u * kChunk * dv;
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       uint32_t r1[16], r2[16];
+      tmem_ld16(tmem + lane_base + 64 + q * 16, r1);
+      tmem_ld16(tmem + lane_base + 0 + q * 16, r2);
+      tmem_ld_wait();
+      if (r < dv) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) olu[(q * 16 + jj) * dv + r] = __uint_as_float(r1[jj]);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 16; jj += 4) {
+        const int j = q * 16 + jj;
+        float w2v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w2v[e] = to_tf32(__uint_as_float(r2[jj + e]));
+        *reinterpret_cast<float4*>(sm.buf + sw_off(128, r, j)) = make_float4(w2v[0], w2v[1], w2v[2], w2v[3]);
+        if (r < DK) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) bq[sw_off(128, j + e, r) >> 2] = w2v[e];
+        }
+      }
+    }
+  }
+  to_async();
+  mma_buf(0, mq, kChunk, false);
+  mma_wait();
+  // 8. Qe = gamma q^ - Mq W2 into the bq image rows 64..127
+  {
+    const int r = tid;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t r1[16];
       tmem_ld16(tmem + lane_base + 0 + q * 16, r1);
-      tmem_ld16(tmem + lane_base + 192 + q * 16, r2);
       tmem_ld_wait();
       if (r < DK) {
         // all 16 loads before any store (one round trip)
@@ -511,17 +531,12 @@ delta_prep_kernel(ScanArgs a, long long slots) {
         for (int jj = 0; jj < 16; ++jj)
           bq[sw_off(128, 64 + q * 16 + jj, r) >> 2] = to_tf32(gq[jj] - __uint_as_float(r1[jj]));
       }
-      if (r < dv) {
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) olu[(q * 16 + jj) * dv + r] = __uint_as_float(r2[jj]);
-      }
     }
     if (tid == 0) ws.gc[u] = expf(GC);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 256);
-  (void)ok;
+  if (warp == 1) tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------------------
@@ -553,7 +568,7 @@ struct ChainSmem {
   alignas(1024) uint8_t bq[2][128 * DK * 4];       // [W2; Qe] images
   alignas(1024) uint8_t kd[2][DK * kChunk * 4];    // Kd^T images
   alignas(16) uint16_t ostage[2][kChunk * 128];    // a chunk's bf16 outputs, [token][value row]
-  uint64_t full[2], empty[2], a1_done, a3_done[2], d_free[2], u_ready, init_ready, fin;
+  uint64_t bq_full[2], kd_full[2], bq_empty[2], kd_empty[2], a1_done, a3_done[2], d_free[2], u_ready, init_ready, fin;
   uint32_t tmem_base;
   int abort;
 };
@@ -582,8 +597,10 @@ delta_chain_kernel(ScanArgs a, long long slots) {
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.bq_full[s], 1);
+      mbar_init(&sm.kd_full[s], 1);
+      mbar_init(&sm.bq_empty[s], 1);
+      mbar_init(&sm.kd_empty[s], 1);
       mbar_init(&sm.a3_done[s], 1);
       mbar_init(&sm.d_free[s], 4);
     }
@@ -607,22 +624,35 @@ delta_chain_kernel(ScanArgs a, long long slots) {
 
   if (warp == 4) {
     // ---------------- operand copies ----------------
+    // the [W2; Qe] image of a stage is free once the chunk's two first
+    // products have read it, its Kd^T image once the state update has: each
+    // is refilled as soon as it is free
     if (lane == 0) {
-      int c = 0;
-      for (; c < nc && !sm.abort; ++c) {
+      int bq_issued = 0, kd_issued = 0;
+      for (int c = 0; c < nc && !sm.abort; ++c) {
         const int s = c & 1;
-        if (c >= 2 && !mbar_wait(&sm.empty[s], ((c >> 1) - 1) & 1, wd, a.status, kStatusTimeout)) {
+        const long long u = (slot0 + c) * a.hv + h;
+        if (c >= 2 && !mbar_wait(&sm.bq_empty[s], ((c >> 1) - 1) & 1, wd, a.status, kStatusTimeout)) {
           sm.abort = 1;
           break;
         }
-        const long long u = (slot0 + c) * a.hv + h;
-        mbar_arrive_expect_tx(&sm.full[s], kBqBytes + kKdBytes);
-        bulk_copy_g2s(sm.bq[s], ws.bq + u * 128 * DK, kBqBytes, &sm.full[s]);
-        bulk_copy_g2s(sm.kd[s], ws.kd + u * DK * kChunk, kKdBytes, &sm.full[s]);
+        mbar_arrive_expect_tx(&sm.bq_full[s], kBqBytes);
+        bulk_copy_g2s(sm.bq[s], ws.bq + u * 128 * DK, kBqBytes, &sm.bq_full[s]);
+        bq_issued = c + 1;
+        if (c >= 2 && !mbar_wait(&sm.kd_empty[s], ((c >> 1) - 1) & 1, wd, a.status, kStatusTimeout)) {
+          sm.abort = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.kd_full[s], kKdBytes);
+        bulk_copy_g2s(sm.kd[s], ws.kd + u * DK * kChunk, kKdBytes, &sm.kd_full[s]);
+        kd_issued = c + 1;
       }
-      // every copy issued has landed before the CTA leaves
-      for (int c2 = max(0, c - 2); c2 < c; ++c2)
-        mbar_wait(&sm.full[c2 & 1], (c2 >> 1) & 1, kDrainCycles, a.status, kStatusTimeout);
+      // every copy issued has landed before the CTA leaves (the earlier ones
+      // were waited for by the MMA issuer before it freed their stages)
+      for (int c2 = max(0, bq_issued - 2); c2 < bq_issued; ++c2)
+        mbar_wait(&sm.bq_full[c2 & 1], (c2 >> 1) & 1, kDrainCycles, a.status, kStatusTimeout);
+      for (int c2 = max(0, kd_issued - 2); c2 < kd_issued; ++c2)
+        mbar_wait(&sm.kd_full[c2 & 1], (c2 >> 1) & 1, kDrainCycles, a.status, kStatusTimeout);
     }
   } else if (warp == 5) {
     // ---------------- MMA issue ----------------
@@ -635,7 +665,7 @@ delta_chain_kernel(ScanArgs a, long long slots) {
     int issued = 0;
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c & 1;
-      if (!wait(&sm.full[s], (c >> 1) & 1)) { ok = false; break; }
+      if (!wait(&sm.bq_full[s], (c >> 1) & 1)) { ok = false; break; }
       if (c >= 2 && !wait(&sm.d_free[s], ((c >> 1) - 1) & 1)) { ok = false; break; }
       tc_fence_after();
       // D1 = S~ W2^T (the critical product), then D3 = S~ Qe^T (the output's)
@@ -649,14 +679,16 @@ delta_chain_kernel(ScanArgs a, long long slots) {
       for (int ks = 0; ks < DK / 8; ++ks)
         mma_tf32_ts_warp(tD(s) + 64, tS + ks * 8, dq + (sw_kstep(128, ks) >> 4), idesc_a, ks > 0 ? 1u : 0u);
       mma_commit_warp(&sm.a3_done[s]);
+      mma_commit_warp(&sm.bq_empty[s]);
       if (!wait(&sm.u_ready, c & 1)) { ok = false; break; }
+      if (!wait(&sm.kd_full[s], (c >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
       // S~ += U^T Kd
       const uint64_t dkd = smem_desc_sw128(smem_u32(sm.kd[s]), 16, 1024);
 #pragma unroll
       for (int ks = 0; ks < kChunk / 8; ++ks)
         mma_tf32_ts_warp(tS, tU + ks * 8, dkd + (sw_kstep(DK, ks) >> 4), idesc_b, 1u);
-      mma_commit_warp(&sm.empty[s]);
+      mma_commit_warp(&sm.kd_empty[s]);
       issued = c + 1;
     }
     if (!ok && nc > 0 && lane == 0) sm.abort = 1;
@@ -714,9 +746,11 @@ delta_chain_kernel(ScanArgs a, long long slots) {
     prefetch_l2(1);
     float Gamma = 1.f;
     bool ok = true;
+    float gc_next = nc > 0 ? gc_of(0) : 1.f;
     auto step = [&](int c) -> bool {
       const int s = c & 1;
-      const float gc = gc_of(c);
+      const float gc = gc_next;
+      if (c + 1 < nc) gc_next = gc_of(c + 1);
       if (!mbar_wait(&sm.a1_done, c & 1, wd, a.status, kStatusTimeout) || sm.abort) return false;
       tc_fence_after();
       const float G0 = Gamma;
@@ -803,12 +837,14 @@ delta_chain_kernel(ScanArgs a, long long slots) {
     // every output warp takes the named barrier of every chunk, also after an
     // abort (work skipped, waits bounded), so that none waits on it forever
     bool dead = false;
+    float gc_next = nc > 0 ? gc_of(0) : 1.f;
     for (int c = 0; c < nc; ++c) {
       const int s = c & 1;
       const int n = min(kChunk, len - c * kChunk);
       uint16_t* stage = sm.ostage[c & 1];
+      const float gc = gc_next;
+      if (c + 1 < nc) gc_next = gc_of(c + 1);
       if (!dead) {
-        const float gc = gc_of(c);
         if (!mbar_wait(&sm.a3_done[s], (c >> 1) & 1, wd, a.status, kStatusTimeout) || sm.abort) {
           sm.abort = 1;
           dead = true;
@@ -836,14 +872,19 @@ delta_chain_kernel(ScanArgs a, long long slots) {
           }
         }
       }
+      // the previous chunk's row copies have read their stage: after the
+      // barrier every output thread may write the stage they read two chunks ago
+      if (lane == 0) bulk_wait_read_0();
+      fence_proxy_async_smem();
       asm volatile("bar.sync 2, 128;" ::: "memory");     // the four output warps
       if (!dead) {
-        const int per_row = dv / 8;                      // 16-byte pieces of a token row
-        const int q = (warp - 6) * 32 + lane;
-        for (int e = q; e < n * per_row; e += 128) {
-          const int j = e / per_row, p8 = e - j * per_row;
-          const uint4 v = *reinterpret_cast<const uint4*>(stage + j * dv + p8 * 8);
-          *reinterpret_cast<uint4*>(o + (static_cast<long long>(t_seq0 + c * kChunk + j) * a.hv + h) * dv + p8 * 8) = v;
+        // the token rows leave by the bulk-copy engine, one copy per row, each
+        // warp's lane 0 issuing every fourth row
+        if (lane == 0) {
+          for (int j = warp - 6; j < n; j += 4)
+            bulk_copy_s2g(o + (static_cast<long long>(t_seq0 + c * kChunk + j) * a.hv + h) * dv, stage + j * dv,
+                          static_cast<uint32_t>(dv) * 2u);
+          bulk_commit_group();
         }
         fetch(c + 1);
         if (c + 2 < nc) {
@@ -854,6 +895,7 @@ delta_chain_kernel(ScanArgs a, long long slots) {
         }
       }
     }
+    if (lane == 0) bulk_wait_0();          // the outputs are written before the CTA leaves
   }
   tc_fence_before();
   __syncthreads();
