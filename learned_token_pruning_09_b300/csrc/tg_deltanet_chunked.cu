@@ -206,8 +206,15 @@ delta_prep_kernel(ScanArgs a, long long slots) {
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
   uint32_t phase = 0;                       // of the MMA barrier
   bool ok = true;
+  // After a wait that runs out the same phase is waited for again with the
+  // drain limit, so that every MMA has completed before its operands are
+  // rewritten and the phases stay in step (the results are then flagged by
+  // the status word, not used).
   auto mma_wait = [&]() {
-    ok = mbar_wait(&sm.bar, phase & 1u, ok ? a.watchdog : kDrainCycles, a.status, kStatusTimeout) && ok;
+    if (!mbar_wait(&sm.bar, phase & 1u, ok ? a.watchdog : kDrainCycles, a.status, kStatusTimeout)) {
+      ok = false;
+      mbar_wait(&sm.bar, phase & 1u, kDrainCycles, a.status, kStatusTimeout);
+    }
     ++phase;
     tc_fence_after();
   };
@@ -662,7 +669,7 @@ delta_chain_kernel(ScanArgs a, long long slots) {
     const uint32_t idesc_a = idesc_tf32_f32(128, 64);
     const uint32_t idesc_b = idesc_tf32_f32(128, DK);
     bool ok = nc > 0 && wait(&sm.init_ready, 0);
-    int issued = 0;
+    bool any_mma = false;                    // an MMA was issued (then the final commit must cover it)
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c & 1;
       if (!wait(&sm.bq_full[s], (c >> 1) & 1)) { ok = false; break; }
@@ -671,6 +678,7 @@ delta_chain_kernel(ScanArgs a, long long slots) {
       // D1 = S~ W2^T (the critical product), then D3 = S~ Qe^T (the output's)
       const uint64_t dw = smem_desc_sw128(smem_u32(sm.bq[s]), 16, 1024);
       const uint64_t dq = smem_desc_sw128(smem_u32(sm.bq[s]) + 64 * 128, 16, 1024);
+      any_mma = true;
 #pragma unroll
       for (int ks = 0; ks < DK / 8; ++ks)
         mma_tf32_ts_warp(tD(s), tS + ks * 8, dw + (sw_kstep(128, ks) >> 4), idesc_a, ks > 0 ? 1u : 0u);
@@ -689,10 +697,9 @@ delta_chain_kernel(ScanArgs a, long long slots) {
       for (int ks = 0; ks < kChunk / 8; ++ks)
         mma_tf32_ts_warp(tS, tU + ks * 8, dkd + (sw_kstep(DK, ks) >> 4), idesc_b, 1u);
       mma_commit_warp(&sm.kd_empty[s]);
-      issued = c + 1;
     }
     if (!ok && nc > 0 && lane == 0) sm.abort = 1;
-    if (issued > 0 || nc == 0) {
+    if (any_mma || nc == 0) {
       // the final state (or, after an abort, the drain of the MMAs issued)
       mma_commit_warp(&sm.fin);
     } else if (lane == 0) {

@@ -82,3 +82,22 @@ def test_linear_wait_runs_out_then_recovers(tg):
     ref = oracle.bf16_decode(a) @ oracle.bf16_decode(w).T
     ok, err, _ = allclose_report(out, ref, 1e-2, 1e-2)
     assert ok, err
+
+
+def test_chunked_delta_scan_wait_runs_out_then_recovers(tg):
+    """Both kernels of the chunked scan: the per-chunk products wait for each
+    MMA past the limit and then for the same MMA with the drain limit; the
+    state carry's roles stop, drain their copies and MMAs and free TMEM."""
+    d = synth.deltanet_inputs("deltanet-tiny")
+    args = (dev_bf16(d["q"]), dev_bf16(d["k"]), dev_bf16(d["v"]), dev_f32(d["g"]), dev_f32(d["beta"]),
+            dev_i32(d["cu_kept"]))
+    tg.tg_check_device_status()
+    tg.tg_set_watchdog_cycles(200)
+    tg.tg_gated_delta_scan(*args, chunked=True)
+    assert tg.tg_check_device_status() == tg.TG_ERR_TIMEOUT
+    tg.tg_set_watchdog_cycles(0)
+    o = tg.tg_gated_delta_scan(*args, chunked=True)
+    assert tg.tg_check_device_status() == tg.TG_OK
+    ref, _ = oracle.gated_delta_scan(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_kept"])
+    ok, err, _ = allclose_report(host_f64(o), ref, 2e-4, 2.0 ** -8)
+    assert ok, err

@@ -170,3 +170,21 @@ def test_scan_chunked_edge_shapes(tg):
         ref_o, ref_s = oracle.gated_delta_scan(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_kept"],
                                                initial_state=s0.astype(np.float64))
         check(o, s, ref_o, ref_s, f"dk {dk} dv {dv} hv {hv}", True)
+
+
+def test_scan_chunked_many_sequences(tg):
+    """300 sequences of 0 to 200 tokens (the per-chunk kernel finds each
+    chunk's sequence by a binary search over cu_kept), against the oracle."""
+    rng = np.random.default_rng(300)
+    lens = rng.integers(0, 201, 300)
+    lens[::37] = 0
+    t, hk, hv, dk, dv = int(lens.sum()), 1, 2, 64, 32
+    d = {"q": synth.f32_to_bf16_bits(rng.standard_normal((t, hk, dk)).astype(np.float32)),
+         "k": synth.f32_to_bf16_bits(rng.standard_normal((t, hk, dk)).astype(np.float32)),
+         "v": synth.f32_to_bf16_bits(rng.standard_normal((t, hv, dv)).astype(np.float32)),
+         "g": (-np.exp(rng.uniform(np.log(0.005), np.log(0.5), (t, hv)))).astype(np.float32),
+         "beta": rng.uniform(0.05, 0.95, (t, hv)).astype(np.float32),
+         "cu_kept": np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)}
+    o, s = run_scan(tg, d, True)
+    ref_o, ref_s = oracle.gated_delta_scan(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_kept"])
+    check(o, s, ref_o, ref_s, "300 sequences", True)
