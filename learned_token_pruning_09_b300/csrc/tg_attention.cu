@@ -407,10 +407,12 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       const bool masked = __any_sync(0xffffffffu, sm.kmax[ms] > qpos);
       const int* kp = sm.kpos[ms];
       tmem_ld_wait();
+      // the max is taken on the raw scores (the scale is positive), and the
+      // scale and the max meet in one fused multiply-add per pair
       float2 x[kTileRows / 2];
 #pragma unroll
       for (int i = 0; i < kTileRows / 2; ++i)
-        x[i] = __fmul2_rn(make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), sl);
+        x[i] = make_float2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
       if (masked) {
 #pragma unroll
         for (int i = 0; i < kTileRows / 2; ++i) {
@@ -421,7 +423,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int i = 0; i < kTileRows / 2; ++i) mx[i & 3] = fmax3(mx[i & 3], x[i].x, x[i].y);
-      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], -INFINITY);
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], -INFINITY) * sl.x;
       const float m_new = (mt > m + kRescaleThreshold) ? mt : m;
       const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
       const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_use);
@@ -432,7 +434,7 @@ attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         uint32_t p16[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 y = __fadd2_rn(x[c * 16 + i], negm);
+          const float2 y = __ffma2_rn(x[c * 16 + i], sl, negm);
           const float p0 = ex2_approx(y.x);
           const float p1 = ex2_approx(y.y);
           if (i & 1) acc1 = __fadd2_rn(acc1, make_float2(p0, p1));
