@@ -141,6 +141,25 @@ def test_gather_invalid_id_inside_a_long_range(tg):
     np.testing.assert_array_equal(got[rows], ex[rows])
 
 
+def test_gather_positions_and_scores_only(tg):
+    """Without x (positions alone) and without x_kept (positions and scores):
+    no row is copied, and what is written is exact."""
+    shape = synth.custom("gather-pos", [3000, 17, 900], [5, 2, 0], [1000, 17, 64], d=64, seed=91)
+    x = synth.residuals(shape)
+    s = synth.score_draws(shape)
+    kept, cu_kept = oracle.topk_select(s, shape.cu_seqlens, shape.n_doc, shape.k)
+    _, epos, es = oracle.gather_kept(x, s, shape.cu_seqlens, kept, cu_kept)
+    cu, kd, ck = dev_i32(shape.cu_seqlens), dev_i32(kept), dev_i32(cu_kept)
+    _, pos, _ = tg.tg_gather_kept(None, None, cu, kd, ck, len(kept), d=64, want=("pos",))
+    assert tg.tg_check_device_status() == tg.TG_OK
+    np.testing.assert_array_equal(pos.cpu().numpy(), epos)
+    xk, pos2, sk = tg.tg_gather_kept(dev_bf16(x), dev_f32(s), cu, kd, ck, len(kept), want=("pos", "s"))
+    assert tg.tg_check_device_status() == tg.TG_OK
+    assert xk is None
+    np.testing.assert_array_equal(pos2.cpu().numpy(), epos)
+    np.testing.assert_array_equal(sk.cpu().numpy().view(np.uint32), es.view(np.uint32))
+
+
 def test_gather_rejects_out_of_sequence_index(tg):
     """A kept id outside its sequence is reported, not read."""
     cu = np.array([0, 10, 20], np.int32)

@@ -188,3 +188,15 @@ def test_scan_chunked_many_sequences(tg):
     o, s = run_scan(tg, d, True)
     ref_o, ref_s = oracle.gated_delta_scan(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_kept"])
     check(o, s, ref_o, ref_s, "300 sequences", True)
+
+
+@pytest.mark.parametrize("chunked", FORMS)
+def test_scan_without_final_state_gives_the_same_o(tg, chunked):
+    """o does not depend on whether the final state is asked for."""
+    d = synth.deltanet_inputs("deltanet-ragged")
+    args = (dev_bf16(d["q"]), dev_bf16(d["k"]), dev_bf16(d["v"]), dev_f32(d["g"]), dev_f32(d["beta"]),
+            dev_i32(d["cu_kept"]))
+    o1, _ = tg.tg_gated_delta_scan(*args, want_state=True, chunked=chunked)
+    o2 = tg.tg_gated_delta_scan(*args, chunked=chunked)
+    assert tg.tg_check_device_status() == tg.TG_OK
+    assert torch.equal(o1, o2)
