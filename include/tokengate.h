@@ -348,11 +348,17 @@ TG_API size_t tg_attention_bwd_workspace_size(int64_t n_kept, int32_t hq);
  *   final_state   [batch, hv, dv, dk] fp32 output, or NULL
  *   workspace     NULL, or tg_gated_delta_scan_workspace_size(...) bytes,
  *                 256-byte aligned: the chunked form on the tensor cores
- *                 (chunks of 64 tokens; per-chunk products in parallel, then
- *                 the state carried from chunk to chunk; tf32 MMAs on fp32
- *                 operands).  Needs dv <= 128; with a larger dv, or NULL,
- *                 the scan runs token by token on the CUDA cores (fp32) and
- *                 the workspace is not touched.
+ *                 (chunks of 64 tokens; per-chunk products in parallel, the
+ *                 state carried from chunk to chunk; tf32 MMAs on fp32
+ *                 operands).  With batch * hv up to half the SMs (and batch
+ *                 <= 96) both run in one cooperative launch, the state
+ *                 carries on some SMs consuming chunks as the others finish
+ *                 them; otherwise in two launches.  The results are the same
+ *                 bit for bit.  Contents on entry do not matter; the call
+ *                 overwrites them (one call at a time per workspace).  Needs
+ *                 dv <= 128; with a larger dv, or NULL, the scan runs token
+ *                 by token on the CUDA cores (fp32) and the workspace is not
+ *                 touched.
  * Every other pointer 16-byte aligned.  fp32 state and accumulation; o
  * rounded once to bf16.
  * Errors: a workspace smaller than the size -> TG_ERR_WORKSPACE.

@@ -565,6 +565,7 @@ tg_status tg_gated_delta_scan(const void* q, const void* k, const void* v, const
   a.final_state = final_state; a.status = di->status;
   a.ws = chunked ? workspace : nullptr;
   a.watchdog = g_watchdog_cycles;
+  a.num_sms = di->num_sms;
   const cudaError_t e = chunked ? launch_delta_scan_chunked(a, stream) : launch_delta_scan(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gated delta scan launch");
   return ok();

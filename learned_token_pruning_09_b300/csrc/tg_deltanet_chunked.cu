@@ -29,6 +29,8 @@
 //     the current one runs.
 // tf32 MMAs on fp32 operands rounded to nearest (cvt.rna) where they are
 // written; fp32 accumulation, fp32 state; o rounded once to bf16.
+#include <algorithm>
+
 #include "tg_common.cuh"
 
 namespace tg {
@@ -103,12 +105,40 @@ __host__ __device__ __forceinline__ uint32_t sw_kstep(int rows, int ks) {
   return static_cast<uint32_t>((ks >> 2) * rows * 128 + (ks & 3) * 32);
 }
 
+// Cross-CTA hand-off of a finished unit within one (cooperative) launch: the
+// writer group's stores, a barrier of the group, then one release store of
+// the unit's flag; readers poll the flag with acquire loads, a bounded wait.
+// The state carry reads part of the unit with the bulk-copy engine, so both
+// sides also fence the generic stores for the async proxy.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ bool flag_wait(const int* f, long long limit, unsigned int* status) {
+  if (ld_acquire_gpu(f) != 0) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(32);
+    if (ld_acquire_gpu(f) != 0) return true;
+    if (clock64() - t0 > limit) {
+      record_error(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // The workspace, per (chunk slot x, value head h), unit u = x * hv + h:
 //   bq  [u][128 rows][dk]  W2 (rows 0..63) and Qe (rows 64..127), swizzled image
 //   kd  [u][dk rows][64]   Kd^T = (exp(G_C - G_t) k^_t)^T, swizzled image
 //   w1  [u][64][dv]        W1 (token rows), plain fp32
 //   ol  [u][64][dv]        Oloc (token rows), plain fp32
 //   gc  [u]                gamma_C
+//   flag [u]               int, set once unit u is complete (fused launch only)
 // Chunk c of sequence b takes slot floor(cu[b] / 64) + b + c: distinct for
 // distinct (b, c), below n_kept / 64 + batch + 1.
 struct ChunkWs {
@@ -117,6 +147,7 @@ struct ChunkWs {
   float* w1;
   float* ol;
   float* gc;
+  int* flag;
 };
 __host__ __device__ inline long long chunk_slots(long long n_kept, int batch) { return n_kept / kChunk + batch + 1; }
 __host__ __device__ inline ChunkWs chunk_ws(void* base, long long slots, int hv, int dk, int dv) {
@@ -132,6 +163,8 @@ __host__ __device__ inline ChunkWs chunk_ws(void* base, long long slots, int hv,
   w.ol = reinterpret_cast<float*>(p);
   p += units * static_cast<long long>(dv) * kChunk * 4;
   w.gc = reinterpret_cast<float*>(p);
+  p += units * 4;
+  w.flag = reinterpret_cast<int*>(p);
   return w;
 }
 size_t delta_chunked_ws_bytes(long long n_kept, int batch, int hv, int dk, int dv) {
@@ -173,13 +206,17 @@ __device__ __forceinline__ void bf16x8(const uint4 u, float (&f)[8]) {
   }
 }
 
+// One (chunk slot x, value head h) unit of the per-chunk products, by a group
+// of 128 threads (tid 0..127, four whole warps aligned to a multiple of four)
+// that owns `sm`, the TMEM columns tmem .. tmem + 127, the mbarrier sm.bar
+// (its phase count in `phase`, carried from unit to unit) and the named
+// barriers bar_id (the group) and bar_id + 1 (its first two warps).  A slot
+// that holds no chunk returns at once (the same for the whole group).
 template <int DK>
-__global__ void __launch_bounds__(kPrepThreads)
-delta_prep_kernel(ScanArgs a, long long slots) {
-  extern __shared__ uint8_t smem_raw[];
-  PrepSmem<DK>& sm = *reinterpret_cast<PrepSmem<DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int x = blockIdx.x, h = blockIdx.y;
+__device__ __forceinline__ void delta_prep_unit(const ScanArgs& a, long long slots, int x, int h, PrepSmem<DK>& sm,
+                                             int tid, uint32_t tmem, uint32_t& phase, bool& ok, int bar_id) {
+  const int warp = tid >> 5, lane = tid & 31;
+  auto gbar = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory"); };
   // the sequence of this slot: the largest b with floor(cu[b] / 64) + b <= x
   int lo = 0, hi = a.batch - 1;
   while (lo < hi) {
@@ -204,8 +241,6 @@ delta_prep_kernel(ScanArgs a, long long slots) {
   float* kdT = ws.kd + u * DK * kChunk;
   const uint32_t bufa = smem_u32(sm.buf), at = smem_u32(sm.at), mq = smem_u32(sm.mq);
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  uint32_t phase = 0;                       // of the MMA barrier
-  bool ok = true;
   // After a wait that runs out the same phase is waited for again with the
   // drain limit, so that every MMA has completed before its operands are
   // rewritten and the phases stay in step (the results are then flagged by
@@ -228,15 +263,15 @@ delta_prep_kernel(ScanArgs a, long long slots) {
       const uint64_t db = smem_desc_sw128(b_addr, 16, 1024);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_tf32_ss_warp(sm.tmem_base + d_col, da + (sw_kstep(128, ks) >> 4), db + (sw_kstep(b_rows, ks) >> 4),
+        mma_tf32_ss_warp(tmem + d_col, da + (sw_kstep(128, ks) >> 4), db + (sw_kstep(b_rows, ks) >> 4),
                          idesc, (accumulate || ks > 0) ? 1u : 0u);
       mma_commit_warp(&sm.bar);
     }
   };
-  auto to_async = [&]() {                   // this thread's shared-memory writes, then the CTA
+  auto to_async = [&]() {                   // this thread's shared-memory writes, then the group
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    gbar();
   };
 
   // 0. cumulative log-decays and write strengths of the chunk
@@ -254,12 +289,9 @@ delta_prep_kernel(ScanArgs a, long long slots) {
     sm.gam[lane] = expf(g0); sm.gam[lane + 32] = expf(g1);
     sm.beta[lane] = b0; sm.beta[lane + 32] = b1;
   }
-  if (warp == 1) { tmem_alloc(&sm.tmem_base, 128); tmem_relinquish(); }
-  if (tid == 0) { mbar_init(&sm.bar, 1); fence_barrier_init(); }
   tc_fence_before();
-  __syncthreads();
+  gbar();
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
   const float GC = sm.G[kChunk - 1];      // padded tokens have g = 0
   const int t = tid & 63;
   const bool is_k = tid < kChunk;
@@ -286,7 +318,7 @@ delta_prep_kernel(ScanArgs a, long long slots) {
   //    of the rows into the buffer (tf32), with Kd^T and gamma q^ of those dims
   //    to the workspace, then its MMA
   for (int hf = 0; hf < DK / 64; ++hf) {
-    if (hf > 0) __syncthreads();            // every thread has read the previous half
+    if (hf > 0) gbar();                     // every thread has read the previous half
     const float rn = sm.rn[row];
     const float kdc = expf(GC - sm.G[t]);
 #pragma unroll 2
@@ -352,7 +384,7 @@ delta_prep_kernel(ScanArgs a, long long slots) {
     }
   }
   tc_fence_before();
-  __syncthreads();
+  gbar();
   // 4. T = (I + A)^-1 in 2 x 2 blocks of 32 (A strictly lower triangular):
   //    the diagonal blocks T11 = (I + A11)^-1 and T22 = (I + A22)^-1 by
   //    forward substitution, T_i = e_i - sum_{j<i} A_ij T_j (warps 0 and 1 at
@@ -402,7 +434,7 @@ delta_prep_kernel(ScanArgs a, long long slots) {
         ysc[i][k] = (s0 + s1) + (s2 + s3);
       }
     }
-    asm volatile("bar.sync 1, 64;" ::: "memory");     // Y and T22 in the scratch; A is read
+    asm volatile("bar.sync %0, 64;" ::"r"(bar_id + 1) : "memory");   // Y and T22 in the scratch; A is read
     if (warp == 0) {
       // T21 = -Y T11 (column k of T11 in registers) and T11 into the T tile
 #pragma unroll 1
@@ -430,7 +462,7 @@ delta_prep_kernel(ScanArgs a, long long slots) {
     }
   }
   tc_fence_before();
-  __syncthreads();
+  gbar();
   // 5. W1^T = (beta v)^T T^T (TMEM 64..127), then W2^T = (beta gamma k^)^T T^T
   //    (TMEM 0..63), each right-hand side through the buffer, column t from
   //    the rows re-read from L1/L2
@@ -541,9 +573,28 @@ delta_prep_kernel(ScanArgs a, long long slots) {
     }
     if (tid == 0) ws.gc[u] = expf(GC);
   }
+  fence_proxy_async_global();               // the bq and kd images are read by bulk copies
+  tc_fence_before();
+  gbar();
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kPrepThreads)
+delta_prep_kernel(ScanArgs a, long long slots) {
+  extern __shared__ uint8_t smem_raw[];
+  PrepSmem<DK>& sm = *reinterpret_cast<PrepSmem<DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 1) { tmem_alloc(&sm.tmem_base, 128); tmem_relinquish(); }
+  if (tid == 0) { mbar_init(&sm.bar, 1); fence_barrier_init(); }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 128);
+  tc_fence_after();
+  uint32_t phase = 0;
+  bool ok = true;
+  delta_prep_unit<DK>(a, slots, blockIdx.x, blockIdx.y, sm, tid, sm.tmem_base, phase, ok, 1);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(sm.tmem_base, 128);
 }
 
 // ---------------------------------------------------------------------------
@@ -582,13 +633,14 @@ struct ChainSmem {
 
 constexpr int kChainThreads2 = 320;   // warps 0-3 state, 4 copies, 5 MMA issue, 6-9 output
 
+// The state carry of sequence b, value head h, by a whole CTA (warps 0..9;
+// any further warps only take the CTA barriers).  With `fused` the per-chunk
+// products are computed by other CTAs of the same launch, and every read of a
+// unit waits for its flag.
 template <int DK>
-__global__ void __launch_bounds__(kChainThreads2, 1)
-delta_chain_kernel(ScanArgs a, long long slots) {
-  extern __shared__ uint8_t smem_raw[];
-  ChainSmem<DK>& sm = *reinterpret_cast<ChainSmem<DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__device__ __forceinline__ void delta_chain_cta(const ScanArgs& a, long long slots, int b, int h, ChainSmem<DK>& sm,
+                                                bool fused) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x, h = blockIdx.y;
   const int dv = a.dv;
   const int t_seq0 = __ldg(a.cu_kept + b), t_seq1 = __ldg(a.cu_kept + b + 1);
   const int len = t_seq1 - t_seq0;
@@ -601,6 +653,14 @@ delta_chain_kernel(ScanArgs a, long long slots) {
   const ChunkWs ws = chunk_ws(a.ws, slots, a.hv, DK, dv);
   const long long wd = a.watchdog;
   constexpr uint32_t kBqBytes = 128 * DK * 4, kKdBytes = DK * kChunk * 4;
+  // chunk c's unit is complete: by one thread (the copy issuer) or, with
+  // warp_all, by a whole warp, each lane with its own acquire, the result
+  // the same in every lane
+  auto ready = [&](int c, bool warp_all) -> bool {
+    if (!fused) return true;
+    const bool r = flag_wait(ws.flag + (slot0 + c) * a.hv + h, wd, a.status);
+    return warp_all ? __all_sync(0xffffffffu, r) : r;
+  };
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -639,6 +699,11 @@ delta_chain_kernel(ScanArgs a, long long slots) {
       for (int c = 0; c < nc && !sm.abort; ++c) {
         const int s = c & 1;
         const long long u = (slot0 + c) * a.hv + h;
+        if (!ready(c, false)) {
+          sm.abort = 1;
+          break;
+        }
+        if (fused) fence_proxy_async_global();
         if (c >= 2 && !mbar_wait(&sm.bq_empty[s], ((c >> 1) - 1) & 1, wd, a.status, kStatusTimeout)) {
           sm.abort = 1;
           break;
@@ -749,15 +814,17 @@ delta_chain_kernel(ScanArgs a, long long slots) {
     };
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) w[j] = 0.f;
-    fetch(0);
-    prefetch_l2(1);
     float Gamma = 1.f;
-    bool ok = true;
-    float gc_next = nc > 0 ? gc_of(0) : 1.f;
+    bool ok = nc == 0 || ready(0, true);
+    float gc_next = 1.f;
+    if (ok && nc > 0) {
+      fetch(0);
+      gc_next = gc_of(0);
+    }
+    prefetch_l2(1);
     auto step = [&](int c) -> bool {
       const int s = c & 1;
       const float gc = gc_next;
-      if (c + 1 < nc) gc_next = gc_of(c + 1);
       if (!mbar_wait(&sm.a1_done, c & 1, wd, a.status, kStatusTimeout) || sm.abort) return false;
       tc_fence_after();
       const float G0 = Gamma;
@@ -797,7 +864,11 @@ delta_chain_kernel(ScanArgs a, long long slots) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.u_ready);
-      fetch(c + 1);                          // the registers take the next chunk's row
+      if (c + 1 < nc) {                      // the registers take the next chunk's row
+        if (!ready(c + 1, true)) return false;
+        fetch(c + 1);
+        gc_next = gc_of(c + 1);
+      }
       prefetch_l2(c + 2);
       return true;
     };
@@ -822,7 +893,7 @@ delta_chain_kernel(ScanArgs a, long long slots) {
         }
       }
     }
-  } else {
+  } else if (warp < 10) {
     // ---------------- outputs (warps 6..9): O = Gamma D3 + Oloc ----------------
     const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
     const int r = q4 * 32 + lane;
@@ -840,17 +911,20 @@ delta_chain_kernel(ScanArgs a, long long slots) {
     };
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) ol[j] = 0.f;
-    fetch(0);
     // every output warp takes the named barrier of every chunk, also after an
     // abort (work skipped, waits bounded), so that none waits on it forever
-    bool dead = false;
-    float gc_next = nc > 0 ? gc_of(0) : 1.f;
+    bool dead = nc > 0 && !ready(0, true);
+    if (dead) sm.abort = 1;
+    float gc_next = 1.f;
+    if (!dead && nc > 0) {
+      fetch(0);
+      gc_next = gc_of(0);
+    }
     for (int c = 0; c < nc; ++c) {
       const int s = c & 1;
       const int n = min(kChunk, len - c * kChunk);
       uint16_t* stage = sm.ostage[c & 1];
       const float gc = gc_next;
-      if (c + 1 < nc) gc_next = gc_of(c + 1);
       if (!dead) {
         if (!mbar_wait(&sm.a3_done[s], (c >> 1) & 1, wd, a.status, kStatusTimeout) || sm.abort) {
           sm.abort = 1;
@@ -893,8 +967,16 @@ delta_chain_kernel(ScanArgs a, long long slots) {
                           static_cast<uint32_t>(dv) * 2u);
           bulk_commit_group();
         }
-        fetch(c + 1);
-        if (c + 2 < nc) {
+        if (c + 1 < nc) {
+          if (ready(c + 1, true)) {
+            fetch(c + 1);
+            gc_next = gc_of(c + 1);
+          } else {
+            sm.abort = 1;
+            dead = true;
+          }
+        }
+        if (!dead && c + 2 < nc) {
           const char* base = reinterpret_cast<const char*>(ol_unit(c + 2));
           const int lines = kChunk * dv * 4 / 128;
           for (int l = (warp - 6) * 32 + lane; l < lines; l += 128)
@@ -910,6 +992,123 @@ delta_chain_kernel(ScanArgs a, long long slots) {
 }
 
 template <int DK>
+__global__ void __launch_bounds__(kChainThreads2, 1)
+delta_chain_kernel(ScanArgs a, long long slots) {
+  extern __shared__ uint8_t smem_raw[];
+  ChainSmem<DK>& sm = *reinterpret_cast<ChainSmem<DK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  delta_chain_cta<DK>(a, slots, blockIdx.x, blockIdx.y, sm, false);
+}
+
+// ---------------------------------------------------------------------------
+// both in one launch
+// ---------------------------------------------------------------------------
+constexpr int kFusedMaxBatch = 96;
+constexpr long long kStaggerCycles = 235;   // per key dim: about a third of a unit's duration
+
+// The chunks in the order (chunk index c within its sequence, then sequence
+// b), the order in which the state carries of all sequences reach them.  Held
+// by a whole warp (batch <= 96): lane keeps the start and the chunk count of
+// sequences lane, lane + 32 and lane + 64.
+struct ChunkOrder {
+  int cu[3], nc[3];
+  int max_nc;
+  __device__ __forceinline__ void init(const ScanArgs& a, int lane) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int b = lane + 32 * i;
+      cu[i] = 0;
+      nc[i] = 0;
+      if (b < a.batch) {
+        cu[i] = __ldg(a.cu_kept + b);
+        const int len = __ldg(a.cu_kept + b + 1) - cu[i];
+        nc[i] = len > 0 ? (len + kChunk - 1) / kChunk : 0;
+      }
+    }
+    max_nc = __reduce_max_sync(0xffffffffu, max(nc[0], max(nc[1], nc[2])));
+  }
+  // the chunks ahead of chunk index c: the sum over b of min(nc_b, c)
+  __device__ __forceinline__ long long ahead(int c) const {
+    return static_cast<long long>(__reduce_add_sync(0xffffffffu, min(nc[0], c) + min(nc[1], c) + min(nc[2], c)));
+  }
+  // the slot of the q-th chunk, -1 past the last one
+  __device__ __forceinline__ int slot(long long q) const {
+    if (q >= ahead(max_nc)) return -1;
+    int lo = 0, hi = max_nc;                // ahead(lo) <= q < ahead(hi)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ahead(mid) <= q) lo = mid; else hi = mid;
+    }
+    int j = static_cast<int>(q - ahead(lo));   // the j-th sequence with more than lo chunks
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      unsigned m = __ballot_sync(0xffffffffu, nc[i] > lo);
+      const int cnt = __popc(m);
+      if (j < cnt) {
+        for (int t = 0; t < j; ++t) m &= m - 1;
+        const int l = __ffs(m) - 1;
+        const int b = 32 * i + l;
+        return __shfl_sync(0xffffffffu, cu[i], l) / kChunk + b + lo;
+      }
+      j -= cnt;
+    }
+    return -1;
+  }
+};
+
+// The state carry of a sequence walks its chunks one after another on one SM
+// while the per-chunk products have no order among them, so one cooperative
+// launch (every CTA resident, so that a CTA may wait for another) runs both
+// side by side: CTAs 0 .. batch * hv - 1 carry the states, the others compute
+// the units chunk index by chunk index (the order the chains consume them),
+// three groups of four warps per CTA, each group with its own shared-memory
+// share and 128 TMEM columns, and publish each finished unit by its flag.
+constexpr int kFusedThreads = 384;
+
+template <int DK>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+delta_fused_kernel(ScanArgs a, long long slots, int n_chain) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int cta = static_cast<int>(blockIdx.x);
+  if (cta < n_chain) {
+    delta_chain_cta<DK>(a, slots, cta / a.hv, cta % a.hv, *reinterpret_cast<ChainSmem<DK>*>(base), true);
+    return;
+  }
+  PrepSmem<DK>* psm = reinterpret_cast<PrepSmem<DK>*>(base);
+  const int tid = threadIdx.x, warp = tid >> 5, grp = warp >> 2, gtid = tid & 127;
+  if (warp == 0) { tmem_alloc(&psm[0].tmem_base, 512); tmem_relinquish(); }
+  if (gtid == 0) { mbar_init(&psm[grp].bar, 1); fence_barrier_init(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = psm[0].tmem_base + static_cast<uint32_t>(grp) * 128u;
+  const ChunkWs ws = chunk_ws(a.ws, slots, a.hv, DK, a.dv);
+  const int n_prep = static_cast<int>(gridDim.x) - n_chain;
+  const long long units = slots * a.hv;
+  uint32_t phase = 0;
+  bool ok = true;
+  ChunkOrder order;
+  order.init(a, tid & 31);
+  // the three groups of a CTA start a third of a unit apart, so that their
+  // load, barrier and MMA phases interleave instead of coinciding
+  if (grp > 0) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < grp * kStaggerCycles * DK) __nanosleep(200);
+  }
+  for (long long k = static_cast<long long>(grp) * n_prep + (cta - n_chain); k < units; k += 3LL * n_prep) {
+    const int x = order.slot(k / a.hv);                        // the same in every warp
+    if (x < 0) break;                                          // and so are later k
+    const int h = static_cast<int>(k % a.hv);
+    delta_prep_unit<DK>(a, slots, x, h, psm[grp], gtid, tmem, phase, ok, 1 + 2 * grp);
+    // the unit ends with a barrier of the group after every thread's stores
+    if (gtid == 0) st_release_gpu(ws.flag + static_cast<long long>(x) * a.hv + h, 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(psm[0].tmem_base, 512);
+}
+
+template <int DK>
 static cudaError_t launch_chunked_dk(const ScanArgs& a, cudaStream_t st) {
   const long long slots = chunk_slots(a.n_kept, a.batch);
   const size_t prep_smem = sizeof(PrepSmem<DK>) + 1024;
@@ -920,6 +1119,29 @@ static cudaError_t launch_chunked_dk(const ScanArgs& a, cudaStream_t st) {
   e = cudaFuncSetAttribute(delta_chain_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(chain_smem));
   if (e != cudaSuccess) return e;
+  const long long n_chain = static_cast<long long>(a.batch) * a.hv;
+  const long long units = slots * a.hv;
+  if (a.n_kept > 0 && n_chain <= a.num_sms / 2 && a.batch <= kFusedMaxBatch) {
+    // one launch: a CTA per SM, the chains on the first, units on the rest
+    const size_t fused_smem = std::max(sizeof(ChainSmem<DK>), 3 * sizeof(PrepSmem<DK>)) + 1024;
+    e = cudaFuncSetAttribute(delta_fused_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(fused_smem));
+    if (e != cudaSuccess) return e;
+    const long long n_prep = std::min<long long>(a.num_sms - n_chain, (units + 2) / 3);
+    e = cudaMemsetAsync(chunk_ws(a.ws, slots, a.hv, DK, a.dv).flag, 0, static_cast<size_t>(units) * sizeof(int), st);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_chain + n_prep));
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = fused_smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, delta_fused_kernel<DK>, a, slots, static_cast<int>(n_chain));
+  }
   if (a.n_kept > 0) {
     delta_prep_kernel<DK><<<dim3(static_cast<unsigned>(slots), static_cast<unsigned>(a.hv)), kPrepThreads, prep_smem,
                             st>>>(a, slots);

@@ -186,6 +186,7 @@ struct ScanArgs {
   unsigned int* status;
   void* ws;                   // chunked form: per-chunk products (delta_chunked_ws_bytes), or null
   long long watchdog;
+  int num_sms;
 };
 cudaError_t launch_delta_scan(const ScanArgs& a, cudaStream_t st);
 // chunked form on the tensor cores (dk 64 or 128, dv <= 128), with a workspace

@@ -200,3 +200,24 @@ def test_scan_without_final_state_gives_the_same_o(tg, chunked):
     o2 = tg.tg_gated_delta_scan(*args, chunked=chunked)
     assert tg.tg_check_device_status() == tg.TG_OK
     assert torch.equal(o1, o2)
+
+
+def test_scan_one_launch_and_two_launches_agree(tg):
+    """With few (sequence, head) pairs the chunked form runs as one
+    cooperative launch, the per-chunk products on some SMs and the state carry
+    on others, handing chunks over by flags; with many it runs two launches.
+    The arithmetic is the same, so the same chunks padded with empty
+    sequences (enough pairs for the two-launch form on any GPU up to 320 SMs)
+    give bit-identical outputs: a hand-off that let the state carry read a
+    unit before it was complete would show here."""
+    d = synth.deltanet_inputs("deltanet-ragged")
+    hv = d["v"].shape[1]
+    one = run_scan(tg, d, True)
+    padded = dict(d)
+    n_empty = 160 // hv + 1
+    padded["cu_kept"] = np.concatenate([d["cu_kept"], np.full(n_empty, d["cu_kept"][-1])]).astype(np.int32)
+    two = run_scan(tg, padded, True)
+    nb = len(d["cu_kept"]) - 1
+    assert np.array_equal(one[0], two[0])
+    assert np.array_equal(one[1], two[1][:nb])
+    assert not np.any(two[1][nb:])                # empty sequences keep the zero state
