@@ -233,7 +233,7 @@ def measure_deltanet(dev, flush, steps, peaks, name="deltanet-32k-k4096"):
     us_token = timed(False)
     byts = deltanet_bytes(t, cfg["hk"], cfg["hv"], cfg["dk"], cfg["dv"])
     return {"workload": name, "tokens": t, "hk": cfg["hk"], "hv": cfg["hv"], "dk": cfg["dk"], "dv": cfg["dv"],
-            "form": "chunked (tf32 tensor cores, workspace)", "us": us, "gbs": byts / (us * 1e-6) / 1e9,
+            "form": "chunked (tf32 tensor cores, workspace); per-chunk products and state carry in one cooperative launch when batch x hv <= SMs / 2", "us": us, "gbs": byts / (us * 1e-6) / 1e9,
             "bytes": byts, "frac_of_measured_hbm": byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
             "workspace_bytes": int(ws.numel()), "token_by_token_us": us_token}
 
