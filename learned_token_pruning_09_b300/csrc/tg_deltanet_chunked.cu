@@ -1140,7 +1140,11 @@ static cudaError_t launch_chunked_dk(const ScanArgs& a, cudaStream_t st) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, delta_fused_kernel<DK>, a, slots, static_cast<int>(n_chain));
+    e = cudaLaunchKernelEx(&cfg, delta_fused_kernel<DK>, a, slots, static_cast<int>(n_chain));
+    // a device that cannot hold the grid at once (part of its SMs unavailable)
+    // runs the same work as two launches below
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    (void)cudaGetLastError();
   }
   if (a.n_kept > 0) {
     delta_prep_kernel<DK><<<dim3(static_cast<unsigned>(slots), static_cast<unsigned>(a.hv)), kPrepThreads, prep_smem,
