@@ -844,36 +844,63 @@ def run_gpu(args, shape):
     deltanet = measure_deltanet(dev, flush, args.steps, peaks)
 
     # ---- end to end through the public API, host buffers ----
+    # Every step copies its inputs from pinned host memory and reads its
+    # result back, all inside the timed region.  The next step's inputs travel
+    # on a copy stream into a second set of device buffers while this step
+    # computes (two input buffer sets, ordered by events); the result's
+    # read-back stays on the compute stream, behind the step.
     import torch as _t
     x_h = _t.from_numpy(np.ascontiguousarray(inputs["x"]).view(np.int16)).view(_t.bfloat16).pin_memory()
-    h2d_list = [(P.X, x_h)]
+    inputs_2 = [(lambda b: setattr(P, "X", b), [P.X, _t.empty_like(P.X)], x_h)]
     if not shape.with_proj:
-        for dst, key in ((P.q, "q"), (P.k, "k"), (P.layers[0]["v"], "v")):
-            h2d_list.append((dst, _t.from_numpy(np.ascontiguousarray(inputs["ai"][key]).view(np.int16))
-                             .view(_t.bfloat16).pin_memory()))
+        def v_setter(b):
+            P.layers[0]["v"] = b
+        for dst, key, setter in ((P.q, "q", lambda b: setattr(P, "q", b)), (P.k, "k", lambda b: setattr(P, "k", b)),
+                                 (P.layers[0]["v"], "v", v_setter)):
+            host = _t.from_numpy(np.ascontiguousarray(inputs["ai"][key]).view(np.int16)).view(_t.bfloat16).pin_memory()
+            inputs_2.append((setter, [dst, _t.empty_like(dst)], host))
     out_dev = P.xk if shape.with_proj else P.o
     out_h = _t.empty(out_dev.shape, dtype=_t.bfloat16).pin_memory()
     kept_h = _t.empty(P.T, dtype=_t.int32).pin_memory()
-    h2d = sum(h.numel() * h.element_size() for _, h in h2d_list)
+    h2d = sum(h.numel() * h.element_size() for _, _, h in inputs_2)
     d2h = out_h.numel() * 2 + kept_h.numel() * 4
+    copy_stream = _t.cuda.Stream()
+    ev_in = [_t.cuda.Event(), _t.cuda.Event()]       # buffer set landed
+    ev_free = [_t.cuda.Event(), _t.cuda.Event()]     # the step that read buffer set is done
 
-    def e2e_step():
-        for dst, h in h2d_list:
-            dst.copy_(h, non_blocking=True)
-        for _, f in segs:
-            f()
-        out_h.copy_(out_dev, non_blocking=True)
-        kept_h.copy_(P.kept, non_blocking=True)
+    def h2d_into(b):
+        with _t.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_free[b])
+            for _, bufs, host in inputs_2:
+                bufs[b].copy_(host, non_blocking=True)
+            ev_in[b].record(copy_stream)
 
-    e2e_step()
+    def e2e_run(n):
+        h2d_into(0)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                h2d_into(b ^ 1)
+            stream.wait_event(ev_in[b])
+            for setter, bufs, _ in inputs_2:
+                setter(bufs[b])
+            for _, f in segs:
+                f()
+            ev_free[b].record(stream)
+            out_h.copy_(out_dev, non_blocking=True)
+            kept_h.copy_(P.kept, non_blocking=True)
+
+    e2e_run(2)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 10))
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    copy_stream.wait_event(e0)                  # no copy starts before the timed region
+    e2e_run(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
+    for setter, bufs, _ in inputs_2:
+        setter(bufs[0])
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms, = max_over_ranks([e2e_ms], dev)
     e2e_val = whole_job_tflops(flops_layer * nl, world, e2e_ms)
@@ -931,7 +958,9 @@ def run_gpu(args, shape):
                          "frac_of_sustained": kern_tflops / peaks["bf16_tflops_sustained"]
                          if peaks.get("bf16_tflops_sustained") else None},
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
+                    "ms_per_step": e2e_ms,
+                    "overlap": "each step's host-to-device copy runs on a copy stream into one of two device "
+                               "input buffers while the previous step computes; read-back after each step"},
             "gpu_launches": P.launches_per_step() * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
