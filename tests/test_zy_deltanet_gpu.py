@@ -221,3 +221,48 @@ def test_scan_one_launch_and_two_launches_agree(tg):
     assert np.array_equal(one[0], two[0])
     assert np.array_equal(one[1], two[1][:nb])
     assert not np.any(two[1][nb:])                # empty sequences keep the zero state
+
+
+def _random_scan_inputs(rng, lens, hk, hv, dk, dv):
+    t = int(sum(lens))
+    return {"q": synth.f32_to_bf16_bits(rng.standard_normal((t, hk, dk)).astype(np.float32)),
+            "k": synth.f32_to_bf16_bits(rng.standard_normal((t, hk, dk)).astype(np.float32)),
+            "v": synth.f32_to_bf16_bits(rng.standard_normal((t, hv, dv)).astype(np.float32)),
+            "g": (-np.exp(rng.uniform(np.log(0.005), np.log(0.5), (t, hv)))).astype(np.float32),
+            "beta": rng.uniform(0.05, 0.95, (t, hv)).astype(np.float32),
+            "cu_kept": np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)}
+
+
+@pytest.mark.parametrize("extra", [0, 1])
+def test_scan_chunked_at_the_one_launch_threshold(tg, extra):
+    """batch * hv equal to half the SMs (the largest one-launch shape) and one
+    sequence more (two launches), against the oracle."""
+    half = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    hv, hk, dk, dv = 2, 1, 64, 32
+    batch = half // hv + extra
+    rng = np.random.default_rng(half + extra)
+    lens = rng.integers(1, 140, batch)
+    d = _random_scan_inputs(rng, lens, hk, hv, dk, dv)
+    o, s = run_scan(tg, d, True)
+    ref_o, ref_s = oracle.gated_delta_scan(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_kept"])
+    check(o, s, ref_o, ref_s, f"batch {batch} x hv {hv} (SMs / 2 = {half})", True)
+
+
+def test_scan_chunked_workspace_contents_do_not_matter(tg):
+    """The same workspace used twice, then filled with 0xFF bytes (every flag
+    and every operand set to garbage): the outputs are the same bits each
+    time."""
+    d = synth.deltanet_inputs("deltanet-ragged")
+    args = (dev_bf16(d["q"]), dev_bf16(d["k"]), dev_bf16(d["v"]), dev_f32(d["g"]), dev_f32(d["beta"]),
+            dev_i32(d["cu_kept"]))
+    t, hv, dv = d["v"].shape
+    dk = d["q"].shape[2]
+    nb = len(d["cu_kept"]) - 1
+    ws = torch.zeros(tg.tg_gated_delta_scan_workspace_size(t, nb, hv, dk, dv), dtype=torch.uint8, device="cuda")
+    o1, s1 = tg.tg_gated_delta_scan(*args, want_state=True, workspace=ws)
+    o2, s2 = tg.tg_gated_delta_scan(*args, want_state=True, workspace=ws)
+    ws.fill_(0xFF)
+    o3, s3 = tg.tg_gated_delta_scan(*args, want_state=True, workspace=ws)
+    assert tg.tg_check_device_status() == tg.TG_OK
+    assert torch.equal(o1, o2) and torch.equal(o1, o3)
+    assert torch.equal(s1, s2) and torch.equal(s1, s3)
