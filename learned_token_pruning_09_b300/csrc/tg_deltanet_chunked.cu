@@ -1098,6 +1098,9 @@ delta_fused_kernel(ScanArgs a, long long slots, int n_chain) {
   for (long long k = static_cast<long long>(grp) * n_prep + (cta - n_chain); k < units; k += 3LL * n_prep) {
     const int x = order.slot(k / a.hv);                        // the same in every warp
     if (x < 0) break;                                          // and so are later k
+    // a sequence outside the tokens (flagged by its state carry) can give a
+    // slot past the workspace; no unit and no flag for it
+    if (x >= slots) continue;
     const int h = static_cast<int>(k % a.hv);
     delta_prep_unit<DK>(a, slots, x, h, psm[grp], gtid, tmem, phase, ok, 1 + 2 * grp);
     // the unit ends with a barrier of the group after every thread's stores

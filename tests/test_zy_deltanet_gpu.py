@@ -140,11 +140,17 @@ def test_scan_pruned_tokens_are_skipped(tg, chunked):
 
 
 @pytest.mark.parametrize("chunked", FORMS)
-def test_scan_rejects_bad_sequences(tg, chunked):
-    """cu_kept past n_kept is flagged on the device and nothing is read."""
+@pytest.mark.parametrize("cu", ["end+5", "far"])
+def test_scan_rejects_bad_sequences(tg, chunked, cu):
+    """cu_kept past n_kept is flagged on the device and nothing is read or
+    written outside the buffers: a sequence ending 5 tokens past the last
+    one, and two sequences far past it (whose chunk slots lie beyond the
+    workspace's)."""
     d = synth.deltanet_inputs("deltanet-tiny")
     bad = dict(d)
-    bad["cu_kept"] = np.array([0, len(d["g"]) + 5], np.int32)
+    n = len(d["g"])
+    bad["cu_kept"] = (np.array([0, n + 5], np.int32) if cu == "end+5"
+                      else np.array([0, 5000, 5100], np.int32))
     tg.tg_check_device_status()
     tg.tg_gated_delta_scan(dev_bf16(bad["q"]), dev_bf16(bad["k"]), dev_bf16(bad["v"]), dev_f32(bad["g"]),
                            dev_f32(bad["beta"]), dev_i32(bad["cu_kept"]), chunked=chunked)
