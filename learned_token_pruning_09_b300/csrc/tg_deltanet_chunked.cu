@@ -14,19 +14,23 @@
 //   S  = gamma_C S0 + U^T (exp(G_C - G) k^)
 // which is the recurrence token by token, regrouped (the WY form).
 //
-// Two kernels:
-//   delta_prep_kernel, one CTA per (chunk, value head), all chunks in
+// Two parts:
+//   the per-chunk products, one unit per (chunk, value head), all in
 //     parallel: Gram products [k^; q^] k^^T (tf32 MMA), T by forward
 //     substitution, W1^T, W2^T (tf32 MMA), Qe, Oloc^T (tf32 MMA); written to
-//     the workspace, the state-carry kernel's MMA operands as ready shared-
-//     memory images (128-byte swizzle, K-major);
-//   delta_chain_kernel, one CTA per (sequence, value head): the state S lives
+//     the workspace, the state carry's MMA operands as ready shared-memory
+//     images (128-byte swizzle, K-major);
+//   the state carry, one CTA per (sequence, value head): the state S lives
 //     in tensor memory (lane = value row, column = key dim) and is the A
 //     operand of both MMAs of a chunk:
 //       D = S [W2; Qe]^T          (U = W1 - D1 and O = D3 + Oloc)
 //       S = gamma_C S + U^T Kd    (U^T back in tensor memory as the A operand)
 //     with the next chunk's operands copied in by the bulk-copy engine while
 //     the current one runs.
+// With few (sequence, head) pairs both run in one cooperative launch
+// (delta_fused_kernel: the carries on some SMs, units on the others, handed
+// over by flags); otherwise as two launches (delta_prep_kernel, one CTA per
+// unit, then delta_chain_kernel).  The arithmetic is the same either way.
 // tf32 MMAs on fp32 operands rounded to nearest (cvt.rna) where they are
 // written; fp32 accumulation, fp32 state; o rounded once to bf16.
 #include <algorithm>
