@@ -180,10 +180,11 @@ size_t delta_chunked_ws_bytes(long long n_kept, int batch, int hv, int dk, int d
 // ---------------------------------------------------------------------------
 // per-chunk products
 // ---------------------------------------------------------------------------
-// The kernel is written for a small instruction footprint (rolled loops over
+// A unit is written for a small instruction footprint (rolled loops over
 // 16-byte pieces and 16-column TMEM tiles, rows re-read from L1/L2 rather than
 // held in registers) and a small shared-memory and TMEM share, so that three
-// CTAs fit an SM and hide one another's latencies: every MMA operand passes
+// units (three CTAs, or three groups of one CTA) fit an SM and hide one
+// another's latencies: every MMA operand passes
 // through one 32 KB buffer (the Gram product in 64-wide halves of the key
 // dims, then the four other products one after another), and the
 // accumulators use 128 TMEM columns.
