@@ -142,7 +142,9 @@ __device__ __forceinline__ bool flag_wait(const int* f, long long limit, unsigne
 //   w1  [u][64][dv]        W1 (token rows), plain fp32
 //   ol  [u][64][dv]        Oloc (token rows), plain fp32
 //   gc  [u]                gamma_C
-//   flag [u]               int, set once unit u is complete (fused launch only)
+//   flag [u]               int, set once unit u is complete (one-launch form only),
+//                          then a 64-bit count of the units handed out
+// (gc, the flags and the counter fit the 16 bytes per unit added to the size)
 // Chunk c of sequence b takes slot floor(cu[b] / 64) + b + c: distinct for
 // distinct (b, c), below n_kept / 64 + batch + 1.
 struct ChunkWs {
@@ -199,6 +201,7 @@ struct PrepSmem {
   float rn[128];                            // 1 / |k_t| (rows 0..63), scale / |q_t| (64..127)
   uint64_t bar;
   uint32_t tmem_base;
+  long long next_unit;                      // one-launch form: the group's next unit, from its thread 0
 };
 
 // 8 bf16 (one 16-byte piece) to fp32
@@ -1017,6 +1020,7 @@ constexpr long long kStaggerCycles = 235;   // per key dim: about a third of a u
 struct ChunkOrder {
   int cu[3], nc[3];
   int max_nc;
+  bool single;                              // one sequence: its chunks in order, no search
   __device__ __forceinline__ void init(const ScanArgs& a, int lane) {
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
@@ -1030,6 +1034,11 @@ struct ChunkOrder {
       }
     }
     max_nc = __reduce_max_sync(0xffffffffu, max(nc[0], max(nc[1], nc[2])));
+    single = a.batch == 1;
+    if (single) {                           // every lane holds sequence 0's start and count
+      cu[0] = __shfl_sync(0xffffffffu, cu[0], 0);
+      nc[0] = __shfl_sync(0xffffffffu, nc[0], 0);
+    }
   }
   // the chunks ahead of chunk index c: the sum over b of min(nc_b, c)
   __device__ __forceinline__ long long ahead(int c) const {
@@ -1037,6 +1046,7 @@ struct ChunkOrder {
   }
   // the slot of the q-th chunk, -1 past the last one
   __device__ __forceinline__ int slot(long long q) const {
+    if (single) return q < nc[0] ? cu[0] / kChunk + static_cast<int>(q) : -1;
     if (q >= ahead(max_nc)) return -1;
     int lo = 0, hi = max_nc;                // ahead(lo) <= q < ahead(hi)
     while (hi - lo > 1) {
@@ -1067,6 +1077,8 @@ struct ChunkOrder {
 // the units chunk index by chunk index (the order the chains consume them),
 // three groups of four warps per CTA, each group with its own shared-memory
 // share and 128 TMEM columns, and publish each finished unit by its flag.
+// A group takes its next unit from a counter in the workspace (cleared with
+// the flags), so that groups that started later take fewer units.
 constexpr int kFusedThreads = 384;
 
 template <int DK>
@@ -1088,7 +1100,6 @@ delta_fused_kernel(ScanArgs a, long long slots, int n_chain) {
   tc_fence_after();
   const uint32_t tmem = psm[0].tmem_base + static_cast<uint32_t>(grp) * 128u;
   const ChunkWs ws = chunk_ws(a.ws, slots, a.hv, DK, a.dv);
-  const int n_prep = static_cast<int>(gridDim.x) - n_chain;
   const long long units = slots * a.hv;
   uint32_t phase = 0;
   bool ok = true;
@@ -1100,16 +1111,29 @@ delta_fused_kernel(ScanArgs a, long long slots, int n_chain) {
     const long long t0 = clock64();
     while (clock64() - t0 < grp * kStaggerCycles * DK) __nanosleep(200);
   }
-  for (long long k = static_cast<long long>(grp) * n_prep + (cta - n_chain); k < units; k += 3LL * n_prep) {
+  // the unit counter, 8-byte aligned after the flags (the workspace base is
+  // 256-byte aligned and every region before it a multiple of 256 bytes)
+  unsigned long long* next = reinterpret_cast<unsigned long long*>(ws.flag + units);
+  auto group_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + 2 * grp) : "memory"); };
+  if (gtid == 0) psm[grp].next_unit = static_cast<long long>(atomicAdd(next, 1ull));
+  group_sync();
+  long long k = psm[grp].next_unit;
+  while (k < units) {
     const int x = order.slot(k / a.hv);                        // the same in every warp
     if (x < 0) break;                                          // and so are later k
     // a sequence outside the tokens (flagged by its state carry) can give a
     // slot past the workspace; no unit and no flag for it
-    if (x >= slots) continue;
-    const int h = static_cast<int>(k % a.hv);
-    delta_prep_unit<DK>(a, slots, x, h, psm[grp], gtid, tmem, phase, ok, 1 + 2 * grp);
-    // the unit ends with a barrier of the group after every thread's stores
-    if (gtid == 0) st_release_gpu(ws.flag + static_cast<long long>(x) * a.hv + h, 1);
+    if (x < slots) {
+      const int h = static_cast<int>(k % a.hv);
+      delta_prep_unit<DK>(a, slots, x, h, psm[grp], gtid, tmem, phase, ok, 1 + 2 * grp);
+      // the unit ends with a barrier of the group after every thread's stores
+      if (gtid == 0) st_release_gpu(ws.flag + static_cast<long long>(x) * a.hv + h, 1);
+    }
+    // the next unit is taken only now, so that it goes to whichever group is
+    // free first
+    if (gtid == 0) psm[grp].next_unit = static_cast<long long>(atomicAdd(next, 1ull));
+    group_sync();
+    k = psm[grp].next_unit;
   }
   tc_fence_before();
   __syncthreads();
@@ -1136,7 +1160,9 @@ static cudaError_t launch_chunked_dk(const ScanArgs& a, cudaStream_t st) {
                              static_cast<int>(fused_smem));
     if (e != cudaSuccess) return e;
     const long long n_prep = std::min<long long>(a.num_sms - n_chain, (units + 2) / 3);
-    e = cudaMemsetAsync(chunk_ws(a.ws, slots, a.hv, DK, a.dv).flag, 0, static_cast<size_t>(units) * sizeof(int), st);
+    // the flags and, after them, the unit counter
+    e = cudaMemsetAsync(chunk_ws(a.ws, slots, a.hv, DK, a.dv).flag, 0, static_cast<size_t>(units + 2) * sizeof(int),
+                        st);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(n_chain + n_prep));
