@@ -310,7 +310,14 @@ __device__ __forceinline__ void delta_prep_unit(const ScanArgs& a, long long slo
                                                                   (static_cast<long long>(t0 + t) * a.hk + kh) * DK);
   const int row = is_k ? t : 64 + t;
 
-  // 1. the norms of the k (threads 0..63) and q (64..127) rows
+  // 1. the norms of the k (threads 0..63) and q (64..127) rows; the q threads
+  //    also start their token's v row (read in step 5) on its way into L2
+  if (!is_k && valid_t) {
+    const char* vr = reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.v) +
+                                                   (static_cast<long long>(t0 + t) * a.hv + h) * dv);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(vr));              // a row is at most 256 bytes
+    if (dv > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(vr + 128));
+  }
   {
     float ss = 0.f;
 #pragma unroll 4
