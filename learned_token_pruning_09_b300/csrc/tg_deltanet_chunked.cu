@@ -481,12 +481,14 @@ __device__ __forceinline__ void delta_prep_unit(const ScanArgs& a, long long slo
   // 5. W1^T = (beta v)^T T^T (TMEM 64..127), then W2^T = (beta gamma k^)^T T^T
   //    (TMEM 0..63), each right-hand side through the buffer, column t from
   //    the rows re-read from L1/L2
-  if (!is_k) {
+  // (threads t and t + 64 share token t's row, each half of its 16-byte pieces)
+  {
     const float bt = sm.beta[t];
     const uint4* vrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) +
                                                        (static_cast<long long>(t0 + t) * a.hv + h) * dv);
+    const int p0 = is_k ? 0 : dv / 16, p1 = p0 + dv / 16;
 #pragma unroll 2
-    for (int p = 0; p < dv / 8; ++p) {
+    for (int p = p0; p < p1; ++p) {
       float f[8];
       bf16x8(valid_t ? __ldg(vrow + p) : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
@@ -496,10 +498,11 @@ __device__ __forceinline__ void delta_prep_unit(const ScanArgs& a, long long slo
   to_async();
   mma_buf(64, at, kChunk, false);
   mma_wait();
-  if (is_k) {
+  {
     const float sc = sm.beta[t] * sm.gam[t] * sm.rn[t];
+    const int p0 = is_k ? 0 : DK / 16;
 #pragma unroll 2
-    for (int p = 0; p < DK / 8; ++p) {
+    for (int p = p0; p < p0 + DK / 16; ++p) {
       float f[8];
       bf16x8(valid_t ? __ldg(krow + p) : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
