@@ -218,8 +218,8 @@ __device__ __forceinline__ void bf16x8(const uint4 u, float (&f)[8]) {
 // of 128 threads (tid 0..127, four whole warps aligned to a multiple of four)
 // that owns `sm`, the TMEM columns tmem .. tmem + 127, the mbarrier sm.bar
 // (its phase count in `phase`, carried from unit to unit) and the named
-// barriers bar_id (the group) and bar_id + 1 (its first two warps).  A slot
-// that holds no chunk returns at once (the same for the whole group).
+// barrier bar_id (the group).  A slot that holds no chunk returns at once (the
+// same for the whole group).
 template <int DK>
 __device__ __forceinline__ void delta_prep_unit(const ScanArgs& a, long long slots, int x, int h, PrepSmem<DK>& sm,
                                              int tid, uint32_t tmem, uint32_t& phase, bool& ok, int bar_id) {
@@ -404,73 +404,81 @@ __device__ __forceinline__ void delta_prep_unit(const ScanArgs& a, long long slo
   //    the diagonal blocks T11 = (I + A11)^-1 and T22 = (I + A22)^-1 by
   //    forward substitution, T_i = e_i - sum_{j<i} A_ij T_j (warps 0 and 1 at
   //    the same time, one column per lane, in registers); then Y = T22 A21
-  //    (warp 1, one column per lane) and T21 = -Y T11 (warp 0); T12 = 0.  The
-  //    scratch for T22 and Y is the (free) buffer.
-  if (warp < 2) {
-    float (*tsc)[36] = reinterpret_cast<float(*)[36]>(sm.buf);
-    float (*ysc)[36] = reinterpret_cast<float(*)[36]>(sm.buf + 32 * 36 * 4);
+  //    (warps 1 and 3, 16 rows each) and T21 = -Y T11 (warps 0 and 2); T12 = 0.
+  //    The scratch for T11, T22 and Y is the (free) buffer.
+  {
+    float (*t11)[36] = reinterpret_cast<float(*)[36]>(sm.buf);
+    float (*tsc)[36] = reinterpret_cast<float(*)[36]>(sm.buf + 32 * 36 * 4);
+    float (*ysc)[36] = reinterpret_cast<float(*)[36]>(sm.buf + 2 * 32 * 36 * 4);
     const int k = lane;
-    const int o = warp * 32;               // the block's first row and column
     const float* A = reinterpret_cast<const float*>(sm.at);
-    float tc[32];
+    if (warp < 2) {
+      const int o = warp * 32;             // the block's first row and column
+      float tc[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) tc[i] = 0.f;
+      for (int i = 0; i < 32; ++i) tc[i] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float s0 = (i == k) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-      for (int j4 = 0; j4 < (i + 3) / 4; ++j4) {
-        const float4 av = *reinterpret_cast<const float4*>(A + (o + i) * kAStride + o + 4 * j4);
-        s0 = fmaf(-av.x, tc[4 * j4], s0);
-        s1 = fmaf(-av.y, tc[4 * j4 + 1], s1);
-        s2 = fmaf(-av.z, tc[4 * j4 + 2], s2);
-        s3 = fmaf(-av.w, tc[4 * j4 + 3], s3);
-      }
-      tc[i] = (s0 + s1) + (s2 + s3);
-    }
-    if (warp == 1) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) tsc[i][k] = tc[i];        // T22, [row][column]
-      __syncwarp();
-      // Y = T22 A21, column k: A21's column in registers, T22's rows broadcast
-#pragma unroll
-      for (int m = 0; m < 32; ++m) tc[m] = A[(32 + m) * kAStride + k];
-#pragma unroll 1
       for (int i = 0; i < 32; ++i) {
+        float s0 = (i == k) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int j4 = 0; j4 < (i + 3) / 4; ++j4) {
+          const float4 av = *reinterpret_cast<const float4*>(A + (o + i) * kAStride + o + 4 * j4);
+          s0 = fmaf(-av.x, tc[4 * j4], s0);
+          s1 = fmaf(-av.y, tc[4 * j4 + 1], s1);
+          s2 = fmaf(-av.z, tc[4 * j4 + 2], s2);
+          s3 = fmaf(-av.w, tc[4 * j4 + 3], s3);
+        }
+        tc[i] = (s0 + s1) + (s2 + s3);
+      }
+      float (*dst)[36] = warp == 0 ? t11 : tsc;   // [row][column]
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dst[i][k] = tc[i];
+    }
+    gbar();                                 // T11 and T22 in the scratch
+    const int i0 = (warp >> 1) * 16;        // this warp's 16 rows of Y or T21
+    if (warp & 1) {
+      // Y = T22 A21, column k: A21's column in registers, T22's rows broadcast
+      float ac[32];
+#pragma unroll
+      for (int m = 0; m < 32; ++m) ac[m] = A[(32 + m) * kAStride + k];
+#pragma unroll 1
+      for (int i = i0; i < i0 + 16; ++i) {
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
         for (int m4 = 0; m4 < 8; ++m4) {
           const float4 tv = *reinterpret_cast<const float4*>(&tsc[i][4 * m4]);
-          s0 = fmaf(tv.x, tc[4 * m4], s0);
-          s1 = fmaf(tv.y, tc[4 * m4 + 1], s1);
-          s2 = fmaf(tv.z, tc[4 * m4 + 2], s2);
-          s3 = fmaf(tv.w, tc[4 * m4 + 3], s3);
+          s0 = fmaf(tv.x, ac[4 * m4], s0);
+          s1 = fmaf(tv.y, ac[4 * m4 + 1], s1);
+          s2 = fmaf(tv.z, ac[4 * m4 + 2], s2);
+          s3 = fmaf(tv.w, ac[4 * m4 + 3], s3);
         }
         ysc[i][k] = (s0 + s1) + (s2 + s3);
       }
     }
-    asm volatile("bar.sync %0, 64;" ::"r"(bar_id + 1) : "memory");   // Y and T22 in the scratch; A is read
-    if (warp == 0) {
-      // T21 = -Y T11 (column k of T11 in registers) and T11 into the T tile
+    gbar();                                 // Y complete; A is read, so T may overwrite it
+    if (!(warp & 1)) {
+      // T21 = -Y T11 (column k of T11 in registers), and T11's rows i0..i0+15
+      float tk[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) tk[j] = t11[j][k];
 #pragma unroll 1
-      for (int i = 0; i < 32; ++i) {
+      for (int i = i0; i < i0 + 16; ++i) {
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
           const float4 yv = *reinterpret_cast<const float4*>(&ysc[i][4 * j4]);
-          s0 = fmaf(-yv.x, tc[4 * j4], s0);
-          s1 = fmaf(-yv.y, tc[4 * j4 + 1], s1);
-          s2 = fmaf(-yv.z, tc[4 * j4 + 2], s2);
-          s3 = fmaf(-yv.w, tc[4 * j4 + 3], s3);
+          s0 = fmaf(-yv.x, tk[4 * j4], s0);
+          s1 = fmaf(-yv.y, tk[4 * j4 + 1], s1);
+          s2 = fmaf(-yv.z, tk[4 * j4 + 2], s2);
+          s3 = fmaf(-yv.w, tk[4 * j4 + 3], s3);
         }
         *reinterpret_cast<float*>(sm.at + sw_off(kChunk, 32 + i, k)) = to_tf32((s0 + s1) + (s2 + s3));
+        *reinterpret_cast<float*>(sm.at + sw_off(kChunk, i, k)) = to_tf32(t11[i][k]);
       }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) *reinterpret_cast<float*>(sm.at + sw_off(kChunk, i, k)) = to_tf32(tc[i]);
     } else {
-      // T22 and T12 = 0
+      // T22's rows i0..i0+15, and T12 = 0
 #pragma unroll 1
-      for (int i = 0; i < 32; ++i) {
+      for (int i = i0; i < i0 + 16; ++i) {
         *reinterpret_cast<float*>(sm.at + sw_off(kChunk, 32 + i, 32 + k)) = to_tf32(tsc[i][k]);
         *reinterpret_cast<float*>(sm.at + sw_off(kChunk, i, 32 + k)) = 0.f;
       }
