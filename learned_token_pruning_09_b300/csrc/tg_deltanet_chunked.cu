@@ -653,6 +653,7 @@ struct ChainSmem {
   alignas(1024) uint8_t kd[2][DK * kChunk * 4];    // Kd^T images
   alignas(16) uint16_t ostage[2][kChunk * 128];    // a chunk's bf16 outputs, [token][value row]
   uint64_t bq_full[2], kd_full[2], bq_empty[2], kd_empty[2], a1_done, a3_done[2], d_free[2], u_ready, init_ready, fin;
+  uint64_t seen[8];                 // one-launch form: chunk c's unit seen complete by the copy issuer (slot c % 8)
   uint32_t tmem_base;
   int abort;
 };
@@ -679,13 +680,18 @@ __device__ __forceinline__ void delta_chain_cta(const ScanArgs& a, long long slo
   const ChunkWs ws = chunk_ws(a.ws, slots, a.hv, DK, dv);
   const long long wd = a.watchdog;
   constexpr uint32_t kBqBytes = 128 * DK * 4, kKdBytes = DK * kChunk * 4;
-  // chunk c's unit is complete: by one thread (the copy issuer) or, with
-  // warp_all, by a whole warp, each lane with its own acquire, the result
-  // the same in every lane
+  // chunk c's unit is complete.  The copy issuer polls the unit's flag (an
+  // acquire at GPU scope) and then arrives on seen[c % 8]; the state and
+  // output warps wait on that barrier (whole warps, the verdict the same in
+  // every lane), which orders their loads of the unit after its stores
+  // without a round trip to L2 on their path.  The issuer runs at most four
+  // chunks ahead of the slowest of them (its copies of chunk c wait for the
+  // output warps' release of chunk c - 4), so eight slots never alias.
   auto ready = [&](int c, bool warp_all) -> bool {
     if (!fused) return true;
-    const bool r = flag_wait(ws.flag + (slot0 + c) * a.hv + h, wd, a.status);
-    return warp_all ? __all_sync(0xffffffffu, r) : r;
+    if (!warp_all) return flag_wait(ws.flag + (slot0 + c) * a.hv + h, wd, a.status);
+    const bool r = mbar_wait(&sm.seen[c & 7], static_cast<uint32_t>(c >> 3) & 1u, wd, a.status, kStatusTimeout);
+    return __all_sync(0xffffffffu, r);
   };
 
   if (tid == 0) {
@@ -701,6 +707,7 @@ __device__ __forceinline__ void delta_chain_cta(const ScanArgs& a, long long slo
     mbar_init(&sm.u_ready, 4);
     mbar_init(&sm.init_ready, 4);
     mbar_init(&sm.fin, 1);
+    for (int s8 = 0; s8 < 8; ++s8) mbar_init(&sm.seen[s8], 1);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -729,7 +736,10 @@ __device__ __forceinline__ void delta_chain_cta(const ScanArgs& a, long long slo
           sm.abort = 1;
           break;
         }
-        if (fused) fence_proxy_async_global();
+        if (fused) {
+          fence_proxy_async_global();
+          mbar_arrive(&sm.seen[c & 7]);
+        }
         if (c >= 2 && !mbar_wait(&sm.bq_empty[s], ((c >> 1) - 1) & 1, wd, a.status, kStatusTimeout)) {
           sm.abort = 1;
           break;
