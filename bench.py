@@ -218,7 +218,7 @@ def measure_deltanet(dev, flush, steps, peaks, name="deltanet-32k-k4096"):
     ws = torch.empty(tg.tg_gated_delta_scan_workspace_size(t, nb, cfg["hv"], cfg["dk"], cfg["dv"]),
                      dtype=torch.uint8, device=dev)
 
-    def timed(chunked):
+    def timed(chunked, cu=cu, ws=ws):
         call = lambda: tg.tg_gated_delta_scan(q, k, v, g, beta, cu, o=o, workspace=ws, chunked=chunked)
         call()
         torch.cuda.synchronize()
@@ -231,11 +231,22 @@ def measure_deltanet(dev, flush, steps, peaks, name="deltanet-32k-k4096"):
 
     us = timed(True)
     us_token = timed(False)
+    # the same chunks as two launches: padded with empty sequences to more
+    # (sequence, head) pairs than the one-launch form takes on any GPU up to
+    # 320 SMs; the empty sequences do no work
+    n_pad = 160 // cfg["hv"] + 1
+    cu_pad = torch.as_tensor(np.concatenate([inp["cu_kept"], np.full(n_pad, t)]).astype(np.int32)).to(dev)
+    ws_pad = torch.empty(tg.tg_gated_delta_scan_workspace_size(t, nb + n_pad, cfg["hv"], cfg["dk"], cfg["dv"]),
+                         dtype=torch.uint8, device=dev)
+    us_two = timed(True, cu_pad, ws_pad)
     byts = deltanet_bytes(t, cfg["hk"], cfg["hv"], cfg["dk"], cfg["dv"])
     return {"workload": name, "tokens": t, "hk": cfg["hk"], "hv": cfg["hv"], "dk": cfg["dk"], "dv": cfg["dv"],
             "form": "chunked (tf32 tensor cores, workspace); per-chunk products and state carry in one cooperative launch when batch x hv <= SMs / 2", "us": us, "gbs": byts / (us * 1e-6) / 1e9,
             "bytes": byts, "frac_of_measured_hbm": byts / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
-            "workspace_bytes": int(ws.numel()), "token_by_token_us": us_token}
+            "workspace_bytes": int(ws.numel()), "token_by_token_us": us_token,
+            "two_launch_us": us_two,
+            "two_launch": "the same chunks in two launches (per-chunk products, then the state carry), forced by "
+                          "padding with empty sequences"}
 
 
 def max_over_ranks(values, device):
