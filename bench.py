@@ -98,16 +98,18 @@ def measure_masked(P, shape, flush, steps):
     ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
 
     def calls_plain(n_kept):
-        tg.tg_gate_score_masked(P.X, mask, P.W1, None, P.W2, P.b2, s_out=s)
-        tg.tg_topk_select_masked(s, P.cu, mask, P.kk, max_len, kept_idx=kept, cu_kept=cu_kept, n_prunable=n_prun)
+        tg.tg_gate_score_masked(P.X, mask, P.W1, None, P.W2, P.b2, s_out=s, cu_seqlens=P.cu, topk_ws=P.topk_ws)
+        tg.tg_topk_select_masked(s, P.cu, mask, P.kk, max_len, kept_idx=kept, cu_kept=cu_kept, n_prunable=n_prun,
+                                 workspace=P.topk_ws)
         tg.tg_gather_kept(P.X, s, P.cu, kept[:n_kept], cu_kept, n_kept, x_kept=P.xk_masked[:n_kept],
                           pos_kept=P.pos_masked[:n_kept], s_kept=P.s_masked[:n_kept])
 
     def calls(n_kept):
         ev[0].record()
-        tg.tg_gate_score_masked(P.X, mask, P.W1, None, P.W2, P.b2, s_out=s)
+        tg.tg_gate_score_masked(P.X, mask, P.W1, None, P.W2, P.b2, s_out=s, cu_seqlens=P.cu, topk_ws=P.topk_ws)
         ev[1].record()
-        tg.tg_topk_select_masked(s, P.cu, mask, P.kk, max_len, kept_idx=kept, cu_kept=cu_kept, n_prunable=n_prun)
+        tg.tg_topk_select_masked(s, P.cu, mask, P.kk, max_len, kept_idx=kept, cu_kept=cu_kept, n_prunable=n_prun,
+                                 workspace=P.topk_ws)
         ev[2].record()
         tg.tg_gather_kept(P.X, s, P.cu, kept[:n_kept], cu_kept, n_kept, x_kept=P.xk_masked[:n_kept],
                           pos_kept=P.pos_masked[:n_kept], s_kept=P.s_masked[:n_kept])

@@ -155,7 +155,11 @@ TG_API tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* c
  * the results of tg_gate_score and tg_topk_select.
  *
  * tg_gate_score_masked: as tg_gate_score, with s = 0 on rows outside the
- *   mask; no sequence arguments (the mask is per row).
+ *   mask.  The sequence arguments serve only the top-K workspace: with
+ *   topk_ws (tg_topk_workspace_size(batch) bytes, zero on entry, as for
+ *   tg_gate_score) the gate also counts each sequence's prunable scores for
+ *   the masked top-K's first two radix digits, and needs cu_seqlens [batch+1]
+ *   and batch >= 1; with topk_ws NULL both are ignored.
  *
  * tg_topk_select_masked: per sequence b, the min(k[b], n_prunable[b])
  *   prunable rows with the largest score (ties: lower row first) together with
@@ -166,6 +170,9 @@ TG_API tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* c
  *                  past it writes nothing and sets TG_ERR_DEVICE_INDEX
  *   n_prunable     [batch] int32 output: prunable rows per sequence (also the
  *                  call's scratch: written by a counting kernel, then read)
+ *   workspace      NULL, or the top-K workspace a tg_gate_score_masked call
+ *                  with the same cu_seqlens filled (its first two digits come
+ *                  from there; cleared again for the next gate call)
  *   The total kept count is cu_kept[batch] = sum_b min(k[b], n_prunable[b]) +
  *   (length_b - n_prunable[b]); a caller that does not know the mask on the
  *   host can size kept_idx by n_rows.
@@ -173,11 +180,13 @@ TG_API tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* c
 TG_API tg_status tg_gate_score_masked(const void* x_bf16, int64_t n_rows, int32_t d,
                                const uint8_t* prunable, const void* w1_bf16,
                                const float* b1, const void* w2_bf16, float b2, int32_t h,
-                               float* s_out, cudaStream_t stream);
+                               float* s_out, const int32_t* cu_seqlens, int32_t batch, void* topk_ws,
+                               size_t topk_ws_bytes, cudaStream_t stream);
 TG_API tg_status tg_topk_select_masked(const float* s, int64_t n_rows, const int32_t* cu_seqlens,
                                 const uint8_t* prunable, const int32_t* k, int32_t batch,
                                 int32_t max_len, int64_t kept_capacity, int32_t* kept_idx,
-                                int32_t* cu_kept, int32_t* n_prunable, cudaStream_t stream);
+                                int32_t* cu_kept, int32_t* n_prunable, void* workspace,
+                                size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Gather of the kept rows (third phase: the layers above L run on the kept

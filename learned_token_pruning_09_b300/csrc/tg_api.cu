@@ -153,6 +153,8 @@ static tg_status gate_score_any(const void* x_bf16, int64_t n_rows, int32_t d, c
   if (h < 16 || h > 256 || h % 16 != 0) return fail(TG_ERR_INVALID_ARG, "h must be a multiple of 16 in [16, 256]");
   if ((!masked && (!cu_seqlens || !n_doc)) || !w1_bf16 || !w2_bf16)
     return fail(TG_ERR_INVALID_ARG, "null pointer argument");
+  if (masked && topk_ws && (!cu_seqlens || batch < 1))
+    return fail(TG_ERR_INVALID_ARG, "a top-K workspace needs cu_seqlens and batch >= 1");
   if (n_rows == 0) return ok();
   if (masked && !prunable) return fail(TG_ERR_INVALID_ARG, "null prunable mask");
   if (!x_bf16 || !s_out) return fail(TG_ERR_INVALID_ARG, "null pointer argument");
@@ -218,9 +220,11 @@ tg_status tg_gate_score(const void* x_bf16, int64_t n_rows, int32_t d, const int
 
 tg_status tg_gate_score_masked(const void* x_bf16, int64_t n_rows, int32_t d, const uint8_t* prunable,
                                const void* w1_bf16, const float* b1, const void* w2_bf16, float b2, int32_t h,
-                               float* s_out, cudaStream_t stream) {
-  return gate_score_any(x_bf16, n_rows, d, nullptr, nullptr, 0, true, prunable, w1_bf16, b1, w2_bf16, b2, h, s_out,
-                        nullptr, 0, stream);
+                               float* s_out, const int32_t* cu_seqlens, int32_t batch, void* topk_ws,
+                               size_t topk_ws_bytes, cudaStream_t stream) {
+  if (!topk_ws) { cu_seqlens = nullptr; batch = 0; }
+  return gate_score_any(x_bf16, n_rows, d, cu_seqlens, nullptr, batch, true, prunable, w1_bf16, b1, w2_bf16, b2, h,
+                        s_out, topk_ws, topk_ws_bytes, stream);
 }
 
 tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* cu_seqlens, const int32_t* n_doc,
@@ -261,8 +265,16 @@ tg_status tg_topk_select(const float* s, int64_t n_rows, const int32_t* cu_seqle
 
 tg_status tg_topk_select_masked(const float* s, int64_t n_rows, const int32_t* cu_seqlens, const uint8_t* prunable,
                                 const int32_t* k, int32_t batch, int32_t max_len, int64_t kept_capacity,
-                                int32_t* kept_idx, int32_t* cu_kept, int32_t* n_prunable, cudaStream_t stream) {
+                                int32_t* kept_idx, int32_t* cu_kept, int32_t* n_prunable, void* workspace,
+                                size_t ws_bytes, cudaStream_t stream) {
   if (batch < 0 || batch > (1 << 24)) return fail(TG_ERR_INVALID_ARG, "batch out of range");
+  if (batch > 0 && workspace) {
+    if (batch > kTopkMaxHistBatch) return fail(TG_ERR_INVALID_ARG, "a top-K workspace needs batch <= %d", kTopkMaxHistBatch);
+    if (ws_bytes < tg_topk_workspace_size(batch))
+      return fail(TG_ERR_WORKSPACE, "top-K workspace of %zu bytes needed, %zu given", tg_topk_workspace_size(batch),
+                  ws_bytes);
+    if (!aligned16(workspace)) return fail(TG_ERR_INVALID_ARG, "top-K workspace must be 16-byte aligned");
+  }
   if (n_rows < 0 || n_rows > 0x7FFFFFFF) return fail(TG_ERR_INVALID_ARG, "n_rows out of range");
   if (max_len < 0) return fail(TG_ERR_INVALID_ARG, "max_len must be >= 0");
   if (kept_capacity < 0) return fail(TG_ERR_INVALID_ARG, "kept_capacity must be >= 0");
@@ -276,6 +288,7 @@ tg_status tg_topk_select_masked(const float* s, int64_t n_rows, const int32_t* c
   cudaError_t e = launch_topk_count(prunable, cu_seqlens, batch, n_prunable, di->status, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prunable count kernel launch");
   TopkArgs a{};
+  a.hist = static_cast<uint32_t*>(workspace);
   a.s = s;
   a.cu_seqlens = cu_seqlens;
   a.n_doc = n_prunable;

@@ -169,12 +169,18 @@ struct GateTail {
 };
 
 // Whether `row` is a document row; *seq = its sequence.
-__device__ __forceinline__ bool row_is_doc(const GateArgs& a, long long row, int* seq) {
+// the sequence of a row: the largest b with cu_seqlens[b] <= row
+__device__ __forceinline__ int seq_of_row(const GateArgs& a, long long row) {
   int lo = 0, hi = a.batch - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (__ldg(a.cu_seqlens + mid) <= row) lo = mid; else hi = mid - 1;
   }
+  return lo;
+}
+
+__device__ __forceinline__ bool row_is_doc(const GateArgs& a, long long row, int* seq) {
+  const int lo = seq_of_row(a, row);
   *seq = lo;
   const int start = __ldg(a.cu_seqlens + lo);
   const int nd = __ldg(a.n_doc + lo);
@@ -331,7 +337,13 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
         z += a.b2;
         // logsigmoid(z) = -log1p(exp(-z)) (z >= 0), z - log1p(exp(z)) (z < 0)
         sc = (z >= 0.0f) ? -log1pf(expf(-z)) : z - log1pf(expf(z));
-        const bool prun = a.prunable ? __ldg(a.prunable + row) != 0 : row_is_doc(a, row, &seq);
+        bool prun;
+        if (a.prunable) {
+          prun = __ldg(a.prunable + row) != 0;
+          if (prun && a.hist) seq = seq_of_row(a, row);   // the histograms are per sequence
+        } else {
+          prun = row_is_doc(a, row, &seq);
+        }
         a.s_out[row] = prun ? sc : 0.0f;
         counted = prun;
       }

@@ -51,8 +51,8 @@ _SIGS = {
     "tg_gate_score": [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _f32, _i32, _vp, _vp, _sz, _vp],
     "tg_topk_workspace_size": [_i32],
     "tg_topk_select": [_vp, _i64, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _sz, _vp],
-    "tg_gate_score_masked": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _f32, _i32, _vp, _vp],
-    "tg_topk_select_masked": [_vp, _i64, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
+    "tg_gate_score_masked": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _f32, _i32, _vp, _vp, _i32, _vp, _sz, _vp],
+    "tg_topk_select_masked": [_vp, _i64, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _sz, _vp],
     "tg_gather_kept": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp],
     "tg_gated_attention_fwd": [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _i32, _i64, _i32, _i32, _i32,
                                _i32, _vp, _vp, _vp, _vp, _sz, _vp],
@@ -198,9 +198,12 @@ def tg_topk_select(s: torch.Tensor, cu_seqlens: torch.Tensor, n_doc: torch.Tenso
 
 def tg_gate_score_masked(x: torch.Tensor, prunable: torch.Tensor, w1: torch.Tensor, b1: Optional[torch.Tensor],
                          w2: torch.Tensor, b2: float, s_out: Optional[torch.Tensor] = None,
+                         cu_seqlens: Optional[torch.Tensor] = None, topk_ws: Optional[torch.Tensor] = None,
                          stream=None) -> torch.Tensor:
     """Gate scores s [n_rows] fp32 on the rows of a per-row prunable mask
-    (uint8 [n_rows], nonzero = prunable), 0 on every other row."""
+    (uint8 [n_rows], nonzero = prunable), 0 on every other row.  With
+    ``topk_ws`` (and ``cu_seqlens``) the gate also counts the masked top-K's
+    first two radix digits per sequence."""
     _need(x, torch.bfloat16, "x", 2)
     _need(prunable, torch.uint8, "prunable", 1)
     _need(w1, torch.bfloat16, "w1", 2)
@@ -214,18 +217,27 @@ def tg_gate_score_masked(x: torch.Tensor, prunable: torch.Tensor, w1: torch.Tens
     if s_out is None:
         s_out = torch.empty(n_rows, dtype=torch.float32, device=x.device)
     _need(s_out, torch.float32, "s_out", 1)
+    batch = 0
+    if topk_ws is not None:
+        if cu_seqlens is None:
+            raise ValueError("topk_ws needs cu_seqlens")
+        _need(cu_seqlens, torch.int32, "cu_seqlens", 1)
+        batch = cu_seqlens.shape[0] - 1
     _check(lib.tg_gate_score_masked(_ptr(x), n_rows, d, _ptr(prunable), _ptr(w1), _ptr(b1), _ptr(w2), float(b2), h,
-                                    _ptr(s_out), _stream(stream)), "tg_gate_score_masked")
+                                    _ptr(s_out), _ptr(cu_seqlens if topk_ws is not None else None), batch,
+                                    _ptr(topk_ws), topk_ws.numel() if topk_ws is not None else 0, _stream(stream)),
+           "tg_gate_score_masked")
     return s_out
 
 
 def tg_topk_select_masked(s: torch.Tensor, cu_seqlens: torch.Tensor, prunable: torch.Tensor, k: torch.Tensor,
                           max_len: int, kept_capacity: Optional[int] = None, kept_idx: Optional[torch.Tensor] = None,
                           cu_kept: Optional[torch.Tensor] = None, n_prunable: Optional[torch.Tensor] = None,
-                          stream=None):
+                          workspace: Optional[torch.Tensor] = None, stream=None):
     """(kept_idx, cu_kept, n_prunable) with general prunable spans.  kept_idx
     has ``kept_capacity`` entries (default n_rows); its first cu_kept[batch]
-    entries are the kept rows."""
+    entries are the kept rows.  ``workspace``: the top-K workspace a
+    tg_gate_score_masked call filled (its first two digits come from there)."""
     _need(s, torch.float32, "s", 1)
     _need(prunable, torch.uint8, "prunable", 1)
     for t, nme in ((cu_seqlens, "cu_seqlens"), (k, "k")):
@@ -243,7 +255,8 @@ def tg_topk_select_masked(s: torch.Tensor, cu_seqlens: torch.Tensor, prunable: t
         n_prunable = torch.empty(batch, dtype=torch.int32, device=s.device)
     _check(lib.tg_topk_select_masked(_ptr(s), n_rows, _ptr(cu_seqlens), _ptr(prunable), _ptr(k), batch,
                                      int(max_len), kept_idx.shape[0], _ptr(kept_idx), _ptr(cu_kept),
-                                     _ptr(n_prunable), _stream(stream)), "tg_topk_select_masked")
+                                     _ptr(n_prunable), _ptr(workspace), workspace.numel() if workspace is not None else 0,
+                                     _stream(stream)), "tg_topk_select_masked")
     return kept_idx, cu_kept, n_prunable
 
 

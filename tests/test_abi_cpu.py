@@ -86,14 +86,14 @@ def test_host_validation_rejects_before_launch(tg):
     assert L.tg_gate_score(p, 10, 64, p, p, 3, p, None, p, 0.0, 64, p, p, ws - 4, None) == tg.TG_ERR_WORKSPACE
     assert L.tg_gate_score(p, 10, 64, p, p, 3, p, None, p, 0.0, 64, p, _c(264), ws, None) == tg.TG_ERR_INVALID_ARG
     # general prunable spans
-    assert L.tg_gate_score_masked(p, 10, 64, None, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_gate_score_masked(p, 10, 63, p, p, None, p, 0.0, 64, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_gate_score_masked(p, 0, 64, None, p, None, p, 0.0, 64, p, None) == tg.TG_OK
-    assert L.tg_topk_select_masked(p, 10, p, p, p, 1, -1, 10, p, p, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_topk_select_masked(p, 10, p, p, p, 1, 10, -1, p, p, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_topk_select_masked(p, 10, p, None, p, 1, 10, 10, p, p, p, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_topk_select_masked(p, 10, p, p, p, 1, 10, 10, p, p, None, None) == tg.TG_ERR_INVALID_ARG
-    assert L.tg_topk_select_masked(p, 10, p, p, p, 0, 10, 10, p, p, p, None) == tg.TG_OK     # empty batch
+    assert L.tg_gate_score_masked(p, 10, 64, None, p, None, p, 0.0, 64, p, None, 0, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score_masked(p, 10, 63, p, p, None, p, 0.0, 64, p, None, 0, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_gate_score_masked(p, 0, 64, None, p, None, p, 0.0, 64, p, None, 0, None, 0, None) == tg.TG_OK
+    assert L.tg_topk_select_masked(p, 10, p, p, p, 1, -1, 10, p, p, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select_masked(p, 10, p, p, p, 1, 10, -1, p, p, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select_masked(p, 10, p, None, p, 1, 10, 10, p, p, p, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select_masked(p, 10, p, p, p, 1, 10, 10, p, p, None, None, 0, None) == tg.TG_ERR_INVALID_ARG
+    assert L.tg_topk_select_masked(p, 10, p, p, p, 0, 10, 10, p, p, p, None, 0, None) == tg.TG_OK     # empty batch
     # gather
     assert L.tg_gather_kept(p, 10, 12, p, p, p, p, 1, 4, p, p, p, None) == tg.TG_ERR_INVALID_ARG
     assert L.tg_gather_kept(p, 10, 64, p, p, None, p, 1, 4, p, p, p, None) == tg.TG_ERR_INVALID_ARG

@@ -169,3 +169,29 @@ def test_masked_chain_keeps_the_oracle_set(tg):
     np.testing.assert_array_equal(xk.cpu().view(torch.int16).numpy().view(np.uint16), np.asarray(x)[k_np])
     b_of = np.searchsorted(cu, k_np, side="right") - 1
     np.testing.assert_array_equal(pos.cpu().numpy(), k_np - cu[b_of])
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3-1.7b-16k", "ragged-8"])
+def test_masked_chain_with_the_gate_histograms(tg, name):
+    """With the top-K workspace, the masked gate counts each sequence's
+    prunable scores and the masked top-K starts from those digits: the same
+    scores and the same kept rows, bit for bit, as without the workspace;
+    the workspace is zero again afterwards, and a second round gives the same."""
+    shape = synth.ALL_SHAPES[name]()
+    x, p = synth.residuals(shape), synth.gate_weights(shape)
+    mask = synth.prunable_spans(shape)
+    cu = np.asarray(shape.cu_seqlens, np.int32)
+    max_len = int(np.diff(cu).max())
+    X, W1, W2, M, CU, K = dev_bf16(x), dev_bf16(p["w1"]), dev_bf16(p["w2"]), dev_u8(mask), dev_i32(cu), dev_i32(shape.k)
+    s0 = tg.tg_gate_score_masked(X, M, W1, None, W2, p["b2"])
+    kept0, cu0, _ = tg.tg_topk_select_masked(s0, CU, M, K, max_len)
+    ws = tg.tg_topk_workspace(len(cu) - 1)
+    for _ in range(2):
+        s1 = tg.tg_gate_score_masked(X, M, W1, None, W2, p["b2"], cu_seqlens=CU, topk_ws=ws)
+        kept1, cu1, _ = tg.tg_topk_select_masked(s1, CU, M, K, max_len, workspace=ws)
+        assert tg.tg_check_device_status() == tg.TG_OK
+        assert torch.equal(s0, s1)
+        assert torch.equal(cu0, cu1)
+        n = int(cu0[-1])
+        assert torch.equal(kept0[:n], kept1[:n])
+        assert not torch.any(ws)
