@@ -101,3 +101,23 @@ def test_chunked_delta_scan_wait_runs_out_then_recovers(tg):
     ref, _ = oracle.gated_delta_scan(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_kept"])
     ok, err, _ = allclose_report(host_f64(o), ref, 2e-4, 2.0 ** -8)
     assert ok, err
+
+
+def test_chunked_delta_scan_two_launches_wait_runs_out_then_recovers(tg):
+    """The same for the two-launch form of the chunked scan (the input padded
+    with empty sequences to more (sequence, head) pairs than one launch takes
+    on any GPU up to 320 SMs)."""
+    d = synth.deltanet_inputs("deltanet-tiny")
+    t, hv = d["v"].shape[0], d["v"].shape[1]
+    cu = np.concatenate([d["cu_kept"], np.full(160 // hv + 1, t)]).astype(np.int32)
+    args = (dev_bf16(d["q"]), dev_bf16(d["k"]), dev_bf16(d["v"]), dev_f32(d["g"]), dev_f32(d["beta"]), dev_i32(cu))
+    tg.tg_check_device_status()
+    tg.tg_set_watchdog_cycles(200)
+    tg.tg_gated_delta_scan(*args, chunked=True)
+    assert tg.tg_check_device_status() == tg.TG_ERR_TIMEOUT
+    tg.tg_set_watchdog_cycles(0)
+    o = tg.tg_gated_delta_scan(*args, chunked=True)
+    assert tg.tg_check_device_status() == tg.TG_OK
+    ref, _ = oracle.gated_delta_scan(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_kept"])
+    ok, err, _ = allclose_report(host_f64(o), ref, 2e-4, 2.0 ** -8)
+    assert ok, err
