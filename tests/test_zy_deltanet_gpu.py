@@ -272,3 +272,15 @@ def test_scan_chunked_workspace_contents_do_not_matter(tg):
     assert tg.tg_check_device_status() == tg.TG_OK
     assert torch.equal(o1, o2) and torch.equal(o1, o3)
     assert torch.equal(s1, s2) and torch.equal(s1, s3)
+
+
+def test_scan_chunked_dk64_at_scale(tg):
+    """dk = dv = 64 on two sequences of ~4k tokens in all, 32 value heads over
+    8 q/k heads (64 (sequence, head) pairs: the one-launch form with dk = 64
+    at a size that keeps every SM busy), against the oracle."""
+    rng = np.random.default_rng(64)
+    lens = [2000, 2100]
+    d = _random_scan_inputs(rng, lens, 8, 32, 64, 64)
+    o, s = run_scan(tg, d, True)
+    ref_o, ref_s = oracle.gated_delta_scan(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_kept"])
+    check(o, s, ref_o, ref_s, "dk 64 at scale", True)
