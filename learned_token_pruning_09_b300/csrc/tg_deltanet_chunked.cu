@@ -400,6 +400,15 @@ __device__ __forceinline__ void delta_prep_unit(const ScanArgs& a, long long slo
   }
   tc_fence_before();
   gbar();
+  // this thread's half of its token's v row (read again in step 5), loaded
+  // now so that the loads overlap the T solve
+  const uint4* vrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) +
+                                                     (static_cast<long long>(t0 + t) * a.hv + h) * dv);
+  const int vp0 = is_k ? 0 : dv / 16;
+  uint4 vpiece[8];                          // dv / 16 <= 8 pieces
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    vpiece[i] = (i < dv / 16 && valid_t) ? __ldg(vrow + vp0 + i) : make_uint4(0, 0, 0, 0);
   // 4. T = (I + A)^-1 in 2 x 2 blocks of 32 (A strictly lower triangular):
   //    the diagonal blocks T11 = (I + A11)^-1 and T22 = (I + A22)^-1 by
   //    forward substitution, T_i = e_i - sum_{j<i} A_ij T_j (warps 0 and 1 at
@@ -492,15 +501,15 @@ __device__ __forceinline__ void delta_prep_unit(const ScanArgs& a, long long slo
   // (threads t and t + 64 share token t's row, each half of its 16-byte pieces)
   {
     const float bt = sm.beta[t];
-    const uint4* vrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) +
-                                                       (static_cast<long long>(t0 + t) * a.hv + h) * dv);
-    const int p0 = is_k ? 0 : dv / 16, p1 = p0 + dv / 16;
-#pragma unroll 2
-    for (int p = p0; p < p1; ++p) {
-      float f[8];
-      bf16x8(valid_t ? __ldg(vrow + p) : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) *reinterpret_cast<float*>(sm.buf + sw_off(128, 8 * p + e, t)) = to_tf32(bt * f[e]);
+    for (int i = 0; i < 8; ++i) {
+      if (i < dv / 16) {
+        const int p = vp0 + i;
+        float f[8];
+        bf16x8(vpiece[i], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) *reinterpret_cast<float*>(sm.buf + sw_off(128, 8 * p + e, t)) = to_tf32(bt * f[e]);
+      }
     }
   }
   to_async();
